@@ -1,0 +1,388 @@
+// Batch-1 kernels (ntok == 1) for the packed formats and the no-weights
+// control.  One lane owns one output row; a warp owns 32 rows of one
+// 256-column slice (an "item").  CTAs take contiguous, equal shares of the
+// items in slice-major order and keep the x-dependent tables of the current
+// slice in shared memory; per-slice partial sums are reduced in a fixed order
+// by the last warp of each row block (q2::arrive / q2::gather).
+//
+// BPDQ and Leech use subset-sum tables in place of a per-weight decode: for
+// each 8-column byte of a bit-plane the table holds the sum of the x values
+// the byte selects, so one shared-memory load covers 8 weights of a plane.
+// This is the "multiply without dequantising" formulation of
+// "Qwen3-8B -- 2-bit BPDQ (packed)", Kernels (c0*S0 + c1*S1 + off*sum(x)
+// per 256-column group), laid out for 32 banks: each lane visits the 32
+// column-bytes of its row in an order rotated by its lane index, so the 32
+// lanes of a load always hit 32 different banks.
+#include <cuda_fp16.h>
+
+#include "q2_common.cuh"
+
+extern __shared__ __align__(1024) unsigned char q2_smem[];
+
+namespace q2 {
+namespace {
+
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+
+// T lookup for byte b of word at rotated position P (see build_table).
+__device__ __forceinline__ float tl(uint32_t lane4, uint32_t word, int b, int P) {
+  const uint32_t a = __byte_perm(word, lane4, 0x5504u | ((uint32_t)b << 4));
+  return *reinterpret_cast<const float*>(q2_smem + a + P * 4);
+}
+
+// Sum of the table entries selected by 32 rotated bytes (two uint4 chunks).
+__device__ __forceinline__ float plane_sum(uint32_t lane4, const uint4& c0, const uint4& c1) {
+  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int P = 0; P < 32; P += 2) {
+    s0 += tl(lane4, w[P >> 2], P & 3, P);
+    s1 += tl(lane4, w[(P + 1) >> 2], (P + 1) & 3, P + 1);
+  }
+  return s0 + s1;
+}
+
+struct BpdqArgs {
+  const unsigned char* bits;
+  const __half2* c01;
+  const __half* off;
+  const __half* x;
+  __half* y;
+  Reduce rd;
+  int R, nrb;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) k_bpdq_b1(BpdqArgs a) {
+  float* T = reinterpret_cast<float*>(q2_smem);
+  float* gsum = T + (kBuildBytes - 16) / 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t lane4 = lane * 4u;
+  int i0, i1;
+  cta_range(a.rd.nslice * a.nrb, i0, i1);
+  for (int s0 = i0; s0 < i1;) {
+    const int g = s0 / a.nrb;
+    const int s1 = min(i1, (g + 1) * a.nrb);
+    int it = s0 + warp;
+    uint4 w0, w1, w2, w3;
+    if (it < s1) {
+      const unsigned char* p = a.bits + (size_t)it * Q2_ITEM_BYTES_BPDQ + lane * 16;
+      w0 = ldg_stream(p);
+      w1 = ldg_stream(p + 512);
+      w2 = ldg_stream(p + 1024);
+      w3 = ldg_stream(p + 1536);
+    }
+    __syncthreads();
+    build_table<kThreads>(a.x + (size_t)g * Q2_SLICE, Q2_SLICE, T, gsum);
+    const float xg = *gsum;
+    for (; it < s1; it += kWarps) {
+      const int nx = it + kWarps;
+      uint4 n0, n1, n2, n3;
+      if (nx < s1) {
+        const unsigned char* p = a.bits + (size_t)nx * Q2_ITEM_BYTES_BPDQ + lane * 16;
+        n0 = ldg_stream(p);
+        n1 = ldg_stream(p + 512);
+        n2 = ldg_stream(p + 1024);
+        n3 = ldg_stream(p + 1536);
+      }
+      const int rb = it - g * a.nrb;
+      const int row = rb * 32 + lane;
+      const float S0 = plane_sum(lane4, w0, w1);
+      const float S1 = plane_sum(lane4, w2, w3);
+      const float2 c = __half22float2(a.c01[(size_t)g * a.rd.Rpad + row]);
+      const float of = __half2float(a.off[(size_t)g * a.rd.Rpad + row]);
+      a.rd.partial[(size_t)g * a.rd.Rpad + row] = fmaf(c.x, S0, fmaf(c.y, S1, of * xg));
+      if (arrive(a.rd, rb)) {
+        const float v = gather(a.rd, 0, row);
+        if (row < a.R) a.y[row] = __float2half_rn(v);
+      }
+      w0 = n0; w1 = n1; w2 = n2; w3 = n3;
+    }
+    s0 = s1;
+  }
+}
+
+// ------------------------------------------------------------------ Leech
+struct LeechArgs {
+  const unsigned char* planes;
+  const uint16_t* parity;     // [nslice][Rpad]
+  const __half* scale;        // [Rpad]
+  const __half* tail;         // [Rpad][tailpad]
+  const uint32_t* excptr;     // [Rpad + 1]
+  const uint32_t* exccol;
+  const __half* x;
+  __half* y;
+  Reduce rd;
+  int R, C, nrb, nblock, tail_n, tailpad;
+  float inv_sqrt8;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) k_leech_b1(LeechArgs a) {
+  float* T = reinterpret_cast<float*>(q2_smem);
+  float* gsum = T + (kBuildBytes - 16) / 4;
+  float* xb = reinterpret_cast<float*>(q2_smem + kBuildBytes);   // block sums of x, <= 11
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t lane4 = lane * 4u;
+  int i0, i1;
+  cta_range(a.rd.nslice * a.nrb, i0, i1);
+  for (int s0 = i0; s0 < i1;) {
+    const int sl = s0 / a.nrb;
+    const int s1 = min(i1, (sl + 1) * a.nrb);
+    const int bfirst = (sl * Q2_SLICE + 23) / 24;
+    const int blast = min(a.nblock - 1, (sl * Q2_SLICE + Q2_SLICE + 23) / 24 - 1);
+    const int nbk = max(0, blast - bfirst + 1);
+    int it = s0 + warp;
+    uint4 w[6];
+    if (it < s1) {
+      const unsigned char* p = a.planes + (size_t)it * Q2_ITEM_BYTES_LEECH + lane * 16;
+#pragma unroll
+      for (int k = 0; k < 6; ++k) w[k] = ldg_stream(p + k * 512);
+    }
+    __syncthreads();
+    if (threadIdx.x < nbk) {
+      const __half* xp = a.x + (size_t)(bfirst + threadIdx.x) * 24;
+      float v = 0.f;
+      for (int i = 0; i < 24; ++i) v += __half2float(xp[i]);
+      xb[threadIdx.x] = v;
+    }
+    const int ncols = min(Q2_SLICE, a.C - sl * Q2_SLICE);
+    build_table<kThreads>(a.x + (size_t)sl * Q2_SLICE, ncols, T, gsum);
+    for (; it < s1; it += kWarps) {
+      const int nx = it + kWarps;
+      uint4 n[6];
+      if (nx < s1) {
+        const unsigned char* p = a.planes + (size_t)nx * Q2_ITEM_BYTES_LEECH + lane * 16;
+#pragma unroll
+        for (int k = 0; k < 6; ++k) n[k] = ldg_stream(p + k * 512);
+      }
+      const int rb = it - sl * a.nrb;
+      const int row = rb * 32 + lane;
+      const float P0 = plane_sum(lane4, w[0], w[1]);
+      const float P1 = plane_sum(lane4, w[2], w[3]);
+      const float P2 = plane_sum(lane4, w[4], w[5]);
+      const uint32_t pw = a.parity[(size_t)sl * a.rd.Rpad + row];
+      float pacc = 0.f;
+      for (int j = 0; j < nbk; ++j) pacc += ((pw >> j) & 1u) ? xb[j] : 0.f;
+      // v = p + 2*b0 + 4*b1 - 8*b2 per weight
+      a.rd.partial[(size_t)sl * a.rd.Rpad + row] = fmaf(2.f, P0, fmaf(4.f, P1, fmaf(-8.f, P2, pacc)));
+      if (arrive(a.rd, rb)) {
+        float v = gather(a.rd, 0, row);
+        for (uint32_t e = a.excptr[row]; e < a.excptr[row + 1]; ++e)
+          v = fmaf(16.f, __half2float(a.x[a.exccol[e]]), v);     // v = +8 stored as -8
+        float acc = __half2float(a.scale[row]) * a.inv_sqrt8 * v;
+        const int tbase = a.nblock * 24;
+        for (int j = 0; j < a.tail_n; ++j)
+          acc = fmaf(__half2float(a.tail[(size_t)row * a.tailpad + j]), __half2float(a.x[tbase + j]), acc);
+        if (row < a.R) a.y[row] = __float2half_rn(acc);
+      }
+#pragma unroll
+      for (int k = 0; k < 6; ++k) w[k] = n[k];
+    }
+    s0 = s1;
+  }
+}
+
+// ------------------------------------------------------- no-weights control
+// Same grid, table build, per-lane lookups and reduction as k_bpdq_b1; the
+// "weight" words are derived from the lane and item index instead of being
+// loaded, so the kernel reads x and writes y and the workspace only.
+__global__ void __launch_bounds__(kThreads, 1) k_noweights_b1(BpdqArgs a) {
+  float* T = reinterpret_cast<float*>(q2_smem);
+  float* gsum = T + (kBuildBytes - 16) / 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t lane4 = lane * 4u;
+  int i0, i1;
+  cta_range(a.rd.nslice * a.nrb, i0, i1);
+  for (int s0 = i0; s0 < i1;) {
+    const int g = s0 / a.nrb;
+    const int s1 = min(i1, (g + 1) * a.nrb);
+    __syncthreads();
+    build_table<kThreads>(a.x + (size_t)g * Q2_SLICE, Q2_SLICE, T, gsum);
+    const float xg = *gsum;
+    for (int it = s0 + warp; it < s1; it += kWarps) {
+      const uint32_t h = (uint32_t)it * 0x9E3779B9u ^ (lane4 * 0x85EBCA6Bu);
+      const uint4 w0 = make_uint4(h, h ^ 0x5bd1e995u, h * 3u, h * 5u);
+      const uint4 w1 = make_uint4(h * 7u, h ^ 0x27d4eb2fu, h * 11u, h * 13u);
+      const int rb = it - g * a.nrb;
+      const int row = rb * 32 + lane;
+      const float S0 = plane_sum(lane4, w0, w1);
+      const float S1 = plane_sum(lane4, w1, w0);
+      a.rd.partial[(size_t)g * a.rd.Rpad + row] = fmaf(0.02f, S0, fmaf(0.01f, S1, 0.01f * xg));
+      if (arrive(a.rd, rb)) {
+        const float v = gather(a.rd, 0, row);
+        if (row < a.R) a.y[row] = __float2half_rn(v);
+      }
+    }
+    s0 = s1;
+  }
+}
+
+// ---------------------------------------------------------------- trellis
+// Lane = row, item = (segment, 32 rows).  The 16 KiB table and all of x sit
+// in shared memory for the whole kernel.  Step k of a segment reads the
+// 16-bit state at bit offset 4*(127 - k) of the lane's 512-bit packet (a
+// funnel shift of two words), hashes it, loads one fp16 pair, flips both
+// signs by state bit 0 and accumulates two fp32 FMAs.
+struct TrellisArgs {
+  const unsigned char* stream;
+  const uint32_t* table;     // 4096 half2
+  const __half* scale;
+  const __half* x;
+  __half* y;
+  Reduce rd;
+  int R, C, nrb;
+};
+
+constexpr uint32_t kHashHi = 0x9E37u << 16;   // (s*0x9E37 mod 2^16) lands in bits 16..31
+
+__global__ void __launch_bounds__(kThreads, 1) k_trellis_b1(TrellisArgs a) {
+  uint32_t* tab = reinterpret_cast<uint32_t*>(q2_smem);                 // 16 KiB
+  uint32_t* xs = reinterpret_cast<uint32_t*>(q2_smem + 4096 * 4);      // x as half2, C/2 words
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int i0, i1;
+  cta_range(a.rd.nslice * a.nrb, i0, i1);
+  int it = i0 + warp;
+  uint4 w0, w1, w2, w3;
+  if (it < i1) {
+    const unsigned char* p = a.stream + (size_t)it * Q2_ITEM_BYTES_TRL + lane * 16;
+    w0 = ldg_stream(p);
+    w1 = ldg_stream(p + 512);
+    w2 = ldg_stream(p + 1024);
+    w3 = ldg_stream(p + 1536);
+  }
+  for (int i = threadIdx.x; i < 4096; i += kThreads) tab[i] = a.table[i];
+  const uint32_t* xg = reinterpret_cast<const uint32_t*>(a.x);
+  for (int i = threadIdx.x; i < a.C / 2; i += kThreads) xs[i] = xg[i];
+  __syncthreads();
+  for (; it < i1; it += kWarps) {
+    const int nx = it + kWarps;
+    uint4 n0, n1, n2, n3;
+    if (nx < i1) {
+      const unsigned char* p = a.stream + (size_t)nx * Q2_ITEM_BYTES_TRL + lane * 16;
+      n0 = ldg_stream(p);
+      n1 = ldg_stream(p + 512);
+      n2 = ldg_stream(p + 1024);
+      n3 = ldg_stream(p + 1536);
+    }
+    const int sg = it / a.nrb, rb = it - sg * a.nrb;
+    const int row = rb * 32 + lane;
+    const uint32_t W[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
+                            w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+    const uint4* xv = reinterpret_cast<const uint4*>(xs + sg * 128);
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int k4 = 0; k4 < 32; ++k4) {
+      const uint4 x4 = xv[k4];
+      const uint32_t xx[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const int k = k4 * 4 + kk;
+        const int n = 127 - k;
+        const uint32_t f = __funnelshift_r(W[n >> 3], W[((n >> 3) + 1) & 15], 4 * (n & 7));
+        const uint32_t h = f * kHashHi;
+        uint32_t e = tab[h >> 20];
+        e ^= (f & 1u) ? 0x80008000u : 0u;
+        if (kk & 1) {
+          acc1 = fma_h(lo16(e), lo16(xx[kk]), acc1);
+          acc1 = fma_h(hi16(e), hi16(xx[kk]), acc1);
+        } else {
+          acc0 = fma_h(lo16(e), lo16(xx[kk]), acc0);
+          acc0 = fma_h(hi16(e), hi16(xx[kk]), acc0);
+        }
+      }
+    }
+    a.rd.partial[(size_t)sg * a.rd.Rpad + row] = acc0 + acc1;
+    if (arrive(a.rd, rb)) {
+      const float v = gather(a.rd, 0, row);
+      if (row < a.R) a.y[row] = __float2half_rn(__half2float(a.scale[row]) * v);
+    }
+    w0 = n0; w1 = n1; w2 = n2; w3 = n3;
+  }
+}
+
+template <typename K, typename A>
+int launch(K kernel, const A& args, int smem, int items, void* stream) {
+  const DevInfo di = dev_info();
+  if (set_smem(reinterpret_cast<const void*>(kernel), smem)) return Q2_ECUDA;
+  const int grid = max(1, min(items, di.sms));
+  kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(args);
+  return cudaGetLastError() == cudaSuccess ? Q2_OK : Q2_ECUDA;
+}
+
+Reduce make_reduce(const q2_handle* h, int ntok) {
+  Reduce r;
+  r.counter = reinterpret_cast<unsigned*>(h->ws);
+  r.partial = reinterpret_cast<float*>(static_cast<unsigned char*>(h->ws) + q2_counter_bytes(h->hdr));
+  r.nslice = h->hdr.nslice;
+  r.Rpad = h->hdr.Rpad;
+  (void)ntok;
+  return r;
+}
+
+}  // namespace
+}  // namespace q2
+
+using namespace q2;
+
+extern "C" int q2_b1_bpdq(const q2_handle* h, const void* x, void* y, void* stream) {
+  const q2_blob_header& d = h->hdr;
+  BpdqArgs a;
+  a.bits = h->dev + d.off[SEC_BPDQ_BITS];
+  a.c01 = reinterpret_cast<const __half2*>(h->dev + d.off[SEC_BPDQ_C01]);
+  a.off = reinterpret_cast<const __half*>(h->dev + d.off[SEC_BPDQ_OFF]);
+  a.x = static_cast<const __half*>(x);
+  a.y = static_cast<__half*>(y);
+  a.rd = make_reduce(h, 1);
+  a.R = d.R;
+  a.nrb = q2_nrb(d);
+  return launch(k_bpdq_b1, a, kBuildBytes, d.nslice * a.nrb, stream);
+}
+
+extern "C" int q2_b1_noweights(const q2_handle* h, const void* x, void* y, void* stream) {
+  const q2_blob_header& d = h->hdr;
+  BpdqArgs a = {};
+  a.x = static_cast<const __half*>(x);
+  a.y = static_cast<__half*>(y);
+  a.rd = make_reduce(h, 1);
+  a.R = d.R;
+  a.nrb = q2_nrb(d);
+  return launch(k_noweights_b1, a, kBuildBytes, d.nslice * a.nrb, stream);
+}
+
+extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* stream) {
+  const q2_blob_header& d = h->hdr;
+  LeechArgs a;
+  a.planes = h->dev + d.off[SEC_LEECH_PLANES];
+  a.parity = reinterpret_cast<const uint16_t*>(h->dev + d.off[SEC_LEECH_PARITY]);
+  a.scale = reinterpret_cast<const __half*>(h->dev + d.off[SEC_LEECH_SCALE]);
+  a.tail = reinterpret_cast<const __half*>(h->dev + d.off[SEC_LEECH_TAIL]);
+  a.excptr = reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_LEECH_EXCPTR]);
+  a.exccol = reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_LEECH_EXCCOL]);
+  a.x = static_cast<const __half*>(x);
+  a.y = static_cast<__half*>(y);
+  a.rd = make_reduce(h, 1);
+  a.R = d.R;
+  a.C = d.C;
+  a.nrb = q2_nrb(d);
+  a.nblock = d.nblock;
+  a.tail_n = d.tail;
+  a.tailpad = d.tailpad;
+  a.inv_sqrt8 = d.inv_sqrt8;
+  return launch(k_leech_b1, a, kBuildBytes + 64, d.nslice * a.nrb, stream);
+}
+
+extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* stream) {
+  const q2_blob_header& d = h->hdr;
+  TrellisArgs a;
+  a.stream = h->dev + d.off[SEC_TRL_STREAM];
+  a.table = reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_TRL_TABLE]);
+  a.scale = reinterpret_cast<const __half*>(h->dev + d.off[SEC_TRL_SCALE]);
+  a.x = static_cast<const __half*>(x);
+  a.y = static_cast<__half*>(y);
+  a.rd = make_reduce(h, 1);
+  a.R = d.R;
+  a.C = d.C;
+  a.nrb = q2_nrb(d);
+  const int smem = 4096 * 4 + d.C * 2;
+  return launch(k_trellis_b1, a, smem, d.nslice * a.nrb, stream);
+}

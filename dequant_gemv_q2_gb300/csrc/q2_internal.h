@@ -1,0 +1,33 @@
+// Internal declarations shared by the host code and the CUDA sources.
+#pragma once
+#include "q2_layout.h"
+#include "../../include/q2.h"
+
+struct q2_handle {
+  q2_blob_header hdr;
+  const unsigned char* dev;  // device copy of the blob (caller-owned)
+  void* ws;                  // split-K workspace (caller-owned), may be null
+  size_t ws_bytes;
+};
+
+static inline int q2_nrb(const q2_blob_header& h) { return h.Rpad / Q2_ROWS; }
+
+// Workspace layout: [counters: nrb x uint32, padded to 256 B][partials: fp32]
+static inline size_t q2_counter_bytes(const q2_blob_header& h) {
+  size_t b = (size_t)q2_nrb(h) * 4;
+  return (b + 255) & ~(size_t)255;
+}
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+// Launchers (CUDA side).  Each returns a q2 status.
+int q2_launch_fp16(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
+int q2_launch_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
+int q2_launch_trellis(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
+int q2_launch_leech(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
+int q2_launch_noweights(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
+int q2_launch_decode(const q2_handle* h, void* out, void* stream);
+#ifdef __cplusplus
+}
+#endif

@@ -1,0 +1,156 @@
+/*
+ * q2.h -- C ABI of the fused dequantize-plus-matvec library for packed
+ * ~2-bit weights on GB300 (sm_103a).
+ *
+ * The operation is y = W x for a packed weight matrix W with R output rows
+ * and C input columns, called once per projection ("Unfolding the Leech
+ * Lattice", introduction: a fused dequantize-plus-matvec, decode-phase GEMV
+ * at batch 1; "Qwen3-8B -- 2-bit BPDQ (packed)", Kernels: one kernel per
+ * matmul, tile shape picked per batch size).  x holds ntok token vectors,
+ * fp16 row-major [ntok][C]; y is fp16 row-major [ntok][R]; accumulation is
+ * fp32.  The weights stay packed and are never expanded to dense fp16.
+ *
+ * Formats:
+ *   Q2_FP16      dense fp16 control.
+ *   Q2_BPDQ      two bit-planes, w = c0*b0 + c1*b1 + off per (256-column
+ *                group, row) ("Qwen3-8B -- 2-bit BPDQ (packed)", Format).
+ *   Q2_TRELLIS   bitshift trellis, L=16, T=4, V=2, 4096x2 fp16 table
+ *                codebook, fp16 row scale, restart every 256 columns
+ *                ("Qwen3.8-27B on a 12 GB card", "A trellis is a codebook
+ *                you walk").
+ *   Q2_LEECH     Leech-lattice blocks of 24 weights, w = scale_r * v / sqrt(8),
+ *                fp16 tail for the last C % 24 columns ("Unfolding the Leech
+ *                Lattice", introduction and section 2; "Tetra", section 5.1).
+ *   Q2_NOWEIGHTS launch-geometry control: same grid, table build and
+ *                reduction as the BPDQ kernel, reads no weight bytes
+ *                ("Unfolding the Leech Lattice", contribution C4).
+ *
+ * Conventions (all entry points):
+ *   - Return Q2_OK (0) or a negative Q2_E* status; nothing aborts, nothing
+ *     throws across the ABI.  q2_strerror() names a status.
+ *   - Host pointers are read during the call only.  Device pointers stay
+ *     owned by the caller; the library allocates no device memory.
+ *   - Packers are two-phase: call with out == NULL to get *out_bytes, then
+ *     with a buffer of that size.
+ */
+#ifndef Q2_H
+#define Q2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  Q2_FP16 = 0,
+  Q2_BPDQ = 1,
+  Q2_TRELLIS = 2,
+  Q2_LEECH = 3,
+  Q2_NOWEIGHTS = 4
+} q2_fmt;
+
+enum {
+  Q2_OK = 0,
+  Q2_EINVAL = -1,      /* null pointer or bad scalar argument            */
+  Q2_ESHAPE = -2,      /* R, C outside what the format accepts            */
+  Q2_EALIGN = -3,      /* x, y or the device blob not 16-byte aligned     */
+  Q2_EFMT = -4,        /* fmt does not match the handle                    */
+  Q2_ENTOK = -5,       /* ntok outside 1..64                               */
+  Q2_EBLOB = -6,       /* blob header corrupt or wrong version            */
+  Q2_EWORKSPACE = -7,  /* no workspace bound, or smaller than needed       */
+  Q2_ECUDA = -8,       /* a CUDA call or kernel launch failed              */
+  Q2_ENOMEM = -9,      /* host allocation failed                           */
+  Q2_ESIZE = -10       /* caller's buffer smaller than required            */
+};
+
+typedef struct q2_handle q2_handle;   /* opaque; owns no device memory */
+typedef struct CUstream_st* q2_stream; /* a cudaStream_t; NULL = legacy default stream */
+
+#define Q2_MAX_NTOK 64
+
+/* ------------------------------------------------------------------ packers
+ * Offline packers: canonical host arrays in, self-describing host blob out
+ * (header + sections, each 256-byte aligned).  The blob can be written to a
+ * file and bound later; its device copy must be byte-identical.
+ */
+
+/* Dense fp16 control.  w: fp16 bits [R][C] row-major.  C % 8 == 0. */
+int q2_pack_fp16(const uint16_t* w, int R, int C, void* out, size_t* out_bytes);
+
+/* BPDQ ("Qwen3-8B -- 2-bit BPDQ (packed)", Format: w[r,c] = sum_i
+ * coeffs[g(c),r,i] * bit_i(r,c) + coeffs[g(c),r,msbits], group 256).
+ * plane0, plane1: [R][C/8] bytes, bit i (LSB first) of byte j = column 8j+i.
+ * coef: fp16 bits [C/256][R][3] = (c0, c1, off).  C % 256 == 0, R >= 1.
+ * The 2-bit code of a weight is b0 | b1 << 1. */
+int q2_pack_bpdq(const uint8_t* plane0, const uint8_t* plane1, const uint16_t* coef,
+                 int R, int C, void* out, size_t* out_bytes);
+
+/* Bitshift trellis ("Qwen3.8-27B on a 12 GB card": state = last L bits;
+ * each step shifts T bits in and emits V weights).  stream: [R][C/256][64]
+ * bytes, byte i of a segment = symbol 2i (low nibble) and 2i+1 (high
+ * nibble).  table: fp16 bits [4096][2].  scale: fp16 bits [R].  The state of
+ * step k is t[k-3]<<12 | t[k-2]<<8 | t[k-1]<<4 | t[k] (indices modulo 128
+ * inside the segment); its row is ((s*0x9E37) & 0xFFFF) >> 4; bit 0 of the
+ * state negates both weights.  C % 256 == 0. */
+int q2_pack_trellis(const uint8_t* stream, const uint16_t* table, const uint16_t* scale,
+                    int R, int C, void* out, size_t* out_bytes);
+
+/* Leech lattice ("Unfolding the Leech Lattice": blocks of 24 weights, each a
+ * lattice point; unfolded offline into a bit-plane layout).  v: int8
+ * [R][C/24][24] lattice points, |v_i| <= 8 with all coordinates of a block
+ * of one parity; tail: fp16 bits [R][C%24]; scale: fp16 bits [R].  Any C
+ * with C >= 24 is accepted; inv_sqrt8 is the fp32 factor applied with the
+ * row scale (the caller passes 1/sqrt(8) rounded to fp32).  Layout: per
+ * block a parity bit and three two's-complement planes of u = (v - p)/2;
+ * v = +8 goes to an exception side channel. */
+int q2_pack_leech(const int8_t* v, const uint16_t* tail, const uint16_t* scale,
+                  int R, int C, float inv_sqrt8, void* out, size_t* out_bytes);
+
+/* No-weights control: a header only. */
+int q2_pack_noweights(int R, int C, void* out, size_t* out_bytes);
+
+/* ------------------------------------------------------------------ binding
+ * blob_host: the packed blob (read now); blob_dev: its device copy, 256-byte
+ * aligned, kept alive by the caller while the handle is used.  Returns a
+ * handle that holds pointers into blob_dev only. */
+int q2_bind(const void* blob_host, const void* blob_dev, q2_handle** h);
+void q2_unbind(q2_handle* h);
+
+/* Split-K workspace: device memory owned by the caller, zero-filled before
+ * its first use and left zeroed by every completed call.  One workspace may
+ * serve many handles whose calls are ordered on one stream. */
+int q2_workspace_bytes(const q2_handle* h, int ntok, size_t* bytes);
+int q2_set_workspace(q2_handle* h, void* ws_dev, size_t ws_bytes);
+
+/* Format, shape and algorithmic bytes read from HBM per call at ntok tokens
+ * (weights and side data; x and y not included). */
+int q2_info(const q2_handle* h, int* fmt, int* R, int* C);
+int q2_bytes(const q2_handle* h, int ntok, size_t* weight_bytes_read_per_call);
+
+/* ------------------------------------------------------------------ compute
+ * y = W x ("Unfolding the Leech Lattice", introduction).  x: device fp16
+ * [ntok][C]; y: device fp16 [ntok][R]; both 16-byte aligned; 1 <= ntok <= 64.
+ * Asynchronous and ordered on `stream`; never synchronises.  Needs the
+ * workspace of q2_workspace_bytes(h, ntok) bound first (0 bytes for fp16).
+ * Returns Q2_ECUDA if the launch fails. */
+int q2_gemv(q2_fmt fmt, const q2_handle* h, const void* x, void* y, int ntok, q2_stream stream);
+
+/* Debug decode to the canonical form (all formats but Q2_NOWEIGHTS):
+ *   fp16:    fp16 [R][C]
+ *   BPDQ:    fp16 [R][C], one round-to-nearest-even of c0*b0 + c1*b1 + off
+ *   trellis: fp32 [R][C], float(scale_r) * float(sign * table value)
+ *   Leech:   int8 [R][24*(C/24)] lattice coordinates, then fp16 [R][C%24]
+ *            tail at byte offset R*24*(C/24) rounded up to 16.
+ * out: device buffer of q2_decode_bytes() bytes. */
+int q2_decode_bytes(const q2_handle* h, size_t* bytes);
+int q2_decode(const q2_handle* h, void* out_dev, q2_stream stream);
+
+const char* q2_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q2_H */

@@ -1,0 +1,179 @@
+"""Parity of the CUDA path (through the C ABI) against the oracle.
+
+Every output must satisfy |y - y_ref| <= 2e-3 * sum_c |w[r][c] * x[t][c]|
+(fp32 accumulation, fp16 result); decoded weights must equal the oracle's
+canonical decode bit for bit.  Inputs come from the seeded generators in
+``synth``.
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle import bpdq as obpdq, fp16 as ofp16, leech as oleech, matvec, trellis as otrellis
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def q2():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import dequant_gemv_q2_gb300 as m
+    m.load(build_if_missing=True)
+    return m
+
+
+def _run(q2, blob, x, rows=None):
+    pk = q2.Packed(blob)
+    xd = torch.from_numpy(x).cuda()
+    y = pk.gemv(xd)
+    torch.cuda.synchronize()
+    return pk, y.cpu().numpy()
+
+
+def _check(y, w64, x, rows=None):
+    if rows is not None:
+        y = y[:, rows]
+    yref = matvec.gemv(w64, x)
+    bound = matvec.abs_bound(w64, x)
+    ok = matvec.passes(y, yref, bound, TOL)
+    rel = matvec.relative_error(y, yref, bound)
+    assert ok.all(), f"{(~ok).sum()} outputs fail; worst relative error {rel.max():.3e}"
+    return rel.max()
+
+
+# ------------------------------------------------------------------- BPDQ
+@pytest.mark.parametrize("R,C,seed", [(1024, 1024, 0), (70, 768, 1), (32, 256, 2), (1, 512, 3)])
+@pytest.mark.parametrize("ntok", [1, 2, 5, 16, 64])
+def test_bpdq_parity(q2, R, C, seed, ntok):
+    d = synth.bpdq(R, C, seed)
+    x = synth.activations(ntok, C, seed)
+    _, y = _run(q2, q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]), x)
+    _check(y, obpdq.decode_f64(d["plane0"], d["plane1"], d["coef"]), x)
+
+
+def test_bpdq_decode_bit_exact(q2):
+    d = synth.bpdq(70, 768, 9)
+    pk = q2.Packed(q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]))
+    w = pk.decode().cpu().numpy().view(np.float16).reshape(70, 768)
+    assert np.array_equal(w.view(np.uint16), obpdq.decode_fp16(d["plane0"], d["plane1"], d["coef"]).view(np.uint16))
+
+
+def test_bpdq_deterministic_and_repeatable(q2):
+    d = synth.bpdq(4096, 4096, 1001)
+    x = torch.from_numpy(synth.activations(1, 4096, 1001)).cuda()
+    pk = q2.Packed(q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]))
+    ys = [pk.gemv(x).clone() for _ in range(5)]
+    torch.cuda.synchronize()
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+
+
+# ---------------------------------------------------------------- trellis
+@pytest.mark.parametrize("R,C,seed", [(100, 1024, 2000), (32, 256, 2001), (257, 512, 2002)])
+@pytest.mark.parametrize("ntok", [1, 3, 16, 64])
+def test_trellis_parity(q2, R, C, seed, ntok):
+    d = synth.trellis(R, C, seed)
+    x = synth.activations(ntok, C, seed)
+    _, y = _run(q2, q2.q2_pack_trellis(d["stream"], d["table"], d["scale"]), x)
+    _check(y, otrellis.decode_f64(d["stream"], d["table"], d["scale"]), x)
+
+
+def test_trellis_decode_bit_exact(q2):
+    d = synth.trellis(45, 768, 2010)
+    pk = q2.Packed(q2.q2_pack_trellis(d["stream"], d["table"], d["scale"]))
+    w = pk.decode().cpu().numpy().view(np.float32).reshape(45, 768)
+    assert np.array_equal(w, otrellis.decode_fp32(d["stream"], d["table"], d["scale"]))
+
+
+# ------------------------------------------------------------------ Leech
+def _leech_with_exceptions(R, C, seed):
+    d = synth.leech(R, C, seed)
+    v = d["v"].copy()
+    v[0, 0] = 0
+    v[0, 0, 3] = 8                    # (8, 0^23): shell 4, goes to the exception channel
+    if R > 5 and v.shape[1] > 7:
+        v[5, 7] = 0
+        v[5, 7, [1, 2]] = [8, 8]
+    d["v"] = v
+    return d
+
+
+@pytest.mark.parametrize("R,C,seed", [(70, 24 * 40 + 8, 3000), (32, 256, 3001), (100, 5120, 3002), (33, 24, 3003)])
+@pytest.mark.parametrize("ntok", [1, 4, 16, 64])
+def test_leech_parity(q2, R, C, seed, ntok):
+    d = _leech_with_exceptions(R, C, seed)
+    x = synth.activations(ntok, C, seed)
+    _, y = _run(q2, q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C), x)
+    _check(y, oleech.decode_f64(d["v"], d["scale"], d["tail"]), x)
+
+
+def test_leech_decode_bit_exact(q2):
+    R, C = 70, 24 * 40 + 8
+    d = _leech_with_exceptions(R, C, 3010)
+    pk = q2.Packed(q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C))
+    out = pk.decode().cpu().numpy()
+    body = R * 40 * 24
+    v = out[:body].view(np.int8).reshape(R, 40, 24)
+    assert np.array_equal(v, d["v"])
+    start = (body + 15) // 16 * 16
+    tail = out[start:start + R * 8 * 2].view(np.float16).reshape(R, 8)
+    assert np.array_equal(tail.view(np.uint16), d["tail"].view(np.uint16))
+
+
+# ---------------------------------------------------------------- fp16
+@pytest.mark.parametrize("ntok", [1, 3, 16, 64])
+def test_fp16_parity(q2, ntok):
+    d = synth.fp16_dense(300, 1032, 4000)
+    x = synth.activations(ntok, 1032, 4000)
+    _, y = _run(q2, q2.q2_pack_fp16(d["w"]), x)
+    _check(y, ofp16.decode_f64(d["w"]), x)
+
+
+def test_noweights_control_runs(q2):
+    pk = q2.Packed(q2.q2_pack_noweights(1024, 1024))
+    x = torch.from_numpy(synth.activations(1, 1024, 5)).cuda()
+    y1 = pk.gemv(x).clone()
+    y2 = pk.gemv(x)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y1.float()).all() and torch.equal(y1, y2)
+
+
+# ------------------------------------------------------ full-size configs
+def _sampled_rows(R, n=96, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(R, size=min(n, R), replace=False))
+    rows[0], rows[-1] = 0, R - 1
+    return np.unique(rows)
+
+
+@pytest.mark.parametrize("R,C", [(6144, 4096), (4096, 4096), (24576, 4096), (4096, 12288)])
+def test_bpdq_full_size_8b_layers(q2, R, C):
+    seed = 1000 + R + C
+    d = synth.bpdq(R, C, seed)
+    x = synth.activations(1, C, seed)
+    _, y = _run(q2, q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]), x)
+    rows = _sampled_rows(R)
+    w = obpdq.decode_f64(d["plane0"][rows], d["plane1"][rows], d["coef"][:, rows])
+    _check(y, w, x, rows)
+
+
+@pytest.mark.parametrize("R,C", [(12288, 4096), (4096, 12288)])
+def test_trellis_full_size(q2, R, C):
+    d = synth.trellis(R, C, 2000 + (R > C))
+    x = synth.activations(1, C, 2000 + (R > C))
+    _, y = _run(q2, q2.q2_pack_trellis(d["stream"], d["table"], d["scale"]), x)
+    rows = _sampled_rows(R)
+    _check(y, otrellis.decode_f64(d["stream"][rows], d["table"], d["scale"][rows]), x, rows)
+
+
+@pytest.mark.parametrize("R,C", [(17408, 5120), (5120, 17408)])
+def test_leech_full_size(q2, R, C):
+    d = synth.leech(R, C, 3000 + (R > C))
+    x = synth.activations(1, C, 3000 + (R > C))
+    _, y = _run(q2, q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C), x)
+    rows = _sampled_rows(R)
+    _check(y, oleech.decode_f64(d["v"][rows], d["scale"][rows], d["tail"][rows]), x, rows)
