@@ -2,8 +2,9 @@
 // control.  One lane owns one output row; a warp owns 32 rows of one
 // 256-column slice (an "item").  CTAs take contiguous, equal shares of the
 // items in slice-major order and keep the x-dependent tables of the current
-// slice in shared memory; per-slice partial sums are reduced in a fixed order
-// by the last warp of each row block (q2::arrive / q2::gather).
+// slice in shared memory.  Per-slice partial sums go to the workspace with
+// plain stores; a second launch (q2_reduce.cu) sums them in slice order
+// (deterministic) and writes y.
 //
 // BPDQ and Leech use subset-sum tables in place of a per-weight decode: for
 // each 8-column byte of a bit-plane the table holds the sum of the x values
@@ -13,16 +14,23 @@
 // per 256-column group), laid out for 32 banks: each lane visits the 32
 // column-bytes of its row in an order rotated by its lane index, so the 32
 // lanes of a load always hit 32 different banks.
+//
+// Launches use programmatic dependent launch: a CTA prefetches its first
+// weights, then waits for the previous kernel on the stream (griddepcontrol)
+// before it touches x or the workspace, and lets the dependent reduction and
+// the next GEMV's CTAs get scheduled while it runs.
 #include <cuda_fp16.h>
 
 #include "q2_common.cuh"
 
 extern __shared__ __align__(1024) unsigned char q2_smem[];
 
+extern "C" int q2_launch_reduce(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
+
 namespace q2 {
 namespace {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 
 // T lookup for byte b of word at rotated position P (see build_table).
@@ -34,13 +42,10 @@ __device__ __forceinline__ float tl(uint32_t lane4, uint32_t word, int b, int P)
 // Sum of the table entries selected by 32 rotated bytes (two uint4 chunks).
 __device__ __forceinline__ float plane_sum(uint32_t lane4, const uint4& c0, const uint4& c1) {
   const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  float s0 = 0.f, s1 = 0.f;
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int P = 0; P < 32; P += 2) {
-    s0 += tl(lane4, w[P >> 2], P & 3, P);
-    s1 += tl(lane4, w[(P + 1) >> 2], (P + 1) & 3, P + 1);
-  }
-  return s0 + s1;
+  for (int P = 0; P < 32; ++P) s[P & 3] += tl(lane4, w[P >> 2], P & 3, P);
+  return (s[0] + s[1]) + (s[2] + s[3]);
 }
 
 struct BpdqArgs {
@@ -53,50 +58,49 @@ struct BpdqArgs {
   int R, nrb;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) k_bpdq_b1(BpdqArgs a) {
+__device__ __forceinline__ void ld_item4(const unsigned char* base, int it, int lane, uint4 (&w)[4]) {
+  const unsigned char* p = base + (size_t)it * Q2_ITEM_BYTES_BPDQ + lane * 16;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) w[k] = ldg_stream(p + k * 512);
+}
+
+__global__ void __launch_bounds__(kThreads, 2) k_bpdq_b1(BpdqArgs a) {
   float* T = reinterpret_cast<float*>(q2_smem);
   float* gsum = T + (kBuildBytes - 16) / 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t lane4 = lane * 4u;
   int i0, i1;
   cta_range(a.rd.nslice * a.nrb, i0, i1);
+  bool waited = false;
   for (int s0 = i0; s0 < i1;) {
     const int g = s0 / a.nrb;
     const int s1 = min(i1, (g + 1) * a.nrb);
     int it = s0 + warp;
-    uint4 w0, w1, w2, w3;
-    if (it < s1) {
-      const unsigned char* p = a.bits + (size_t)it * Q2_ITEM_BYTES_BPDQ + lane * 16;
-      w0 = ldg_stream(p);
-      w1 = ldg_stream(p + 512);
-      w2 = ldg_stream(p + 1024);
-      w3 = ldg_stream(p + 1536);
+    uint4 wa[4], wb[4];
+    if (it < s1) ld_item4(a.bits, it, lane, wa);
+    if (it + kWarps < s1) ld_item4(a.bits, it + kWarps, lane, wb);
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
     }
     __syncthreads();
     build_table<kThreads>(a.x + (size_t)g * Q2_SLICE, Q2_SLICE, T, gsum);
     const float xg = *gsum;
     for (; it < s1; it += kWarps) {
-      const int nx = it + kWarps;
-      uint4 n0, n1, n2, n3;
-      if (nx < s1) {
-        const unsigned char* p = a.bits + (size_t)nx * Q2_ITEM_BYTES_BPDQ + lane * 16;
-        n0 = ldg_stream(p);
-        n1 = ldg_stream(p + 512);
-        n2 = ldg_stream(p + 1024);
-        n3 = ldg_stream(p + 1536);
-      }
-      const int rb = it - g * a.nrb;
-      const int row = rb * 32 + lane;
-      const float S0 = plane_sum(lane4, w0, w1);
-      const float S1 = plane_sum(lane4, w2, w3);
+      uint4 wc[4];
+      if (it + 2 * kWarps < s1) ld_item4(a.bits, it + 2 * kWarps, lane, wc);
+      const int row = (it - g * a.nrb) * 32 + lane;
+      const float S0 = plane_sum(lane4, wa[0], wa[1]);
+      const float S1 = plane_sum(lane4, wa[2], wa[3]);
       const float2 c = __half22float2(a.c01[(size_t)g * a.rd.Rpad + row]);
       const float of = __half2float(a.off[(size_t)g * a.rd.Rpad + row]);
       a.rd.partial[(size_t)g * a.rd.Rpad + row] = fmaf(c.x, S0, fmaf(c.y, S1, of * xg));
-      if (arrive(a.rd, rb)) {
-        const float v = gather(a.rd, 0, row);
-        if (row < a.R) a.y[row] = __float2half_rn(v);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        wa[k] = wb[k];
+        wb[k] = wc[k];
       }
-      w0 = n0; w1 = n1; w2 = n2; w3 = n3;
     }
     s0 = s1;
   }
@@ -117,7 +121,13 @@ struct LeechArgs {
   float inv_sqrt8;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) k_leech_b1(LeechArgs a) {
+__device__ __forceinline__ void ld_item6(const unsigned char* base, int it, int lane, uint4 (&w)[6]) {
+  const unsigned char* p = base + (size_t)it * Q2_ITEM_BYTES_LEECH + lane * 16;
+#pragma unroll
+  for (int k = 0; k < 6; ++k) w[k] = ldg_stream(p + k * 512);
+}
+
+__global__ void __launch_bounds__(kThreads, 2) k_leech_b1(LeechArgs a) {
   float* T = reinterpret_cast<float*>(q2_smem);
   float* gsum = T + (kBuildBytes - 16) / 4;
   float* xb = reinterpret_cast<float*>(q2_smem + kBuildBytes);   // block sums of x, <= 11
@@ -125,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_leech_b1(LeechArgs a) {
   const uint32_t lane4 = lane * 4u;
   int i0, i1;
   cta_range(a.rd.nslice * a.nrb, i0, i1);
+  bool waited = false;
   for (int s0 = i0; s0 < i1;) {
     const int sl = s0 / a.nrb;
     const int s1 = min(i1, (sl + 1) * a.nrb);
@@ -132,11 +143,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_leech_b1(LeechArgs a) {
     const int blast = min(a.nblock - 1, (sl * Q2_SLICE + Q2_SLICE + 23) / 24 - 1);
     const int nbk = max(0, blast - bfirst + 1);
     int it = s0 + warp;
-    uint4 w[6];
-    if (it < s1) {
-      const unsigned char* p = a.planes + (size_t)it * Q2_ITEM_BYTES_LEECH + lane * 16;
-#pragma unroll
-      for (int k = 0; k < 6; ++k) w[k] = ldg_stream(p + k * 512);
+    uint4 wa[6];
+    if (it < s1) ld_item6(a.planes, it, lane, wa);
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
     }
     __syncthreads();
     if (threadIdx.x < nbk) {
@@ -148,51 +160,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_leech_b1(LeechArgs a) {
     const int ncols = min(Q2_SLICE, a.C - sl * Q2_SLICE);
     build_table<kThreads>(a.x + (size_t)sl * Q2_SLICE, ncols, T, gsum);
     for (; it < s1; it += kWarps) {
-      const int nx = it + kWarps;
-      uint4 n[6];
-      if (nx < s1) {
-        const unsigned char* p = a.planes + (size_t)nx * Q2_ITEM_BYTES_LEECH + lane * 16;
-#pragma unroll
-        for (int k = 0; k < 6; ++k) n[k] = ldg_stream(p + k * 512);
-      }
-      const int rb = it - sl * a.nrb;
-      const int row = rb * 32 + lane;
-      const float P0 = plane_sum(lane4, w[0], w[1]);
-      const float P1 = plane_sum(lane4, w[2], w[3]);
-      const float P2 = plane_sum(lane4, w[4], w[5]);
+      uint4 wn[6];
+      if (it + kWarps < s1) ld_item6(a.planes, it + kWarps, lane, wn);
+      const int row = (it - sl * a.nrb) * 32 + lane;
+      const float P0 = plane_sum(lane4, wa[0], wa[1]);
+      const float P1 = plane_sum(lane4, wa[2], wa[3]);
+      const float P2 = plane_sum(lane4, wa[4], wa[5]);
       const uint32_t pw = a.parity[(size_t)sl * a.rd.Rpad + row];
       float pacc = 0.f;
       for (int j = 0; j < nbk; ++j) pacc += ((pw >> j) & 1u) ? xb[j] : 0.f;
       // v = p + 2*b0 + 4*b1 - 8*b2 per weight
       a.rd.partial[(size_t)sl * a.rd.Rpad + row] = fmaf(2.f, P0, fmaf(4.f, P1, fmaf(-8.f, P2, pacc)));
-      if (arrive(a.rd, rb)) {
-        float v = gather(a.rd, 0, row);
-        for (uint32_t e = a.excptr[row]; e < a.excptr[row + 1]; ++e)
-          v = fmaf(16.f, __half2float(a.x[a.exccol[e]]), v);     // v = +8 stored as -8
-        float acc = __half2float(a.scale[row]) * a.inv_sqrt8 * v;
-        const int tbase = a.nblock * 24;
-        for (int j = 0; j < a.tail_n; ++j)
-          acc = fmaf(__half2float(a.tail[(size_t)row * a.tailpad + j]), __half2float(a.x[tbase + j]), acc);
-        if (row < a.R) a.y[row] = __float2half_rn(acc);
-      }
 #pragma unroll
-      for (int k = 0; k < 6; ++k) w[k] = n[k];
+      for (int k = 0; k < 6; ++k) wa[k] = wn[k];
     }
     s0 = s1;
   }
 }
 
 // ------------------------------------------------------- no-weights control
-// Same grid, table build, per-lane lookups and reduction as k_bpdq_b1; the
-// "weight" words are derived from the lane and item index instead of being
-// loaded, so the kernel reads x and writes y and the workspace only.
-__global__ void __launch_bounds__(kThreads, 1) k_noweights_b1(BpdqArgs a) {
+// Same grid, PDL, table build, per-lane lookups and handoff as k_bpdq_b1;
+// the "weight" words are derived from the lane and item index instead of
+// being loaded, so the kernel reads x and writes y and the workspace only.
+__global__ void __launch_bounds__(kThreads, 2) k_noweights_b1(BpdqArgs a) {
   float* T = reinterpret_cast<float*>(q2_smem);
   float* gsum = T + (kBuildBytes - 16) / 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t lane4 = lane * 4u;
   int i0, i1;
   cta_range(a.rd.nslice * a.nrb, i0, i1);
+  pdl_wait();
+  pdl_trigger();
   for (int s0 = i0; s0 < i1;) {
     const int g = s0 / a.nrb;
     const int s1 = min(i1, (g + 1) * a.nrb);
@@ -203,15 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_noweights_b1(BpdqArgs a) {
       const uint32_t h = (uint32_t)it * 0x9E3779B9u ^ (lane4 * 0x85EBCA6Bu);
       const uint4 w0 = make_uint4(h, h ^ 0x5bd1e995u, h * 3u, h * 5u);
       const uint4 w1 = make_uint4(h * 7u, h ^ 0x27d4eb2fu, h * 11u, h * 13u);
-      const int rb = it - g * a.nrb;
-      const int row = rb * 32 + lane;
+      const int row = (it - g * a.nrb) * 32 + lane;
       const float S0 = plane_sum(lane4, w0, w1);
       const float S1 = plane_sum(lane4, w1, w0);
       a.rd.partial[(size_t)g * a.rd.Rpad + row] = fmaf(0.02f, S0, fmaf(0.01f, S1, 0.01f * xg));
-      if (arrive(a.rd, rb)) {
-        const float v = gather(a.rd, 0, row);
-        if (row < a.R) a.y[row] = __float2half_rn(v);
-      }
     }
     s0 = s1;
   }
@@ -235,39 +228,35 @@ struct TrellisArgs {
 
 constexpr uint32_t kHashHi = 0x9E37u << 16;   // (s*0x9E37 mod 2^16) lands in bits 16..31
 
-__global__ void __launch_bounds__(kThreads, 1) k_trellis_b1(TrellisArgs a) {
+__device__ __forceinline__ void ld_trl(const unsigned char* base, int it, int lane, uint4 (&w)[4]) {
+  const unsigned char* p = base + (size_t)it * Q2_ITEM_BYTES_TRL + lane * 16;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) w[k] = ldg_stream(p + k * 512);
+}
+
+__global__ void __launch_bounds__(kThreads, 2) k_trellis_b1(TrellisArgs a) {
   uint32_t* tab = reinterpret_cast<uint32_t*>(q2_smem);                 // 16 KiB
   uint32_t* xs = reinterpret_cast<uint32_t*>(q2_smem + 4096 * 4);      // x as half2, C/2 words
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int i0, i1;
   cta_range(a.rd.nslice * a.nrb, i0, i1);
   int it = i0 + warp;
-  uint4 w0, w1, w2, w3;
-  if (it < i1) {
-    const unsigned char* p = a.stream + (size_t)it * Q2_ITEM_BYTES_TRL + lane * 16;
-    w0 = ldg_stream(p);
-    w1 = ldg_stream(p + 512);
-    w2 = ldg_stream(p + 1024);
-    w3 = ldg_stream(p + 1536);
-  }
+  uint4 wa[4], wb[4];
+  if (it < i1) ld_trl(a.stream, it, lane, wa);
+  if (it + kWarps < i1) ld_trl(a.stream, it + kWarps, lane, wb);
   for (int i = threadIdx.x; i < 4096; i += kThreads) tab[i] = a.table[i];
+  pdl_wait();
+  pdl_trigger();
   const uint32_t* xg = reinterpret_cast<const uint32_t*>(a.x);
   for (int i = threadIdx.x; i < a.C / 2; i += kThreads) xs[i] = xg[i];
   __syncthreads();
   for (; it < i1; it += kWarps) {
-    const int nx = it + kWarps;
-    uint4 n0, n1, n2, n3;
-    if (nx < i1) {
-      const unsigned char* p = a.stream + (size_t)nx * Q2_ITEM_BYTES_TRL + lane * 16;
-      n0 = ldg_stream(p);
-      n1 = ldg_stream(p + 512);
-      n2 = ldg_stream(p + 1024);
-      n3 = ldg_stream(p + 1536);
-    }
+    uint4 wc[4];
+    if (it + 2 * kWarps < i1) ld_trl(a.stream, it + 2 * kWarps, lane, wc);
     const int sg = it / a.nrb, rb = it - sg * a.nrb;
     const int row = rb * 32 + lane;
-    const uint32_t W[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
-                            w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+    const uint32_t W[16] = {wa[0].x, wa[0].y, wa[0].z, wa[0].w, wa[1].x, wa[1].y, wa[1].z, wa[1].w,
+                            wa[2].x, wa[2].y, wa[2].z, wa[2].w, wa[3].x, wa[3].y, wa[3].z, wa[3].w};
     const uint4* xv = reinterpret_cast<const uint4*>(xs + sg * 128);
     float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
@@ -292,30 +281,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_trellis_b1(TrellisArgs a) {
       }
     }
     a.rd.partial[(size_t)sg * a.rd.Rpad + row] = acc0 + acc1;
-    if (arrive(a.rd, rb)) {
-      const float v = gather(a.rd, 0, row);
-      if (row < a.R) a.y[row] = __float2half_rn(__half2float(a.scale[row]) * v);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      wa[k] = wb[k];
+      wb[k] = wc[k];
     }
-    w0 = n0; w1 = n1; w2 = n2; w3 = n3;
   }
 }
 
-template <typename K, typename A>
-int launch(K kernel, const A& args, int smem, int items, void* stream) {
-  const DevInfo di = dev_info();
-  if (set_smem(reinterpret_cast<const void*>(kernel), smem)) return Q2_ECUDA;
-  const int grid = max(1, min(items, di.sms));
-  kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(args);
-  return cudaGetLastError() == cudaSuccess ? Q2_OK : Q2_ECUDA;
+template <typename A>
+int launch(const q2_handle* h, void (*kernel)(A), const A& args, int smem, int items, const void* x, void* y,
+           void* stream) {
+  const int grid = max(1, min(items, dev_info().sms));
+  const int st = launch_pdl(kernel, args, grid, kThreads, smem, stream);
+  return st ? st : q2_launch_reduce(h, x, y, 1, stream);
 }
 
-Reduce make_reduce(const q2_handle* h, int ntok) {
+Reduce make_reduce(const q2_handle* h) {
   Reduce r;
-  r.counter = reinterpret_cast<unsigned*>(h->ws);
-  r.partial = reinterpret_cast<float*>(static_cast<unsigned char*>(h->ws) + q2_counter_bytes(h->hdr));
+  r.partial = static_cast<float*>(h->ws);
   r.nslice = h->hdr.nslice;
   r.Rpad = h->hdr.Rpad;
-  (void)ntok;
   return r;
 }
 
@@ -332,10 +318,10 @@ extern "C" int q2_b1_bpdq(const q2_handle* h, const void* x, void* y, void* stre
   a.off = reinterpret_cast<const __half*>(h->dev + d.off[SEC_BPDQ_OFF]);
   a.x = static_cast<const __half*>(x);
   a.y = static_cast<__half*>(y);
-  a.rd = make_reduce(h, 1);
+  a.rd = make_reduce(h);
   a.R = d.R;
   a.nrb = q2_nrb(d);
-  return launch(k_bpdq_b1, a, kBuildBytes, d.nslice * a.nrb, stream);
+  return launch(h, k_bpdq_b1, a, kBuildBytes, d.nslice * a.nrb, x, y, stream);
 }
 
 extern "C" int q2_b1_noweights(const q2_handle* h, const void* x, void* y, void* stream) {
@@ -343,10 +329,10 @@ extern "C" int q2_b1_noweights(const q2_handle* h, const void* x, void* y, void*
   BpdqArgs a = {};
   a.x = static_cast<const __half*>(x);
   a.y = static_cast<__half*>(y);
-  a.rd = make_reduce(h, 1);
+  a.rd = make_reduce(h);
   a.R = d.R;
   a.nrb = q2_nrb(d);
-  return launch(k_noweights_b1, a, kBuildBytes, d.nslice * a.nrb, stream);
+  return launch(h, k_noweights_b1, a, kBuildBytes, d.nslice * a.nrb, x, y, stream);
 }
 
 extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* stream) {
@@ -360,7 +346,7 @@ extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* str
   a.exccol = reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_LEECH_EXCCOL]);
   a.x = static_cast<const __half*>(x);
   a.y = static_cast<__half*>(y);
-  a.rd = make_reduce(h, 1);
+  a.rd = make_reduce(h);
   a.R = d.R;
   a.C = d.C;
   a.nrb = q2_nrb(d);
@@ -368,7 +354,7 @@ extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* str
   a.tail_n = d.tail;
   a.tailpad = d.tailpad;
   a.inv_sqrt8 = d.inv_sqrt8;
-  return launch(k_leech_b1, a, kBuildBytes + 64, d.nslice * a.nrb, stream);
+  return launch(h, k_leech_b1, a, kBuildBytes + 64, d.nslice * a.nrb, x, y, stream);
 }
 
 extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* stream) {
@@ -379,10 +365,10 @@ extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* s
   a.scale = reinterpret_cast<const __half*>(h->dev + d.off[SEC_TRL_SCALE]);
   a.x = static_cast<const __half*>(x);
   a.y = static_cast<__half*>(y);
-  a.rd = make_reduce(h, 1);
+  a.rd = make_reduce(h);
   a.R = d.R;
   a.C = d.C;
   a.nrb = q2_nrb(d);
   const int smem = 4096 * 4 + d.C * 2;
-  return launch(k_trellis_b1, a, smem, d.nslice * a.nrb, stream);
+  return launch(h, k_trellis_b1, a, smem, d.nslice * a.nrb, x, y, stream);
 }

@@ -3,6 +3,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "q2_internal.h"
 
 namespace q2 {
@@ -38,9 +40,11 @@ __device__ __forceinline__ unsigned short hi16(uint32_t v) { return (unsigned sh
 // For one 256-column slice of x, T[v][b] = sum of x[8b + i] over the set bits
 // i of the byte v (b = 0..31), stored twice per v (columns b and b + 32) so a
 // lane at rotated position P reads column P + lane without a modulo:
-// address = v*256 + lane*4 + P*4 bytes.  Built from two 16-entry nibble
-// tables.  Also returns the slice sum of x in *gsum.
-// Layout in shared memory: T (64 KiB) | lo[16][32] | hi[16][32] | xs[256].
+// address = v*256 + lane*4 + P*4 bytes.  Built in two phases: 64 threads
+// each load four x values and write the 16 subset sums of that nibble
+// (lo[n][b] for bits 0..3 of byte b, hi[n][b] for bits 4..7); then
+// T[v][b] = lo[v & 15][b] + hi[v >> 4][b].  Also returns the slice sum of x
+// in *gsum.  Layout in shared memory: T (64 KiB) | lo[16][32] | hi[16][32].
 constexpr int kTableBytes = 256 * 64 * 4;
 constexpr int kBuildBytes = kTableBytes + 2 * 16 * 32 * 4 + 256 * 4 + 16;
 
@@ -49,17 +53,24 @@ __device__ __forceinline__ void build_table(const __half* __restrict__ xg, int n
                                             float* gsum) {
   float* lo = T + 256 * 64;
   float* hi = lo + 16 * 32;
-  float* xs = hi + 16 * 32;
   const int t = threadIdx.x;
-  for (int c = t; c < 256; c += NT) xs[c] = (c < ncols) ? __half2float(xg[c]) : 0.f;
-  __syncthreads();
-  for (int e = t; e < 1024; e += NT) {
-    const int which = e >> 9, n = (e >> 5) & 15, b = e & 31;
-    const float* src = xs + 8 * b + 4 * which;
-    float v = 0.f;
+  if (t < 64) {
+    const int b = t & 31, half = t >> 5;
+    const int c0 = 8 * b + 4 * half;
+    float x4[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v += ((n >> i) & 1) ? src[i] : 0.f;
-    (which ? hi : lo)[n * 32 + b] = v;
+    for (int i = 0; i < 4; ++i) x4[i] = (c0 + i < ncols) ? __half2float(xg[c0 + i]) : 0.f;
+    float* dst = (half ? hi : lo) + b;
+    float s[16];
+    s[0] = 0.f;
+#pragma unroll
+    for (int n = 1; n < 16; ++n) {
+      const int low = n & -n;                       // lowest set bit
+      const int i = (low == 1) ? 0 : (low == 2) ? 1 : (low == 4) ? 2 : 3;
+      s[n] = s[n ^ low] + x4[i];
+    }
+#pragma unroll
+    for (int n = 0; n < 16; ++n) dst[n * 32] = s[n];
   }
   __syncthreads();
   // 256 v x 8 quads of b: thread -> (quad, vlo), loops over vhi
@@ -76,49 +87,51 @@ __device__ __forceinline__ void build_table(const __half* __restrict__ xg, int n
     *reinterpret_cast<float4*>(row + 4 * q) = s;
     *reinterpret_cast<float4*>(row + 32 + 4 * q) = s;
   }
-  if (t < 32) {
-    float v = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v += xs[8 * t + i];
+  if (t >= NT - 32) {                                // last warp: slice sum of x
+    const int b = t & 31;
+    float v = lo[15 * 32 + b] + hi[15 * 32 + b];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (t == 0) *gsum = v;
+    if (b == 0) *gsum = v;
   }
   __syncthreads();
 }
 
 // ---------------------------------------------------- split-K reduction
-// Each (slice, 32-row block) item writes fp32 partials for its rows; the
-// last warp to finish a row block (atomic counter) sums the partials of all
-// slices in slice order, so the result does not depend on scheduling, and
-// resets the counter to zero for the next call.  No thread waits.
+// Each (slice, 32-row block) item writes fp32 partials for its rows with
+// plain stores.  A second kernel (q2_reduce.cu), chained by programmatic
+// dependent launch, sums the partials of every output in slice order, so the
+// result does not depend on scheduling.
 struct Reduce {
   float* partial;      // [ntok][nslice][Rpad]
-  unsigned* counter;   // [nrb]
   int nslice;
   int Rpad;
 };
 
-// Returns true in every lane of the warp that must finish row block rb.
-__device__ __forceinline__ bool arrive(const Reduce& rd, int rb) {
-  __threadfence();
-  __syncwarp();
-  unsigned old = 0;
-  if ((threadIdx.x & 31) == 0) old = atomicAdd(rd.counter + rb, 1u);
-  old = __shfl_sync(0xffffffffu, old, 0);
-  const bool last = (old == (unsigned)rd.nslice - 1u);
-  if (last) {
-    __threadfence();
-    if ((threadIdx.x & 31) == 0) rd.counter[rb] = 0u;
-  }
-  return last;
-}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-__device__ __forceinline__ float gather(const Reduce& rd, int tok, int row) {
-  const float* p = rd.partial + (size_t)tok * rd.nslice * rd.Rpad + row;
-  float acc = 0.f;
-  for (int s = 0; s < rd.nslice; ++s) acc += __ldcg(p + (size_t)s * rd.Rpad);
-  return acc;
+// Launch with programmatic stream serialization allowed (PDL): the kernel
+// may start while the previous kernel on the stream drains; it must call
+// pdl_wait() before reading anything that kernel writes.
+template <typename A>
+int launch_pdl(void (*kernel)(A), const A& args, int grid, int threads, int smem, void* stream) {
+  if (set_smem(reinterpret_cast<const void*>(kernel), smem)) return Q2_ECUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, args) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return Q2_ECUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? Q2_OK : Q2_ECUDA;
 }
 
 // Contiguous share of n items for this CTA.

@@ -363,7 +363,7 @@ int q2_workspace_bytes(const q2_handle* h, int ntok, size_t* bytes) {
     *bytes = 0;
     return Q2_OK;
   }
-  *bytes = q2_counter_bytes(h->hdr) + (size_t)h->hdr.nslice * ntok * h->hdr.Rpad * 4;
+  *bytes = (size_t)h->hdr.nslice * ntok * h->hdr.Rpad * 4;
   return Q2_OK;
 }
 

@@ -12,11 +12,7 @@ struct q2_handle {
 
 static inline int q2_nrb(const q2_blob_header& h) { return h.Rpad / Q2_ROWS; }
 
-// Workspace layout: [counters: nrb x uint32, padded to 256 B][partials: fp32]
-static inline size_t q2_counter_bytes(const q2_blob_header& h) {
-  size_t b = (size_t)q2_nrb(h) * 4;
-  return (b + 255) & ~(size_t)255;
-}
+// Workspace layout: fp32 partials [ntok][nslice][Rpad].
 
 #ifdef __cplusplus
 extern "C" {

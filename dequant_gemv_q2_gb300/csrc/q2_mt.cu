@@ -11,6 +11,8 @@
 
 extern __shared__ __align__(1024) unsigned char q2_smem[];
 
+extern "C" int q2_launch_reduce(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
+
 namespace q2 {
 namespace {
 
@@ -50,6 +52,8 @@ __global__ void __launch_bounds__(kThreads) k_bpdq_mt(MtArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int i0, i1;
   cta_range(a.rd.nslice * a.nrb, i0, i1);
+  pdl_wait();
+  pdl_trigger();
   for (int s0 = i0; s0 < i1;) {
     const int g = s0 / a.nrb;
     const int s1 = min(i1, (g + 1) * a.nrb);
@@ -86,12 +90,6 @@ __global__ void __launch_bounds__(kThreads) k_bpdq_mt(MtArgs a) {
 #pragma unroll
       for (int t = 0; t < NT; ++t)
         if (t < a.ntok) a.rd.partial[((size_t)t * a.rd.nslice + g) * a.rd.Rpad + row] = acc[t];
-      if (arrive(a.rd, rb)) {
-        for (int t = 0; t < a.ntok; ++t) {
-          const float val = gather(a.rd, t, row);
-          if (row < a.R) a.y[(size_t)t * a.R + row] = __float2half_rn(val);
-        }
-      }
     }
     s0 = s1;
   }
@@ -104,6 +102,8 @@ __global__ void __launch_bounds__(kThreads) k_leech_mt(MtArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int i0, i1;
   cta_range(a.rd.nslice * a.nrb, i0, i1);
+  pdl_wait();
+  pdl_trigger();
   for (int s0 = i0; s0 < i1;) {
     const int sl = s0 / a.nrb;
     const int s1 = min(i1, (sl + 1) * a.nrb);
@@ -158,19 +158,6 @@ __global__ void __launch_bounds__(kThreads) k_leech_mt(MtArgs a) {
 #pragma unroll
       for (int t = 0; t < NT; ++t)
         if (t < a.ntok) a.rd.partial[((size_t)t * a.rd.nslice + sl) * a.rd.Rpad + row] = acc[t];
-      if (arrive(a.rd, rb)) {
-        const float sc = __half2float(a.scale[row]) * a.inv_sqrt8;
-        for (int t = 0; t < a.ntok; ++t) {
-          const __half* xt = a.x + (size_t)t * a.C;
-          float v = gather(a.rd, t, row);
-          for (uint32_t e = a.excptr[row]; e < a.excptr[row + 1]; ++e)
-            v = fmaf(16.f, __half2float(xt[a.exccol[e]]), v);
-          float o = sc * v;
-          for (int j = 0; j < a.tail_n; ++j)
-            o = fmaf(__half2float(a.tail[(size_t)row * a.tailpad + j]), __half2float(xt[a.nblock * 24 + j]), o);
-          if (row < a.R) a.y[(size_t)t * a.R + row] = __float2half_rn(o);
-        }
-      }
     }
     s0 = s1;
   }
@@ -186,6 +173,8 @@ __global__ void __launch_bounds__(kThreads) k_trellis_mt(MtArgs a) {
   for (int i = threadIdx.x; i < 4096; i += kThreads) tab[i] = a.table[i];
   int i0, i1;
   cta_range(a.rd.nslice * a.nrb, i0, i1);
+  pdl_wait();
+  pdl_trigger();
   for (int s0 = i0; s0 < i1;) {
     const int sg = s0 / a.nrb;
     const int s1 = min(i1, (sg + 1) * a.nrb);
@@ -223,13 +212,6 @@ __global__ void __launch_bounds__(kThreads) k_trellis_mt(MtArgs a) {
 #pragma unroll
       for (int t = 0; t < NT; ++t)
         if (t < a.ntok) a.rd.partial[((size_t)t * a.rd.nslice + sg) * a.rd.Rpad + row] = acc[t];
-      if (arrive(a.rd, rb)) {
-        const float sc = __half2float(a.scale[row]);
-        for (int t = 0; t < a.ntok; ++t) {
-          const float v = gather(a.rd, t, row);
-          if (row < a.R) a.y[(size_t)t * a.R + row] = __float2half_rn(sc * v);
-        }
-      }
     }
     s0 = s1;
   }
@@ -237,8 +219,7 @@ __global__ void __launch_bounds__(kThreads) k_trellis_mt(MtArgs a) {
 
 Reduce make_reduce(const q2_handle* h) {
   Reduce r;
-  r.counter = reinterpret_cast<unsigned*>(h->ws);
-  r.partial = reinterpret_cast<float*>(static_cast<unsigned char*>(h->ws) + q2_counter_bytes(h->hdr));
+  r.partial = static_cast<float*>(h->ws);
   r.nslice = h->hdr.nslice;
   r.Rpad = h->hdr.Rpad;
   return r;
@@ -246,24 +227,10 @@ Reduce make_reduce(const q2_handle* h) {
 
 template <int NT>
 int launch_nt(int fmt, const MtArgs& a, int items, void* stream) {
-  const DevInfo di = dev_info();
-  const int grid = max(1, min(items, 2 * di.sms));
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int smem = 0;
-  if (fmt == Q2_BPDQ) {
-    smem = NT * 256 * 4;
-    if (set_smem(reinterpret_cast<const void*>(k_bpdq_mt<NT>), smem)) return Q2_ECUDA;
-    k_bpdq_mt<NT><<<grid, kThreads, smem, st>>>(a);
-  } else if (fmt == Q2_LEECH) {
-    smem = 64 * 256 * 4 + 11 * 64 * 4;
-    if (set_smem(reinterpret_cast<const void*>(k_leech_mt<NT>), smem)) return Q2_ECUDA;
-    k_leech_mt<NT><<<grid, kThreads, smem, st>>>(a);
-  } else {
-    smem = 4096 * 4 + NT * 256 * 4;
-    if (set_smem(reinterpret_cast<const void*>(k_trellis_mt<NT>), smem)) return Q2_ECUDA;
-    k_trellis_mt<NT><<<grid, kThreads, smem, st>>>(a);
-  }
-  return cudaGetLastError() == cudaSuccess ? Q2_OK : Q2_ECUDA;
+  const int grid = max(1, min(items, 2 * dev_info().sms));
+  if (fmt == Q2_BPDQ) return launch_pdl(k_bpdq_mt<NT>, a, grid, kThreads, NT * 256 * 4, stream);
+  if (fmt == Q2_LEECH) return launch_pdl(k_leech_mt<NT>, a, grid, kThreads, 64 * 256 * 4 + 11 * 64 * 4, stream);
+  return launch_pdl(k_trellis_mt<NT>, a, grid, kThreads, 4096 * 4 + NT * 256 * 4, stream);
 }
 
 }  // namespace
@@ -307,9 +274,11 @@ extern "C" int q2_mt_launch(const q2_handle* h, const void* x, void* y, int ntok
       return Q2_EFMT;
   }
   const int items = d.nslice * a.nrb;
-  if (ntok <= 4) return launch_nt<4>(d.fmt, a, items, stream);
-  if (ntok <= 8) return launch_nt<8>(d.fmt, a, items, stream);
-  if (ntok <= 16) return launch_nt<16>(d.fmt, a, items, stream);
-  if (ntok <= 32) return launch_nt<32>(d.fmt, a, items, stream);
-  return launch_nt<64>(d.fmt, a, items, stream);
+  int st;
+  if (ntok <= 4) st = launch_nt<4>(d.fmt, a, items, stream);
+  else if (ntok <= 8) st = launch_nt<8>(d.fmt, a, items, stream);
+  else if (ntok <= 16) st = launch_nt<16>(d.fmt, a, items, stream);
+  else if (ntok <= 32) st = launch_nt<32>(d.fmt, a, items, stream);
+  else st = launch_nt<64>(d.fmt, a, items, stream);
+  return st ? st : q2_launch_reduce(h, x, y, ntok, stream);
 }

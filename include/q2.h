@@ -118,9 +118,10 @@ int q2_pack_noweights(int R, int C, void* out, size_t* out_bytes);
 int q2_bind(const void* blob_host, const void* blob_dev, q2_handle** h);
 void q2_unbind(q2_handle* h);
 
-/* Split-K workspace: device memory owned by the caller, zero-filled before
- * its first use and left zeroed by every completed call.  One workspace may
- * serve many handles whose calls are ordered on one stream. */
+/* Split-K workspace: device memory owned by the caller (fp32 partial sums,
+ * nslice x ntok x Rpad floats; no initial contents needed).  One workspace
+ * may serve many handles whose calls are ordered on one stream; calls that
+ * overlap on the GPU must use different workspaces. */
 int q2_workspace_bytes(const q2_handle* h, int ntok, size_t* bytes);
 int q2_set_workspace(q2_handle* h, void* ws_dev, size_t ws_bytes);
 
@@ -134,7 +135,9 @@ int q2_bytes(const q2_handle* h, int ntok, size_t* weight_bytes_read_per_call);
  * [ntok][C]; y: device fp16 [ntok][R]; both 16-byte aligned; 1 <= ntok <= 64.
  * Asynchronous and ordered on `stream`; never synchronises.  Needs the
  * workspace of q2_workspace_bytes(h, ntok) bound first (0 bytes for fp16).
- * Returns Q2_ECUDA if the launch fails. */
+ * The packed formats run as two launches (partial sums, then an in-order
+ * reduction with the epilogue), chained by programmatic dependent launch.
+ * Returns Q2_ECUDA if a launch fails. */
 int q2_gemv(q2_fmt fmt, const q2_handle* h, const void* x, void* y, int ntok, q2_stream stream);
 
 /* Debug decode to the canonical form (all formats but Q2_NOWEIGHTS):
