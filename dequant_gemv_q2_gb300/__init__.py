@@ -59,6 +59,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "q2_gemv": [i32, vp, vp, vp, i32, vp],
         "q2_decode_bytes": [vp, psz],
         "q2_decode": [vp, vp, vp],
+        "q2_gemv_bpdq_noalloc": [vp, vp, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -74,7 +75,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
 
 EXPORTS = ["q2_pack_fp16", "q2_pack_bpdq", "q2_pack_trellis", "q2_pack_leech", "q2_pack_noweights",
            "q2_bind", "q2_unbind", "q2_workspace_bytes", "q2_set_workspace", "q2_info", "q2_bytes",
-           "q2_gemv", "q2_decode_bytes", "q2_decode", "q2_strerror"]
+           "q2_gemv", "q2_decode_bytes", "q2_decode", "q2_strerror", "q2_gemv_bpdq_noalloc"]
 
 
 def q2_strerror(status: int) -> str:

@@ -21,6 +21,9 @@
 // the next GEMV's CTAs get scheduled while it runs.
 #include <cuda_fp16.h>
 
+#include <mutex>
+#include <vector>
+
 #include "q2_common.cuh"
 
 extern __shared__ __align__(1024) unsigned char q2_smem[];
@@ -371,4 +374,67 @@ extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* s
   a.nrb = q2_nrb(d);
   const int smem = 4096 * 4 + d.C * 2;
   return launch(h, k_trellis_b1, a, smem, d.nslice * a.nrb, x, y, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free batch-1 BPDQ entry point.
+//
+// Some callers cannot allocate device memory when they call the GEMV: code
+// that runs while a CUDA stream is being captured into a graph (cudaMalloc
+// is not permitted there), plugins whose host framework owns all device
+// memory and offers them no allocator, and real-time decode loops that must
+// not touch the allocator after start-up.  q2_gemv_bpdq_noalloc serves them:
+// the split-K partial sums that q2_gemv keeps in a caller-bound workspace go
+// to a scratch array that belongs to this library instead, so the caller
+// passes only the handle, x, y and a stream.  Every GPU that loads the
+// library holds the array (Q2_NOALLOC_SCRATCH_BYTES) until the process exits.
+
+namespace {
+
+// Device memory for the partial sums; host code must never hand this symbol
+// to a kernel (on the host it only stands in for the device address).
+static __device__ __align__(256) unsigned char q2_noalloc_scratch[Q2_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+std::vector<void*> g_noalloc_ptr;   // device address of the scratch, per device
+
+// The device address of the scratch on the current device, looked up once
+// per device (cudaGetSymbolAddress with that device current).
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return Q2_ECUDA;
+  }
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if ((int)g_noalloc_ptr.size() <= dev) g_noalloc_ptr.resize(dev + 1, nullptr);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, q2_noalloc_scratch) != cudaSuccess || !p) {
+      (void)cudaGetLastError();
+      return Q2_ECUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return Q2_OK;
+}
+
+}  // namespace
+
+extern "C" int q2_gemv_bpdq_noalloc(const q2_handle* h, const void* x, void* y, q2_stream stream) {
+  if (!h || !x || !y) return Q2_EINVAL;
+  if (h->hdr.fmt != Q2_BPDQ) return Q2_EFMT;
+  if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(y) % 16) return Q2_EALIGN;
+  const size_t need = (size_t)h->hdr.nslice * h->hdr.Rpad * 4;
+  if (need > (size_t)Q2_NOALLOC_SCRATCH_BYTES) return Q2_ESCRATCH;
+  void* scratch = nullptr;
+  const int st = noalloc_scratch(&scratch);
+  if (st) return st;
+  // the same two launches as q2_gemv at ntok = 1, with the scratch in place
+  // of the caller's workspace; nothing in the scratch needs to start at zero
+  q2_handle view = *h;
+  view.ws = scratch;
+  view.ws_bytes = Q2_NOALLOC_SCRATCH_BYTES;
+  return q2_b1_bpdq(&view, x, y, static_cast<void*>(stream));
 }

@@ -121,6 +121,7 @@ const char* q2_strerror(int status) {
     case Q2_ECUDA: return "CUDA call or kernel launch failed";
     case Q2_ENOMEM: return "host allocation failed";
     case Q2_ESIZE: return "output buffer too small";
+    case Q2_ESCRATCH: return "problem larger than the built-in scratch (Q2_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown status";
   }
 }

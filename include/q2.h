@@ -62,7 +62,8 @@ enum {
   Q2_EWORKSPACE = -7,  /* no workspace bound, or smaller than needed       */
   Q2_ECUDA = -8,       /* a CUDA call or kernel launch failed              */
   Q2_ENOMEM = -9,      /* host allocation failed                           */
-  Q2_ESIZE = -10       /* caller's buffer smaller than required            */
+  Q2_ESIZE = -10,      /* caller's buffer smaller than required            */
+  Q2_ESCRATCH = -11    /* problem too large for the built-in scratch       */
 };
 
 typedef struct q2_handle q2_handle;   /* opaque; owns no device memory */
@@ -139,6 +140,31 @@ int q2_bytes(const q2_handle* h, int ntok, size_t* weight_bytes_read_per_call);
  * reduction with the epilogue), chained by programmatic dependent launch.
  * Returns Q2_ECUDA if a launch fails. */
 int q2_gemv(q2_fmt fmt, const q2_handle* h, const void* x, void* y, int ntok, q2_stream stream);
+
+/* Allocation-free y = W x for a BPDQ handle at one token (no counterpart on
+ * the source pages; an addition of this library).  For callers that cannot
+ * allocate device memory when they run the GEMV: code running under CUDA
+ * stream capture, plugins whose host framework owns the device memory, and
+ * real-time loops that must not call the allocator.  It does what q2_gemv
+ * does at ntok == 1, but keeps the split-K partial sums in a scratch array
+ * that the library owns (a file-scope __device__ array of
+ * Q2_NOALLOC_SCRATCH_BYTES = 4 MiB, held on every GPU that loads the
+ * library until the process exits) instead of a workspace bound with
+ * q2_set_workspace.  It calls no cudaMalloc or cudaFree.
+ *   - x: device fp16 [C]; y: device fp16 [R]; both 16-byte aligned.
+ *   - Needs nslice * Rpad * 4 bytes of scratch (C/256 groups x R rounded up
+ *     to 32 rows); larger problems return Q2_ESCRATCH.  Every Qwen3-8B and
+ *     -14B linear fits.
+ *   - The first call on a device looks up the scratch's device address
+ *     (cudaGetSymbolAddress, once per device); make that first call before
+ *     any stream capture.
+ *   - All calls in a process share the one scratch array of a GPU: two
+ *     calls that can run at the same time on that GPU (streams with no
+ *     ordering between them) race and corrupt each other's results, so
+ *     order them on one stream.  Nothing in the scratch needs to start at
+ *     zero; it keeps the last call's partial sums. */
+#define Q2_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)
+int q2_gemv_bpdq_noalloc(const q2_handle* h, const void* x, void* y, q2_stream stream);
 
 /* Debug decode to the canonical form (all formats but Q2_NOWEIGHTS):
  *   fp16:    fp16 [R][C]
