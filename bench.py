@@ -34,9 +34,13 @@ HIDDEN, QKV, INTER, LAYERS = 4096, 6144, 12288, 36
 SHAPES_8B = [("qkv", QKV, HIDDEN), ("o", HIDDEN, HIDDEN), ("gate_up", 2 * INTER, HIDDEN), ("down", HIDDEN, INTER)]
 L2_BYTES = 126 * 1024 * 1024
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch from the ncu
-# capture summarised in profiles/ (None until captured for the current kernel)
-NCU_TRAFFIC = {}
+# DRAM traffic of the dominant kernel from the ncu capture summarised in
+# profiles/bpdq_b1_qwen3_8b_stack.md: (dram__bytes_read.sum +
+# dram__bytes_write.sum) / algorithmic bytes on a 24576x4096 launch.  The
+# stack's traffic per launch is that ratio times the stack's algorithmic
+# bytes per launch (traffic scales with the items processed).  Must be reset
+# to None whenever the kernel changes.
+NCU_TRAFFIC_RATIO = {"k_bpdq_b1": 27552768 / 27525120}
 
 
 def _peaks():
@@ -423,7 +427,9 @@ def main():
                        "l2": "weights 1.9 GB > L2, no flush", "parallelism": "replicas" if ws > 1 else "single"},
             "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                         "traffic": NCU_TRAFFIC.get(kname)},
+                         "traffic": (round(NCU_TRAFFIC_RATIO[kname] * step_bytes / len(lin))
+                                     if NCU_TRAFFIC_RATIO.get(kname) else None),
+                         "traffic_unit": "bytes per launch"},
             "gpu_launches": len(lin) * args.steps,
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -67,6 +67,27 @@ __device__ __forceinline__ void ld_item4(const unsigned char* base, int it, int 
   for (int k = 0; k < 4; ++k) w[k] = ldg_stream(p + k * 512);
 }
 
+// The CTA's items are contiguous in the bit stream, and the coefficients of a
+// slice's row blocks are contiguous too: thread 0 prefetches all of them
+// into L2 before waiting on the previous kernel, so the weight stream of
+// this GEMV overlaps the tail of the previous one.
+__device__ __forceinline__ void prefetch_items(const unsigned char* base, int item_bytes, int i0, int i1) {
+  if (i1 > i0) prefetch_l2(base + (size_t)i0 * item_bytes, (size_t)(i1 - i0) * item_bytes);
+}
+
+__device__ __forceinline__ void prefetch_rows(const void* base, int elem_bytes, int nrb, int Rpad, int i0, int i1) {
+  // rows of items i0..i1-1 in [slice][Rpad] arrays: one contiguous run per slice
+  for (int s0 = i0; s0 < i1;) {
+    const int g = s0 / nrb, s1 = min(i1, (g + 1) * nrb);
+    const size_t first = (size_t)g * Rpad + (size_t)(s0 - g * nrb) * 32;
+    const size_t n = (size_t)(s1 - s0) * 32 * elem_bytes;
+    const size_t a0 = (first * elem_bytes) & ~(size_t)15;
+    const size_t a1 = (first * elem_bytes + n + 15) & ~(size_t)15;
+    prefetch_l2(static_cast<const char*>(base) + a0, a1 - a0);
+    s0 = s1;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 2) k_bpdq_b1(BpdqArgs a) {
   float* T = reinterpret_cast<float*>(q2_smem);
   float* gsum = T + (kBuildBytes - 16) / 4;
@@ -74,14 +95,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_bpdq_b1(BpdqArgs a) {
   const uint32_t lane4 = lane * 4u;
   int i0, i1;
   cta_range(a.rd.nslice * a.nrb, i0, i1);
+  if (threadIdx.x == 0) {
+    prefetch_items(a.bits, Q2_ITEM_BYTES_BPDQ, i0, i1);
+    prefetch_rows(a.c01, 4, a.nrb, a.rd.Rpad, i0, i1);
+    prefetch_rows(a.off, 2, a.nrb, a.rd.Rpad, i0, i1);
+  }
   bool waited = false;
   for (int s0 = i0; s0 < i1;) {
     const int g = s0 / a.nrb;
     const int s1 = min(i1, (g + 1) * a.nrb);
     int it = s0 + warp;
-    uint4 wa[4], wb[4];
+    uint4 wa[4];
     if (it < s1) ld_item4(a.bits, it, lane, wa);
-    if (it + kWarps < s1) ld_item4(a.bits, it + kWarps, lane, wb);
     if (!waited) {
       pdl_wait();
       pdl_trigger();
@@ -91,8 +116,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_bpdq_b1(BpdqArgs a) {
     build_table<kThreads>(a.x + (size_t)g * Q2_SLICE, Q2_SLICE, T, gsum);
     const float xg = *gsum;
     for (; it < s1; it += kWarps) {
-      uint4 wc[4];
-      if (it + 2 * kWarps < s1) ld_item4(a.bits, it + 2 * kWarps, lane, wc);
+      uint4 wb[4];
+      if (it + kWarps < s1) ld_item4(a.bits, it + kWarps, lane, wb);
       const int row = (it - g * a.nrb) * 32 + lane;
       const float S0 = plane_sum(lane4, wa[0], wa[1]);
       const float S1 = plane_sum(lane4, wa[2], wa[3]);
@@ -100,10 +125,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_bpdq_b1(BpdqArgs a) {
       const float of = __half2float(a.off[(size_t)g * a.rd.Rpad + row]);
       a.rd.partial[(size_t)g * a.rd.Rpad + row] = fmaf(c.x, S0, fmaf(c.y, S1, of * xg));
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        wa[k] = wb[k];
-        wb[k] = wc[k];
-      }
+      for (int k = 0; k < 4; ++k) wa[k] = wb[k];
     }
     s0 = s1;
   }
@@ -138,6 +160,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_leech_b1(LeechArgs a) {
   const uint32_t lane4 = lane * 4u;
   int i0, i1;
   cta_range(a.rd.nslice * a.nrb, i0, i1);
+  if (threadIdx.x == 0) {
+    prefetch_items(a.planes, Q2_ITEM_BYTES_LEECH, i0, i1);
+    prefetch_rows(a.parity, 2, a.nrb, a.rd.Rpad, i0, i1);
+  }
   bool waited = false;
   for (int s0 = i0; s0 < i1;) {
     const int sl = s0 / a.nrb;
@@ -243,10 +269,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_trellis_b1(TrellisArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int i0, i1;
   cta_range(a.rd.nslice * a.nrb, i0, i1);
+  if (threadIdx.x == 0) prefetch_items(a.stream, Q2_ITEM_BYTES_TRL, i0, i1);
   int it = i0 + warp;
-  uint4 wa[4], wb[4];
+  uint4 wa[4];
   if (it < i1) ld_trl(a.stream, it, lane, wa);
-  if (it + kWarps < i1) ld_trl(a.stream, it + kWarps, lane, wb);
   for (int i = threadIdx.x; i < 4096; i += kThreads) tab[i] = a.table[i];
   pdl_wait();
   pdl_trigger();
@@ -254,8 +280,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_trellis_b1(TrellisArgs a) {
   for (int i = threadIdx.x; i < a.C / 2; i += kThreads) xs[i] = xg[i];
   __syncthreads();
   for (; it < i1; it += kWarps) {
-    uint4 wc[4];
-    if (it + 2 * kWarps < i1) ld_trl(a.stream, it + 2 * kWarps, lane, wc);
+    uint4 wb[4];
+    if (it + kWarps < i1) ld_trl(a.stream, it + kWarps, lane, wb);
     const int sg = it / a.nrb, rb = it - sg * a.nrb;
     const int row = rb * 32 + lane;
     const uint32_t W[16] = {wa[0].x, wa[0].y, wa[0].z, wa[0].w, wa[1].x, wa[1].y, wa[1].z, wa[1].w,
@@ -285,10 +311,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_trellis_b1(TrellisArgs a) {
     }
     a.rd.partial[(size_t)sg * a.rd.Rpad + row] = acc0 + acc1;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      wa[k] = wb[k];
-      wb[k] = wc[k];
-    }
+    for (int k = 0; k < 4; ++k) wa[k] = wb[k];
   }
 }
 

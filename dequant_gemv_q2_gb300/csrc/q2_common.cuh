@@ -26,6 +26,17 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   return v;
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, multiple of 16),
+// issued by one thread in 64 KiB pieces; no registers or shared memory are
+// held while the bytes arrive.
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
+  const char* c = static_cast<const char*>(p);
+  for (size_t off = 0; off < bytes; off += 65536) {
+    const uint32_t n = (uint32_t)((bytes - off) < 65536 ? (bytes - off) : 65536);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + off), "r"(n) : "memory");
+  }
+}
+
 // acc += f16 * f16 in fp32 (mixed-precision FMA, sm_100+ PTX)
 __device__ __forceinline__ float fma_h(unsigned short a, unsigned short b, float c) {
   float d;
@@ -40,59 +51,58 @@ __device__ __forceinline__ unsigned short hi16(uint32_t v) { return (unsigned sh
 // For one 256-column slice of x, T[v][b] = sum of x[8b + i] over the set bits
 // i of the byte v (b = 0..31), stored twice per v (columns b and b + 32) so a
 // lane at rotated position P reads column P + lane without a modulo:
-// address = v*256 + lane*4 + P*4 bytes.  Built in two phases: 64 threads
-// each load four x values and write the 16 subset sums of that nibble
-// (lo[n][b] for bits 0..3 of byte b, hi[n][b] for bits 4..7); then
-// T[v][b] = lo[v & 15][b] + hi[v >> 4][b].  Also returns the slice sum of x
-// in *gsum.  Layout in shared memory: T (64 KiB) | lo[16][32] | hi[16][32].
+// address = v*256 + lane*4 + P*4 bytes.  Each of 512 (column-byte b, high
+// nibble h) tasks loads the 8 x values of byte b, forms the 16 sums of its
+// low nibble by doubling, adds the sum selected by h, and writes the 16
+// entries T[16h + l][b] (consecutive b across a warp: conflict-free stores).
+// Also returns the slice sum of x in *gsum.
 constexpr int kTableBytes = 256 * 64 * 4;
-constexpr int kBuildBytes = kTableBytes + 2 * 16 * 32 * 4 + 256 * 4 + 16;
+constexpr int kBuildBytes = kTableBytes + 16;
 
 template <int NT>
 __device__ __forceinline__ void build_table(const __half* __restrict__ xg, int ncols, float* T,
                                             float* gsum) {
-  float* lo = T + 256 * 64;
-  float* hi = lo + 16 * 32;
-  const int t = threadIdx.x;
-  if (t < 64) {
-    const int b = t & 31, half = t >> 5;
-    const int c0 = 8 * b + 4 * half;
-    float x4[4];
+  for (int e = threadIdx.x; e < 512; e += NT) {
+    const int b = e & 31, h = e >> 5;
+    const int c0 = 8 * b;
+    float x8[8];
+    if (c0 + 8 <= ncols) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(xg + c0);
+      const __half2* hv = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) x4[i] = (c0 + i < ncols) ? __half2float(xg[c0 + i]) : 0.f;
-    float* dst = (half ? hi : lo) + b;
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __half22float2(hv[k]);
+        x8[2 * k] = f.x;
+        x8[2 * k + 1] = f.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x8[i] = (c0 + i < ncols) ? __half2float(xg[c0 + i]) : 0.f;
+    }
+    // sum selected by the high nibble h (bits 4..7)
+    float hs = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) hs += ((h >> i) & 1) ? x8[4 + i] : 0.f;
     float s[16];
-    s[0] = 0.f;
+    s[0] = hs;
 #pragma unroll
     for (int n = 1; n < 16; ++n) {
-      const int low = n & -n;                       // lowest set bit
+      const int low = n & -n;
       const int i = (low == 1) ? 0 : (low == 2) ? 1 : (low == 4) ? 2 : 3;
-      s[n] = s[n ^ low] + x4[i];
+      s[n] = s[n ^ low] + x8[i];
     }
+    float* col = T + (h * 16) * 64 + b;
 #pragma unroll
-    for (int n = 0; n < 16; ++n) dst[n * 32] = s[n];
-  }
-  __syncthreads();
-  // 256 v x 8 quads of b: thread -> (quad, vlo), loops over vhi
-  for (int e = t; e < 16 * 16 * 8; e += NT) {
-    const int q = e & 7, vlo = (e >> 3) & 15, vhi = e >> 7;
-    const float4 a = *reinterpret_cast<const float4*>(lo + vlo * 32 + 4 * q);
-    const float4 bq = *reinterpret_cast<const float4*>(hi + vhi * 32 + 4 * q);
-    float4 s;
-    s.x = a.x + bq.x;
-    s.y = a.y + bq.y;
-    s.z = a.z + bq.z;
-    s.w = a.w + bq.w;
-    float* row = T + (vhi * 16 + vlo) * 64;
-    *reinterpret_cast<float4*>(row + 4 * q) = s;
-    *reinterpret_cast<float4*>(row + 32 + 4 * q) = s;
-  }
-  if (t >= NT - 32) {                                // last warp: slice sum of x
-    const int b = t & 31;
-    float v = lo[15 * 32 + b] + hi[15 * 32 + b];
+    for (int n = 0; n < 16; ++n) {
+      col[n * 64] = s[n];
+      col[n * 64 + 32] = s[n];
+    }
+    if (h == 15) {                               // this warp holds all 32 bytes' full sums
+      float v = s[15];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (b == 0) *gsum = v;
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (b == 0) *gsum = v;
+    }
   }
   __syncthreads();
 }

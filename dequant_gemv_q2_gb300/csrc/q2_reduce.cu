@@ -16,7 +16,7 @@
 namespace q2 {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;   // small CTAs: they co-reside with two GEMV CTAs on an SM
 
 struct RedArgs {
   const float* partial;      // [ntok][nslice][Rpad]
