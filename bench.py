@@ -225,6 +225,112 @@ def per_format(q2, stream, hbm):
     return out
 
 
+SHAPES_14B = [("qkv", 7168, 5120), ("o", 5120, 5120), ("gate_up", 34816, 5120), ("down", 5120, 17408)]
+LAYERS_14B = 40
+
+
+def _leech_pool_matrix(R: int, C: int, seed: int, pool: np.ndarray) -> dict:
+    """Leech weights whose blocks are drawn uniformly from a pool of points
+    sampled exactly (uniform shell, uniform within shell); used only for the
+    14B sweep, where exact sampling of every block would take hours."""
+    import synth
+    rng = np.random.default_rng((seed, 7))
+    nb = C // 24
+    idx = rng.integers(0, pool.shape[0], size=(R, nb))
+    v = pool[idx]
+    scale = rng.uniform(0.005, 0.03, size=R).astype(np.float16)
+    tail = rng.normal(0.0, 0.01, size=(R, C % 24)).astype(np.float16)
+    return {"v": v, "scale": scale, "tail": tail}
+
+
+def sweep(args):
+    """Config 4: Qwen3-14B-shaped stack (40 layers x qkv/o/gate_up/down) in each
+    format, ntok in {1,2,4,8,16,32,64}; `distinct` layer copies are cycled
+    through the 40 layers (their footprint is several times L2)."""
+    import torch
+    import dequant_gemv_q2_gb300 as q2
+    import synth
+    q2.load()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    ntoks = [int(t) for t in args.sweep_ntok.split(",")]
+    distinct = args.sweep_distinct
+    pool = None
+    results = {}
+    for fmt in args.sweep_formats.split(","):
+        mats = []                                   # per distinct layer: 4 Packed
+        for layer in range(distinct):
+            row = []
+            for j, (name, R, C) in enumerate(SHAPES_14B):
+                seed = 4000 + 4 * layer + j
+                if fmt in ("fp16", "cublas"):
+                    g = torch.Generator(device="cuda").manual_seed(seed)
+                    w = torch.randn((R, C), generator=g, device="cuda").mul_(0.02).half()
+                    if fmt == "cublas":
+                        row.append(("cublas", w, R, C))
+                        continue
+                    blob = q2.q2_pack_fp16(np.zeros((R, C), dtype=np.float16))
+                    pk = q2.Packed(blob, ntok_max=max(ntoks))
+                    off = int(np.frombuffer(blob[56:64].tobytes(), dtype="<u8")[0])
+                    pk.dev[off:off + R * C * 2].copy_(w.view(-1).view(torch.uint8))
+                    del w
+                elif fmt == "bpdq":
+                    d = synth.bpdq(R, C, seed)
+                    pk = q2.Packed(q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]), ntok_max=max(ntoks),
+                                   workspace=torch.zeros(16, dtype=torch.uint8, device="cuda"))
+                elif fmt == "trellis":
+                    d = synth.trellis(R, C, seed)
+                    pk = q2.Packed(q2.q2_pack_trellis(d["stream"], d["table"], d["scale"]), ntok_max=max(ntoks),
+                                   workspace=torch.zeros(16, dtype=torch.uint8, device="cuda"))
+                else:
+                    if pool is None:
+                        pool = synth._sample_shell(np.random.default_rng(4242),
+                                                   np.random.default_rng(4243).integers(2, 7, size=2_000_000))
+                    d = _leech_pool_matrix(R, C, seed, pool)
+                    pk = q2.Packed(q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C), ntok_max=max(ntoks),
+                                   workspace=torch.zeros(16, dtype=torch.uint8, device="cuda"))
+                row.append(pk)
+            mats.append(row)
+        if fmt != "cublas" and fmt != "fp16":
+            need = max(p.workspace_bytes(max(ntoks)) for row in mats for p in row)
+            wsbuf = torch.zeros(need, dtype=torch.uint8, device="cuda")
+            for row in mats:
+                for p in row:
+                    p.set_workspace(wsbuf)
+        layer_bytes = 0
+        if fmt == "cublas":
+            layer_bytes = sum(R * C * 2 for _, R, C in SHAPES_14B)
+        results[fmt] = {}
+        for nt in ntoks:
+            xs = {C: torch.from_numpy(synth.activations(nt, C, 9)).cuda() for _, _, C in SHAPES_14B}
+            ys = {R: torch.empty((nt, R), dtype=torch.float16, device="cuda") for _, R, _ in SHAPES_14B}
+            calls = []
+            for layer in range(LAYERS_14B):
+                for j, (name, R, C) in enumerate(SHAPES_14B):
+                    item = mats[layer % distinct][j]
+                    if fmt == "cublas":
+                        w = item[1]
+                        calls.append(lambda w=w, x=xs[C], y=ys[R]: torch.matmul(x, w.t(), out=y))
+                    else:
+                        calls.append(lambda p=item, x=xs[C], y=ys[R]: p.gemv(x, y))
+            g = graph_of(calls, stream)
+            ms = time_graph(g, stream, args.sweep_steps, 3)
+            step_ms = ms / args.sweep_steps
+            if fmt == "cublas":
+                step_bytes = layer_bytes * LAYERS_14B
+            else:
+                step_bytes = sum(mats[l % distinct][j].bytes_read(nt) for l in range(LAYERS_14B) for j in range(4))
+            gbs = step_bytes / (step_ms * 1e-3) / 1e9
+            results[fmt][nt] = {"ms_per_step": round(step_ms, 4), "tok_s": round(nt / (step_ms * 1e-3), 1),
+                                "gbs": round(gbs, 1), "bytes_per_step": step_bytes}
+            del g, calls
+        del mats
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": "Qwen3-14B-shaped stack, 40 layers x (qkv 5120->7168, o 5120->5120, "
+                               "gate_up 5120->34816, down 17408->5120), linears only",
+                      "distinct_layer_copies": distinct, "results": results}), flush=True)
+
+
 def cpu_oracle_sample(seconds_target: float = 15.0) -> dict:
     """Oracle (decode + f64 matvec) on o-projection-shaped BPDQ matrices;
     returns seconds per weight and what was sampled.  Run in a subprocess
@@ -288,7 +394,7 @@ def run_reference(args, ws, rank):
     }), flush=True)
 
 
-def profile_case(fmt: str, launches: int = 4):
+def profile_case(fmt: str, launches: int = 4, ntok: int = 1):
     """A few launches of one config-shaped matrix per format, for ncu captures
     (no timing): bpdq 24576x4096 and 4096x12288, trellis 12288x4096, leech
     17408x5120, fp16 4096x4096, noweights 24576x4096."""
@@ -312,12 +418,12 @@ def profile_case(fmt: str, launches: int = 4):
     elif fmt == "noweights":
         mats.append((q2.q2_pack_noweights(24576, 4096), 4096))
     for blob, C in mats:
-        pk = q2.Packed(blob, ntok_max=1)
-        x = torch.from_numpy(synth.activations(1, C, 7)).cuda()
+        pk = q2.Packed(blob, ntok_max=ntok)
+        x = torch.from_numpy(synth.activations(ntok, C, 7)).cuda()
         for _ in range(launches):
             pk.gemv(x)
     torch.cuda.synchronize()
-    print(json.dumps({"profile_case": fmt, "matrices": len(mats), "launches_each": launches}))
+    print(json.dumps({"profile_case": fmt, "matrices": len(mats), "launches_each": launches, "ntok": ntok}))
 
 
 def main():
@@ -332,10 +438,18 @@ def main():
     ap.add_argument("--profile-case", default=None,
                     choices=["bpdq", "trellis", "leech", "fp16", "noweights"],
                     help="run a few untimed launches of one format for an ncu capture")
+    ap.add_argument("--sweep", action="store_true", help="config-4 sweep (14B stack, formats x ntok)")
+    ap.add_argument("--sweep-formats", default="fp16,cublas,bpdq,trellis,leech")
+    ap.add_argument("--sweep-ntok", default="1,2,4,8,16,32,64")
+    ap.add_argument("--sweep-distinct", type=int, default=4)
+    ap.add_argument("--sweep-steps", type=int, default=20)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.sweep:
+        sweep(args)
+        return
     if args.profile_case:
-        profile_case(args.profile_case)
+        profile_case(args.profile_case, ntok=args.ntok)
         return
 
     if args.impl == "reference":

@@ -60,6 +60,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "q2_decode_bytes": [vp, psz],
         "q2_decode": [vp, vp, vp],
         "q2_gemv_bpdq_noalloc": [vp, vp, vp, vp],
+        "q2_device_errors": [ctypes.POINTER(ctypes.c_uint)],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -75,7 +76,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
 
 EXPORTS = ["q2_pack_fp16", "q2_pack_bpdq", "q2_pack_trellis", "q2_pack_leech", "q2_pack_noweights",
            "q2_bind", "q2_unbind", "q2_workspace_bytes", "q2_set_workspace", "q2_info", "q2_bytes",
-           "q2_gemv", "q2_decode_bytes", "q2_decode", "q2_strerror", "q2_gemv_bpdq_noalloc"]
+           "q2_gemv", "q2_decode_bytes", "q2_decode", "q2_strerror", "q2_gemv_bpdq_noalloc",
+           "q2_device_errors"]
 
 
 def q2_strerror(status: int) -> str:
@@ -144,6 +146,13 @@ def _stream_ptr(stream):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def device_errors() -> int:
+    """The tensor-core kernels' device error word (then cleared); 0 is normal."""
+    v = ctypes.c_uint(0)
+    _check(load().q2_device_errors(ctypes.byref(v)), "q2_device_errors")
+    return v.value
 
 
 class Packed:

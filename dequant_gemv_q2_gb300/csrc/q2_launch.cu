@@ -13,6 +13,7 @@ extern "C" int q2_b1_noweights(const q2_handle* h, const void* x, void* y, void*
 extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* stream);
 extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* stream);
 extern "C" int q2_mt_launch(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
+extern "C" int q2_tc_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
 
 namespace q2 {
 
@@ -57,7 +58,7 @@ int set_smem(const void* fn, int bytes) {
 extern "C" {
 
 int q2_launch_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
-  return ntok == 1 ? q2_b1_bpdq(h, x, y, stream) : q2_mt_launch(h, x, y, ntok, stream);
+  return ntok == 1 ? q2_b1_bpdq(h, x, y, stream) : q2_tc_bpdq(h, x, y, ntok, stream);
 }
 
 int q2_launch_trellis(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {

@@ -71,12 +71,12 @@ __global__ void __launch_bounds__(kThreads) k_reduce(RedArgs a) {
 
 using namespace q2;
 
-// Second launch of every split-K GEMV (batch 1 and multi-token).
-extern "C" int q2_launch_reduce(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
+// Second launch of a split-K GEMV whose partials are [ntok][nsplit][Rpad].
+extern "C" int q2_launch_reduce_n(const q2_handle* h, const void* x, void* y, int ntok, int nsplit, void* stream) {
   const q2_blob_header& d = h->hdr;
   RedArgs a = {};
   a.partial = static_cast<const float*>(h->ws);
-  a.nslice = d.nslice;
+  a.nslice = nsplit;
   a.Rpad = d.Rpad;
   a.R = d.R;
   a.ntok = ntok;
@@ -100,4 +100,9 @@ extern "C" int q2_launch_reduce(const q2_handle* h, const void* x, void* y, int 
   const size_t n = (size_t)ntok * d.R;
   const int grid = (int)std::min<size_t>((n + kThreads - 1) / kThreads, (size_t)4 * di.sms);
   return launch_pdl(k_reduce, a, max(grid, 1), kThreads, 0, stream);
+}
+
+// Second launch of every per-slice split-K GEMV (batch 1 and CUDA-core multi-token).
+extern "C" int q2_launch_reduce(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
+  return q2_launch_reduce_n(h, x, y, ntok, h->hdr.nslice, stream);
 }

@@ -1,0 +1,364 @@
+// Skinny-GEMM path on the 5th-generation tensor cores (tcgen05) for
+// 16 <= padded ntok <= 64: decode once per tile, multiply for every token.
+//
+// A CTA owns 128 output rows (four 32-row blocks) and a range of 256-column
+// slices.  For each slice, its 8 warps decode the packed weights of the
+// 128 x 256 tile into fp16 in shared memory (the canonical decoded weights:
+// BPDQ through the per-(group, row) 4-entry value table, one byte permute
+// per two or four weights), the x tile of all tokens is staged next to it,
+// and one thread issues sixteen tcgen05.mma.kind::f16 (M = 128, N = padded
+// ntok, K = 16) that accumulate in a TMEM fp32 tile.  A and B tiles are
+// double-buffered; an mbarrier per buffer, armed by tcgen05.commit, tells
+// the decoders when the tensor core has finished reading a buffer.  At the
+// end each warp reads its 32 TMEM lanes (its 32 rows) and writes fp32
+// partial sums for the split-K reduction kernel, or y directly.
+//
+// Operand layout in shared memory: K-major, no swizzle, core matrices of
+// 8 rows x 16 bytes; the byte offset of element (row m, k) is
+// (m / 8) * 4096 + (k / 8) * 128 + (m % 8) * 16 + (k % 8) * 2, i.e. leading
+// (K) byte offset 128 and stride (M/N) byte offset 4096.
+//
+// Every wait is bounded: a wait that runs out records an error code in
+// q2_tc_error (read back with q2_device_errors) and the kernel skips the
+// rest of its work, then frees its TMEM columns.
+#include <cuda_fp16.h>
+
+#include "q2_common.cuh"
+
+extern __shared__ __align__(1024) unsigned char q2_smem[];
+extern "C" int q2_launch_reduce_n(const q2_handle* h, const void* x, void* y, int ntok, int nsplit, void* stream);
+
+__device__ unsigned int q2_tc_error = 0;
+
+namespace q2 {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRows = 128;                    // M of the MMA
+constexpr int kTileA = kRows * 256 * 2;       // 64 KiB per A buffer
+constexpr uint32_t kLBO = 128, kSBO = 4096;   // core-matrix strides (bytes)
+constexpr long long kSpinLimit = 1ll << 24;   // bounded mbarrier waits
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Shared-memory matrix descriptor (tcgen05): start >> 4 in bits 0-13,
+// leading byte offset >> 4 in 16-29, stride byte offset >> 4 in 32-45,
+// descriptor version 1 in 46-47, no swizzle (61-63 = 0).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)((kLBO >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((kSBO >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
+// (7-9, 10-12 = 0), both K-major (15, 16 = 0), N >> 3 in 17-22, M >> 4 in 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Wait for the phase with the given parity to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (long long i = 0; i < kSpinLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// 16 fp32 columns of this warp's 32 TMEM lanes (one row per lane).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Decode of 4 column-bytes (32 columns) of one row.  w0, w1: the 4 plane-0
+// and plane-1 bytes.  The 2-bit code of column 8q + i is b0_i | b1_i << 1;
+// E / O hold the codes of the even / odd columns of every byte (code of
+// column 2j of a byte at bits 2j..2j+1 of that byte); masks by 0x33 split
+// each into the codes of columns {0,4} and {2,6} (or {1,5}, {3,7}).  One byte
+// permute per byte then forms a selector with four codes in its nibbles, and
+// two permutes of the row's value table (low bytes, high bytes of v0..v3)
+// give the fp16 weights; two more put them back in column order.
+struct Codes4 {
+  uint32_t ea, eb, oa, ob;
+};
+
+__device__ __forceinline__ Codes4 codes4(uint32_t w0, uint32_t w1) {
+  const uint32_t e = (w0 & 0x55555555u) | ((w1 << 1) & 0xAAAAAAAAu);
+  const uint32_t o = ((w0 >> 1) & 0x55555555u) | (w1 & 0xAAAAAAAAu);
+  Codes4 c;
+  c.ea = e & 0x33333333u;          // cols 0,4 of each byte
+  c.eb = (e >> 2) & 0x33333333u;   // cols 2,6
+  c.oa = o & 0x33333333u;          // cols 1,5
+  c.ob = (o >> 2) & 0x33333333u;   // cols 3,7
+  return c;
+}
+
+// 8 fp16 weights of byte q (0..3) of a Codes4, in column order.
+template <int Q>
+__device__ __forceinline__ uint4 decode_q(const Codes4& c, uint32_t tlo, uint32_t thi) {
+  constexpr uint32_t sel = (uint32_t)Q | ((4u + Q) << 4);
+  const uint32_t s0 = __byte_perm(c.ea, c.oa, sel);   // nibbles: codes of cols 0,4,1,5
+  const uint32_t s1 = __byte_perm(c.eb, c.ob, sel);   // cols 2,6,3,7
+  const uint32_t lo0 = __byte_perm(tlo, 0u, s0), hi0 = __byte_perm(thi, 0u, s0);
+  const uint32_t lo1 = __byte_perm(tlo, 0u, s1), hi1 = __byte_perm(thi, 0u, s1);
+  uint4 r;
+  r.x = __byte_perm(lo0, hi0, 0x6240u);     // cols 0,1
+  r.y = __byte_perm(lo1, hi1, 0x6240u);     // cols 2,3
+  r.z = __byte_perm(lo0, hi0, 0x7351u);     // cols 4,5
+  r.w = __byte_perm(lo1, hi1, 0x7351u);     // cols 6,7
+  return r;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+struct TcArgs {
+  const unsigned char* bits;   // BPDQ item stream
+  const uint2* vtab;           // [G][Rpad] 4 halves
+  const __half* x;             // [ntok][C]
+  __half* y;                   // [ntok][R]  (nsplit == 1)
+  float* partial;              // [ntok][nsplit][Rpad] (nsplit > 1)
+  int R, C, Rpad, nrb, S, ntok, N, nsplit, ntile;
+};
+
+// Shared memory: A[2] (64 KiB each) | B[2] (N x 512 bytes each) | mbarriers | TMEM address.
+// CTA = (tile blockIdx.x % ntile, K-split blockIdx.x / ntile).  Warp w
+// decodes row block w % 4 of the tile, rotated positions [16h, 16h + 16)
+// with h = w / 4.
+__global__ void __launch_bounds__(kThreads, 1) k_bpdq_tc(TcArgs a) {
+  unsigned char* A0 = q2_smem;
+  unsigned char* B0 = q2_smem + 2 * kTileA;
+  const int bbytes = a.N * 512;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(B0 + 2 * bbytes);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rbl = warp & 3, half = warp >> 2;        // row block in tile, half of the slice
+  const int tile = blockIdx.x % a.ntile, split = blockIdx.x / a.ntile;
+  const int sA = split * a.S / a.nsplit, sB = (split + 1) * a.S / a.nsplit;
+  const int rb = tile * 4 + rbl;
+  const bool valid = rb < a.nrb;                     // the last tile may be ragged
+  const int row = rb * 32 + lane;
+  const int m = rbl * 32 + lane;                     // row inside the tile
+  const uint32_t ncols = a.N <= 32 ? 32u : 64u;
+  const int tile_rbs = min(4, a.nrb - tile * 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = sA; s < sB; ++s)
+      prefetch_l2(a.bits + ((size_t)s * a.nrb + tile * 4) * Q2_ITEM_BYTES_BPDQ,
+                  (size_t)tile_rbs * Q2_ITEM_BYTES_BPDQ);
+    mbar_init(saddr(&bars[0]), 1);
+    mbar_init(saddr(&bars[1]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tslot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // zero the padding token rows of both B buffers once
+  for (int i = threadIdx.x; i < 2 * bbytes / 16; i += kThreads) reinterpret_cast<uint4*>(B0)[i] = make_uint4(0, 0, 0, 0);
+  // first slice's bits for this warp: chunks `half` (plane 0) and 2 + half (plane 1)
+  uint4 p0 = make_uint4(0, 0, 0, 0), p1 = p0;
+  uint2 vt = make_uint2(0, 0);
+  if (valid && sA < sB) {
+    const unsigned char* ip = a.bits + ((size_t)sA * a.nrb + rb) * Q2_ITEM_BYTES_BPDQ + lane * 16;
+    p0 = ldg_stream(ip + half * 512);
+    p1 = ldg_stream(ip + (2 + half) * 512);
+    vt = a.vtab[(size_t)sA * a.Rpad + row];
+  }
+  pdl_wait();
+  pdl_trigger();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t idesc = idesc_f16(kRows, a.N);
+  bool ok = true;
+
+  for (int s = sA; s < sB && ok; ++s) {
+    const int buf = (s - sA) & 1;
+    unsigned char* Ab = A0 + buf * kTileA;
+    unsigned char* Bb = B0 + buf * bbytes;
+    // the MMAs that last read this buffer (two slices ago) must be done
+    if (s - sA >= 2) {
+      if (!mbar_wait(saddr(&bars[buf]), (uint32_t)(((s - sA) >> 1) - 1) & 1u)) {
+        ok = false;
+        if (threadIdx.x == 0) atomicExch(&q2_tc_error, 1u);
+      }
+    }
+    if (ok) {
+      // x tile of this slice, copied asynchronously while the weights decode
+      const __half* xs = a.x + (size_t)s * 256;
+      const uint32_t bb0 = saddr(Bb);
+      for (int e = threadIdx.x; e < a.ntok * 32; e += kThreads) {
+        const int n = e >> 5, kc = e & 31;
+        cp_async16(bb0 + (n >> 3) * kSBO + kc * kLBO + (n & 7) * 16, xs + (size_t)n * a.C + kc * 8);
+      }
+    }
+    // next slice's bits
+    uint4 n0 = p0, n1 = p1;
+    uint2 nvt = vt;
+    if (valid && s + 1 < sB) {
+      const unsigned char* np = a.bits + ((size_t)(s + 1) * a.nrb + rb) * Q2_ITEM_BYTES_BPDQ + lane * 16;
+      n0 = ldg_stream(np + half * 512);
+      n1 = ldg_stream(np + (2 + half) * 512);
+      nvt = a.vtab[(size_t)(s + 1) * a.Rpad + row];
+    }
+    if (ok) {
+      // value table split into low bytes and high bytes of v0..v3
+      const uint32_t tlo = __byte_perm(vt.x, vt.y, 0x6420u);
+      const uint32_t thi = __byte_perm(vt.x, vt.y, 0x7531u);
+      const uint32_t w0[4] = {p0.x, p0.y, p0.z, p0.w};
+      const uint32_t w1[4] = {p1.x, p1.y, p1.z, p1.w};
+      unsigned char* arow = Ab + (m >> 3) * kSBO + (m & 7) * 16;
+      // column-byte of rotated position P = half*16 + 4j + q is (P + lane) mod 32
+      const uint32_t rot = (uint32_t)(half * 16 + lane) * kLBO;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const Codes4 c = codes4(w0[j], w1[j]);
+        *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 0) * kLBO) & 4095u)) = decode_q<0>(c, tlo, thi);
+        *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 1) * kLBO) & 4095u)) = decode_q<1>(c, tlo, thi);
+        *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 2) * kLBO) & 4095u)) = decode_q<2>(c, tlo, thi);
+        *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 3) * kLBO) & 4095u)) = decode_q<3>(c, tlo, thi);
+      }
+    }
+    cp_async_wait_all();
+    fence_async_smem();
+    tc_fence_before();
+    ok = __syncthreads_and(ok);
+    tc_fence_after();
+    if (threadIdx.x == 0 && ok) {
+      const uint32_t aa = saddr(Ab), bb = saddr(Bb);
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        mma_f16(tmem, sdesc(aa + k * 2 * kLBO), sdesc(bb + k * 2 * kLBO), idesc, (s > sA || k > 0) ? 1u : 0u);
+      mma_commit(saddr(&bars[buf]));
+    }
+    p0 = n0;
+    p1 = n1;
+    vt = nvt;
+  }
+  // wait for the last MMAs of both buffers
+  const int used = sB - sA;
+  if (ok && used > 0) {
+    const int last = used - 1;
+    if (!mbar_wait(saddr(&bars[last & 1]), (uint32_t)(last >> 1) & 1u)) ok = false;
+    if (ok && used > 1 && !mbar_wait(saddr(&bars[(last - 1) & 1]), (uint32_t)((last - 1) >> 1) & 1u)) ok = false;
+    if (!ok && threadIdx.x == 0) atomicExch(&q2_tc_error, 2u);
+  }
+  ok = __syncthreads_and(ok);
+  tc_fence_after();
+  if (warp < 4 && ok) {
+    // warp w reads TMEM lanes 32w..32w+31 = rows of row block w of the tile
+    const int orow = (tile * 4 + warp) * 32 + lane;
+    for (int c0 = 0; c0 < a.N; c0 += 16) {
+      float v[16];
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int t = c0 + i;
+        if (t < a.ntok) {
+          if (a.nsplit == 1) {
+            if (orow < a.R) a.y[(size_t)t * a.R + orow] = __float2half_rn(v[i]);
+          } else if (orow < a.Rpad) {
+            a.partial[((size_t)t * a.nsplit + split) * a.Rpad + orow] = v[i];
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+}
+
+}  // namespace
+}  // namespace q2
+
+using namespace q2;
+
+// BPDQ at 2..64 tokens on the tensor cores (tokens padded to a multiple of 16).
+extern "C" int q2_tc_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
+  const q2_blob_header& d = h->hdr;
+  TcArgs a;
+  a.bits = h->dev + d.off[SEC_BPDQ_BITS];
+  a.vtab = reinterpret_cast<const uint2*>(h->dev + d.off[SEC_BPDQ_VTAB]);
+  a.x = static_cast<const __half*>(x);
+  a.y = static_cast<__half*>(y);
+  a.partial = static_cast<float*>(h->ws);
+  a.R = d.R;
+  a.C = d.C;
+  a.Rpad = d.Rpad;
+  a.nrb = q2_nrb(d);
+  a.S = d.nslice;
+  a.ntok = ntok;
+  a.N = (ntok + 15) / 16 * 16;
+  a.ntile = (d.Rpad + kRows - 1) / kRows;
+  const int sms = dev_info().sms;
+  a.nsplit = std::max(1, std::min(a.S, sms / std::max(1, a.ntile)));
+  const int smem = 2 * kTileA + 2 * a.N * 512 + 64;
+  int st = launch_pdl(k_bpdq_tc, a, a.ntile * a.nsplit, kThreads, smem, stream);
+  if (st) return st;
+  if (a.nsplit == 1) return Q2_OK;
+  return q2_launch_reduce_n(h, x, y, ntok, a.nsplit, stream);
+}
+
+// Device-side error word of the tensor-core kernels since the last call
+// (then cleared): 0 in normal operation, else the code of a bounded wait
+// that ran out.  Synchronous (reads device memory).
+extern "C" int q2_device_errors(unsigned int* out) {
+  if (!out) return Q2_EINVAL;
+  unsigned int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, q2_tc_error, sizeof(v)) != cudaSuccess) return Q2_ECUDA;
+  if (cudaMemcpyToSymbol(q2_tc_error, &z, sizeof(z)) != cudaSuccess) return Q2_ECUDA;
+  *out = v;
+  return Q2_OK;
+}

@@ -176,6 +176,12 @@ int q2_gemv_bpdq_noalloc(const q2_handle* h, const void* x, void* y, q2_stream s
 int q2_decode_bytes(const q2_handle* h, size_t* bytes);
 int q2_decode(const q2_handle* h, void* out_dev, q2_stream stream);
 
+/* Device-side error word of the tensor-core (multi-token) kernels, then
+ * cleared: 0 in normal operation; nonzero means a bounded wait on the
+ * tensor core ran out and the kernel skipped its work (its outputs are not
+ * valid).  Synchronous: reads device memory of the current device. */
+int q2_device_errors(unsigned int* out);
+
 const char* q2_strerror(int status);
 
 #ifdef __cplusplus

@@ -55,6 +55,19 @@ def test_bpdq_parity(q2, R, C, seed, ntok):
     _check(y, obpdq.decode_f64(d["plane0"], d["plane1"], d["coef"]), x)
 
 
+@pytest.mark.parametrize("ntok", [16, 48, 64])
+def test_bpdq_tensor_path_shapes_and_error_word(q2, ntok):
+    # 8B-shaped rows and columns through the tcgen05 path; ragged 128-row tile
+    for R, C, seed in [(6144, 4096, 11), (4096, 12288, 12), (160, 512, 13)]:
+        d = synth.bpdq(R, C, seed)
+        x = synth.activations(ntok, C, seed)
+        _, y = _run(q2, q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]), x)
+        rows = np.unique(np.linspace(0, R - 1, 64).astype(int))
+        w = obpdq.decode_f64(d["plane0"][rows], d["plane1"][rows], d["coef"][:, rows])
+        _check(y, w, x, rows)
+    assert q2.device_errors() == 0
+
+
 def test_bpdq_decode_bit_exact(q2):
     d = synth.bpdq(70, 768, 9)
     pk = q2.Packed(q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]))
