@@ -14,6 +14,8 @@ extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* str
 extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* stream);
 extern "C" int q2_mt_launch(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
 extern "C" int q2_tc_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
+extern "C" int q2_tc_trellis(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
+extern "C" int q2_tc_leech(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
 
 namespace q2 {
 
@@ -62,11 +64,11 @@ int q2_launch_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* s
 }
 
 int q2_launch_trellis(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
-  return ntok == 1 ? q2_b1_trellis(h, x, y, stream) : q2_mt_launch(h, x, y, ntok, stream);
+  return ntok == 1 ? q2_b1_trellis(h, x, y, stream) : q2_tc_trellis(h, x, y, ntok, stream);
 }
 
 int q2_launch_leech(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
-  return ntok == 1 ? q2_b1_leech(h, x, y, stream) : q2_mt_launch(h, x, y, ntok, stream);
+  return ntok == 1 ? q2_b1_leech(h, x, y, stream) : q2_tc_leech(h, x, y, ntok, stream);
 }
 
 int q2_launch_noweights(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {

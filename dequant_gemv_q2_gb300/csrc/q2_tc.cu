@@ -159,22 +159,96 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 struct TcArgs {
-  const unsigned char* bits;   // BPDQ item stream
-  const uint2* vtab;           // [G][Rpad] 4 halves
+  const unsigned char* bits;   // item stream (BPDQ bits, trellis symbols, Leech planes)
+  const uint2* vtab;           // BPDQ: [G][Rpad] 4 halves
+  const uint32_t* table;       // trellis: 4096 half2
+  const uint16_t* parity;      // Leech: [S][Rpad]
   const __half* x;             // [ntok][C]
-  __half* y;                   // [ntok][R]  (nsplit == 1)
-  float* partial;              // [ntok][nsplit][Rpad] (nsplit > 1)
-  int R, C, Rpad, nrb, S, ntok, N, nsplit, ntile;
+  __half* y;                   // [ntok][R]  (nsplit == 1, BPDQ only)
+  float* partial;              // [ntok][nsplit][Rpad]
+  int R, C, Rpad, nrb, S, ntok, N, nsplit, ntile, nblock;
 };
 
-// Shared memory: A[2] (64 KiB each) | B[2] (N x 512 bytes each) | mbarriers | TMEM address.
-// CTA = (tile blockIdx.x % ntile, K-split blockIdx.x / ntile).  Warp w
-// decodes row block w % 4 of the tile, rotated positions [16h, 16h + 16)
-// with h = w / 4.
-__global__ void __launch_bounds__(kThreads, 1) k_bpdq_tc(TcArgs a) {
-  unsigned char* A0 = q2_smem;
-  unsigned char* B0 = q2_smem + 2 * kTileA;
-  const int bbytes = a.N * 512;
+constexpr uint32_t kHashHi = 0x9E37u << 16;     // trellis: (s*0x9E37 mod 2^16) in bits 16..31
+
+// Per-format shape of a slice's K range: 32 chunks of 8 columns, plus, for
+// Leech, 4 chunks carrying the parity term (A = parity bit of the blocks
+// starting in the slice, B = their block sums of x split into fp16 hi + lo).
+template <int FMT>
+struct TcShape {
+  static constexpr int kch = FMT == Q2_LEECH ? 36 : 32;
+  static constexpr uint32_t sbo = kch * 128;
+  static constexpr int tileA = kRows * kch * 16;
+  static constexpr int table = FMT == Q2_TRELLIS ? 4096 * 4 : 0;
+  static constexpr int item = FMT == Q2_BPDQ ? Q2_ITEM_BYTES_BPDQ : FMT == Q2_TRELLIS ? Q2_ITEM_BYTES_TRL
+                                                                                     : Q2_ITEM_BYTES_LEECH;
+};
+
+__device__ __forceinline__ uint64_t sdesc_s(uint32_t addr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)((kLBO >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Leech: 3-bit codes b0 | b1 << 1 | b2 << 2 of the columns of 4 column-bytes
+// in nibble fields (the BPDQ split of codes4, with bit 2 from plane 2).
+__device__ __forceinline__ Codes4 codes4x3(uint32_t w0, uint32_t w1, uint32_t w2) {
+  Codes4 c = codes4(w0, w1);
+  c.ea |= (w2 << 2) & 0x44444444u;   // cols 0,4: b2 bits 0,4 -> 2,6
+  c.eb |= w2 & 0x44444444u;          // cols 2,6: bits 2,6
+  c.oa |= (w2 << 1) & 0x44444444u;   // cols 1,5: bits 1,5 -> 2,6
+  c.ob |= (w2 >> 1) & 0x44444444u;   // cols 3,7: bits 3,7 -> 2,6
+  return c;
+}
+
+// 2u = 2*(b0 + 2*b1 - 4*b2) in fp16 for the 8 columns of byte Q; the low
+// byte of every such fp16 value is 0, so only high bytes are looked up.
+template <int Q>
+__device__ __forceinline__ uint4 decode_leech_q(const Codes4& c) {
+  // fp16 high bytes of 0, 2, 4, 6, -8, -6, -4, -2 (code 0..7)
+  constexpr uint32_t HA = 0x46444000u, HB = 0xC0C4C6C8u;
+  constexpr uint32_t sel = (uint32_t)Q | ((4u + Q) << 4);
+  const uint32_t s0 = __byte_perm(c.ea, c.oa, sel);   // codes of cols 0,4,1,5
+  const uint32_t s1 = __byte_perm(c.eb, c.ob, sel);   // cols 2,6,3,7
+  const uint32_t h0 = __byte_perm(HA, HB, s0), h1 = __byte_perm(HA, HB, s1);
+  uint4 r;
+  r.x = __byte_perm(h0, 0u, 0x2404u);       // cols 0,1: [0, h(c0), 0, h(c1)]
+  r.y = __byte_perm(h1, 0u, 0x2404u);       // cols 2,3
+  r.z = __byte_perm(h0, 0u, 0x3414u);       // cols 4,5
+  r.w = __byte_perm(h1, 0u, 0x3414u);       // cols 6,7
+  return r;
+}
+
+// Trellis: steps 64*H .. +63 of a segment -> columns 128*H .. +127 of the A
+// row (column-byte = step / 4); H is a template parameter so every window
+// index is static.
+template <int H>
+__device__ __forceinline__ void trellis_half(const uint32_t (&W)[16], const uint32_t* tab, unsigned char* arow) {
+#pragma unroll
+  for (int cb = 0; cb < 16; ++cb) {
+    uint32_t e4[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int k = H * 64 + cb * 4 + t;
+      const int n = 127 - k;
+      const uint32_t f = __funnelshift_r(W[n >> 3], W[((n >> 3) + 1) & 15], 4 * (n & 7));
+      const uint32_t e = tab[(f * kHashHi) >> 20];
+      e4[t] = e ^ ((f & 1u) ? 0x80008000u : 0u);
+    }
+    *reinterpret_cast<uint4*>(arow + (H * 16 + cb) * kLBO) = make_uint4(e4[0], e4[1], e4[2], e4[3]);
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1) k_tc(TcArgs a) {
+  using Sh = TcShape<FMT>;
+  uint32_t* tab = reinterpret_cast<uint32_t*>(q2_smem);            // trellis table
+  unsigned char* A0 = q2_smem + Sh::table;
+  unsigned char* B0 = A0 + 2 * Sh::tileA;
+  const int bbytes = (a.N / 8) * (int)Sh::sbo;
   uint64_t* bars = reinterpret_cast<uint64_t*>(B0 + 2 * bbytes);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -190,8 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bpdq_tc(TcArgs a) {
 
   if (threadIdx.x == 0) {
     for (int s = sA; s < sB; ++s)
-      prefetch_l2(a.bits + ((size_t)s * a.nrb + tile * 4) * Q2_ITEM_BYTES_BPDQ,
-                  (size_t)tile_rbs * Q2_ITEM_BYTES_BPDQ);
+      prefetch_l2(a.bits + ((size_t)s * a.nrb + tile * 4) * Sh::item, (size_t)tile_rbs * Sh::item);
     mbar_init(saddr(&bars[0]), 1);
     mbar_init(saddr(&bars[1]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -202,17 +275,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_bpdq_tc(TcArgs a) {
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // zero the padding token rows of both B buffers once
+  if (FMT == Q2_TRELLIS)
+    for (int i = threadIdx.x; i < 4096; i += kThreads) tab[i] = a.table[i];
+  // zero both B buffers once (padding tokens, unused parity columns)
   for (int i = threadIdx.x; i < 2 * bbytes / 16; i += kThreads) reinterpret_cast<uint4*>(B0)[i] = make_uint4(0, 0, 0, 0);
-  // first slice's bits for this warp: chunks `half` (plane 0) and 2 + half (plane 1)
-  uint4 p0 = make_uint4(0, 0, 0, 0), p1 = p0;
+
+  // per-lane payload of one slice: BPDQ/Leech the half's chunks of each plane,
+  // trellis the whole 64-byte packet; plus BPDQ's value table / Leech's parity
+  constexpr int NP = FMT == Q2_BPDQ ? 2 : FMT == Q2_LEECH ? 3 : 4;
+  uint4 pl[NP];
   uint2 vt = make_uint2(0, 0);
-  if (valid && sA < sB) {
-    const unsigned char* ip = a.bits + ((size_t)sA * a.nrb + rb) * Q2_ITEM_BYTES_BPDQ + lane * 16;
-    p0 = ldg_stream(ip + half * 512);
-    p1 = ldg_stream(ip + (2 + half) * 512);
-    vt = a.vtab[(size_t)sA * a.Rpad + row];
-  }
+  uint32_t par = 0;
+  auto load = [&](int s, uint4 (&d)[NP], uint2& v, uint32_t& pw) {
+    const unsigned char* ip = a.bits + ((size_t)s * a.nrb + rb) * Sh::item + lane * 16;
+    if (FMT == Q2_TRELLIS) {
+#pragma unroll
+      for (int k = 0; k < NP; ++k) d[k] = __ldg(reinterpret_cast<const uint4*>(ip + k * 512));
+    } else {
+#pragma unroll
+      for (int k = 0; k < NP; ++k) d[k] = ldg_stream(ip + (2 * k + half) * 512);
+    }
+    if (FMT == Q2_BPDQ) v = a.vtab[(size_t)s * a.Rpad + row];
+    if (FMT == Q2_LEECH) pw = a.parity[(size_t)s * a.Rpad + row];
+  };
+#pragma unroll
+  for (int k = 0; k < NP; ++k) pl[k] = make_uint4(0, 0, 0, 0);
+  if (valid && sA < sB) load(sA, pl, vt, par);
   pdl_wait();
   pdl_trigger();
   tc_fence_before();
@@ -224,49 +312,109 @@ __global__ void __launch_bounds__(kThreads, 1) k_bpdq_tc(TcArgs a) {
 
   for (int s = sA; s < sB && ok; ++s) {
     const int buf = (s - sA) & 1;
-    unsigned char* Ab = A0 + buf * kTileA;
+    unsigned char* Ab = A0 + buf * Sh::tileA;
     unsigned char* Bb = B0 + buf * bbytes;
-    // the MMAs that last read this buffer (two slices ago) must be done
     if (s - sA >= 2) {
       if (!mbar_wait(saddr(&bars[buf]), (uint32_t)(((s - sA) >> 1) - 1) & 1u)) {
         ok = false;
         if (threadIdx.x == 0) atomicExch(&q2_tc_error, 1u);
       }
     }
+    const int ncols_s = min(256, a.C - s * 256);     // Leech: the last slice may be short
     if (ok) {
-      // x tile of this slice, copied asynchronously while the weights decode
+      // x tile of this slice (zero beyond C), copied asynchronously
       const __half* xs = a.x + (size_t)s * 256;
       const uint32_t bb0 = saddr(Bb);
       for (int e = threadIdx.x; e < a.ntok * 32; e += kThreads) {
         const int n = e >> 5, kc = e & 31;
-        cp_async16(bb0 + (n >> 3) * kSBO + kc * kLBO + (n & 7) * 16, xs + (size_t)n * a.C + kc * 8);
+        const uint32_t dst = bb0 + (n >> 3) * Sh::sbo + kc * kLBO + (n & 7) * 16;
+        if (kc * 8 + 8 <= ncols_s) {
+          cp_async16(dst, xs + (size_t)n * a.C + kc * 8);
+        } else {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          __half* hv = reinterpret_cast<__half*>(&v);
+          for (int i = 0; i < 8; ++i)
+            if (kc * 8 + i < ncols_s) hv[i] = xs[(size_t)n * a.C + kc * 8 + i];
+          *reinterpret_cast<uint4*>(Bb + (n >> 3) * Sh::sbo + kc * kLBO + (n & 7) * 16) = v;
+        }
+      }
+      if (FMT == Q2_LEECH) {
+        // parity columns: block sums of x for the blocks starting in this slice,
+        // hi part in chunks 32-33, lo part (x - hi) in chunks 34-35
+        const int bfirst = (s * 256 + 23) / 24;
+        const int blast = min(a.nblock - 1, (s * 256 + 256 + 23) / 24 - 1);
+        const int nbk = max(0, blast - bfirst + 1);
+        for (int e = threadIdx.x; e < a.ntok * 16; e += kThreads) {
+          const int n = e >> 4, jb = e & 15;
+          float xsum = 0.f;
+          if (jb < nbk) {
+            const __half* xp = a.x + (size_t)n * a.C + (size_t)(bfirst + jb) * 24;
+            for (int i = 0; i < 24; ++i) xsum += __half2float(xp[i]);
+          }
+          const __half hi = __float2half_rn(xsum);
+          const __half lo = __float2half_rn(xsum - __half2float(hi));
+          unsigned char* bn = Bb + (n >> 3) * Sh::sbo + (n & 7) * 16;
+          reinterpret_cast<__half*>(bn + (32 + (jb >> 3)) * kLBO)[jb & 7] = hi;
+          reinterpret_cast<__half*>(bn + (34 + (jb >> 3)) * kLBO)[jb & 7] = lo;
+        }
       }
     }
-    // next slice's bits
-    uint4 n0 = p0, n1 = p1;
+    uint4 nx[NP];
     uint2 nvt = vt;
-    if (valid && s + 1 < sB) {
-      const unsigned char* np = a.bits + ((size_t)(s + 1) * a.nrb + rb) * Q2_ITEM_BYTES_BPDQ + lane * 16;
-      n0 = ldg_stream(np + half * 512);
-      n1 = ldg_stream(np + (2 + half) * 512);
-      nvt = a.vtab[(size_t)(s + 1) * a.Rpad + row];
-    }
-    if (ok) {
-      // value table split into low bytes and high bytes of v0..v3
-      const uint32_t tlo = __byte_perm(vt.x, vt.y, 0x6420u);
-      const uint32_t thi = __byte_perm(vt.x, vt.y, 0x7531u);
-      const uint32_t w0[4] = {p0.x, p0.y, p0.z, p0.w};
-      const uint32_t w1[4] = {p1.x, p1.y, p1.z, p1.w};
-      unsigned char* arow = Ab + (m >> 3) * kSBO + (m & 7) * 16;
-      // column-byte of rotated position P = half*16 + 4j + q is (P + lane) mod 32
-      const uint32_t rot = (uint32_t)(half * 16 + lane) * kLBO;
+    uint32_t npar = par;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const Codes4 c = codes4(w0[j], w1[j]);
-        *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 0) * kLBO) & 4095u)) = decode_q<0>(c, tlo, thi);
-        *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 1) * kLBO) & 4095u)) = decode_q<1>(c, tlo, thi);
-        *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 2) * kLBO) & 4095u)) = decode_q<2>(c, tlo, thi);
-        *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 3) * kLBO) & 4095u)) = decode_q<3>(c, tlo, thi);
+    for (int k = 0; k < NP; ++k) nx[k] = pl[k];
+    if (valid && s + 1 < sB) load(s + 1, nx, nvt, npar);
+    if (ok) {
+      unsigned char* arow = Ab + (m >> 3) * Sh::sbo + (m & 7) * 16;
+      if (FMT == Q2_TRELLIS) {
+        const uint32_t W[16] = {pl[0].x, pl[0].y, pl[0].z, pl[0].w, pl[1].x, pl[1].y, pl[1].z, pl[1].w,
+                                pl[2].x, pl[2].y, pl[2].z, pl[2].w, pl[3].x, pl[3].y, pl[3].z, pl[3].w};
+        if (half == 0) trellis_half<0>(W, tab, arow);
+        else trellis_half<1>(W, tab, arow);
+      } else {
+        const uint32_t rot = (uint32_t)(half * 16 + lane) * kLBO;
+        if (FMT == Q2_BPDQ) {
+          const uint32_t tlo = __byte_perm(vt.x, vt.y, 0x6420u);
+          const uint32_t thi = __byte_perm(vt.x, vt.y, 0x7531u);
+          const uint32_t w0[4] = {pl[0].x, pl[0].y, pl[0].z, pl[0].w};
+          const uint32_t w1[4] = {pl[1].x, pl[1].y, pl[1].z, pl[1].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const Codes4 c = codes4(w0[j], w1[j]);
+            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 0) * kLBO) & 4095u)) = decode_q<0>(c, tlo, thi);
+            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 1) * kLBO) & 4095u)) = decode_q<1>(c, tlo, thi);
+            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 2) * kLBO) & 4095u)) = decode_q<2>(c, tlo, thi);
+            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 3) * kLBO) & 4095u)) = decode_q<3>(c, tlo, thi);
+          }
+        } else {
+          const uint32_t w0[4] = {pl[0].x, pl[0].y, pl[0].z, pl[0].w};
+          const uint32_t w1[4] = {pl[1].x, pl[1].y, pl[1].z, pl[1].w};
+          const uint32_t w2[4] = {pl[2].x, pl[2].y, pl[2].z, pl[2].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const Codes4 c = codes4x3(w0[j], w1[j], w2[j]);
+            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 0) * kLBO) & 4095u)) = decode_leech_q<0>(c);
+            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 1) * kLBO) & 4095u)) = decode_leech_q<1>(c);
+            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 2) * kLBO) & 4095u)) = decode_leech_q<2>(c);
+            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 3) * kLBO) & 4095u)) = decode_leech_q<3>(c);
+          }
+          if (half == 0) {
+            // parity columns: A = 1.0 where the block starting in this slice is odd
+            uint32_t pv[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t lo = ((par >> (2 * q)) & 1u) ? 0x3C00u : 0u;
+              const uint32_t hi = ((par >> (2 * q + 1)) & 1u) ? 0x3C000000u : 0u;
+              pv[q] = lo | hi;
+            }
+            const uint4 p0 = make_uint4(pv[0], pv[1], pv[2], pv[3]), p1 = make_uint4(pv[4], pv[5], pv[6], pv[7]);
+            *reinterpret_cast<uint4*>(arow + 32 * kLBO) = p0;
+            *reinterpret_cast<uint4*>(arow + 33 * kLBO) = p1;
+            *reinterpret_cast<uint4*>(arow + 34 * kLBO) = p0;
+            *reinterpret_cast<uint4*>(arow + 35 * kLBO) = p1;
+          }
+        }
       }
     }
     cp_async_wait_all();
@@ -277,15 +425,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_bpdq_tc(TcArgs a) {
     if (threadIdx.x == 0 && ok) {
       const uint32_t aa = saddr(Ab), bb = saddr(Bb);
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        mma_f16(tmem, sdesc(aa + k * 2 * kLBO), sdesc(bb + k * 2 * kLBO), idesc, (s > sA || k > 0) ? 1u : 0u);
+      for (int k = 0; k < Sh::kch / 2; ++k)
+        mma_f16(tmem, sdesc_s(aa + k * 2 * kLBO, Sh::sbo), sdesc_s(bb + k * 2 * kLBO, Sh::sbo), idesc,
+                (s > sA || k > 0) ? 1u : 0u);
       mma_commit(saddr(&bars[buf]));
     }
-    p0 = n0;
-    p1 = n1;
+#pragma unroll
+    for (int k = 0; k < NP; ++k) pl[k] = nx[k];
     vt = nvt;
+    par = npar;
   }
-  // wait for the last MMAs of both buffers
   const int used = sB - sA;
   if (ok && used > 0) {
     const int last = used - 1;
@@ -296,7 +445,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_bpdq_tc(TcArgs a) {
   ok = __syncthreads_and(ok);
   tc_fence_after();
   if (warp < 4 && ok) {
-    // warp w reads TMEM lanes 32w..32w+31 = rows of row block w of the tile
     const int orow = (tile * 4 + warp) * 32 + lane;
     for (int c0 = 0; c0 < a.N; c0 += 16) {
       float v[16];
@@ -305,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bpdq_tc(TcArgs a) {
       for (int i = 0; i < 16; ++i) {
         const int t = c0 + i;
         if (t < a.ntok) {
-          if (a.nsplit == 1) {
+          if (a.nsplit == 1 && FMT == Q2_BPDQ) {
             if (orow < a.R) a.y[(size_t)t * a.R + orow] = __float2half_rn(v[i]);
           } else if (orow < a.Rpad) {
             a.partial[((size_t)t * a.nsplit + split) * a.Rpad + orow] = v[i];
@@ -320,17 +468,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_bpdq_tc(TcArgs a) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
 }
 
-}  // namespace
-}  // namespace q2
-
-using namespace q2;
-
-// BPDQ at 2..64 tokens on the tensor cores (tokens padded to a multiple of 16).
-extern "C" int q2_tc_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
+// Packed formats at 2..64 tokens on the tensor cores (tokens padded to a
+// multiple of 16).  Split-K partials (and every trellis / Leech result, whose
+// epilogue needs the row scale, exceptions and tail) go through the reduce
+// kernel.
+template <int FMT>
+int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
+  using Sh = TcShape<FMT>;
   const q2_blob_header& d = h->hdr;
-  TcArgs a;
-  a.bits = h->dev + d.off[SEC_BPDQ_BITS];
-  a.vtab = reinterpret_cast<const uint2*>(h->dev + d.off[SEC_BPDQ_VTAB]);
+  TcArgs a = {};
+  if (FMT == Q2_BPDQ) {
+    a.bits = h->dev + d.off[SEC_BPDQ_BITS];
+    a.vtab = reinterpret_cast<const uint2*>(h->dev + d.off[SEC_BPDQ_VTAB]);
+  } else if (FMT == Q2_TRELLIS) {
+    a.bits = h->dev + d.off[SEC_TRL_STREAM];
+    a.table = reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_TRL_TABLE]);
+  } else {
+    a.bits = h->dev + d.off[SEC_LEECH_PLANES];
+    a.parity = reinterpret_cast<const uint16_t*>(h->dev + d.off[SEC_LEECH_PARITY]);
+    a.nblock = d.nblock;
+  }
   a.x = static_cast<const __half*>(x);
   a.y = static_cast<__half*>(y);
   a.partial = static_cast<float*>(h->ws);
@@ -344,11 +501,24 @@ extern "C" int q2_tc_bpdq(const q2_handle* h, const void* x, void* y, int ntok, 
   a.ntile = (d.Rpad + kRows - 1) / kRows;
   const int sms = dev_info().sms;
   a.nsplit = std::max(1, std::min(a.S, sms / std::max(1, a.ntile)));
-  const int smem = 2 * kTileA + 2 * a.N * 512 + 64;
-  int st = launch_pdl(k_bpdq_tc, a, a.ntile * a.nsplit, kThreads, smem, stream);
+  const int smem = Sh::table + 2 * Sh::tileA + 2 * (a.N / 8) * (int)Sh::sbo + 64;
+  int st = launch_pdl(k_tc<FMT>, a, a.ntile * a.nsplit, kThreads, smem, stream);
   if (st) return st;
-  if (a.nsplit == 1) return Q2_OK;
+  if (a.nsplit == 1 && FMT == Q2_BPDQ) return Q2_OK;
   return q2_launch_reduce_n(h, x, y, ntok, a.nsplit, stream);
+}
+
+}  // namespace
+}  // namespace q2
+
+extern "C" int q2_tc_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
+  return q2::launch_tc<Q2_BPDQ>(h, x, y, ntok, stream);
+}
+extern "C" int q2_tc_trellis(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
+  return q2::launch_tc<Q2_TRELLIS>(h, x, y, ntok, stream);
+}
+extern "C" int q2_tc_leech(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
+  return q2::launch_tc<Q2_LEECH>(h, x, y, ntok, stream);
 }
 
 // Device-side error word of the tensor-core kernels since the last call
