@@ -438,7 +438,7 @@ def main():
     ap.add_argument("--profile-case", default=None,
                     choices=["bpdq", "trellis", "leech", "fp16", "noweights"],
                     help="run a few untimed launches of one format for an ncu capture")
-    ap.add_argument("--sweep", action="store_true", help="config-4 sweep (14B stack, formats x ntok)")
+    ap.add_argument("--sweep", action="store_true", help="sweep over the 14B layer stack: formats x tokens")
     ap.add_argument("--sweep-formats", default="fp16,cublas,bpdq,trellis,leech")
     ap.add_argument("--sweep-ntok", default="1,2,4,8,16,32,64")
     ap.add_argument("--sweep-distinct", type=int, default=4)

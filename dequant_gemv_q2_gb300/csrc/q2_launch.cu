@@ -1,5 +1,5 @@
 // Launch-side state (SM count, shared-memory opt-in) and the per-format
-// launchers that pick the batch-1 or the multi-token kernel.
+// launchers that pick the batch-1 CUDA-core or the tensor-core kernel.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -12,7 +12,6 @@ extern "C" int q2_b1_bpdq(const q2_handle* h, const void* x, void* y, void* stre
 extern "C" int q2_b1_noweights(const q2_handle* h, const void* x, void* y, void* stream);
 extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* stream);
 extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* stream);
-extern "C" int q2_mt_launch(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
 extern "C" int q2_tc_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
 extern "C" int q2_tc_trellis(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
 extern "C" int q2_tc_leech(const q2_handle* h, const void* x, void* y, int ntok, void* stream);

@@ -102,7 +102,7 @@ extern "C" int q2_launch_reduce_n(const q2_handle* h, const void* x, void* y, in
   return launch_pdl(k_reduce, a, max(grid, 1), kThreads, 0, stream);
 }
 
-// Second launch of every per-slice split-K GEMV (batch 1 and CUDA-core multi-token).
+// Second launch of every batch-1 GEMV, whose partials are one per 256-column slice.
 extern "C" int q2_launch_reduce(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
   return q2_launch_reduce_n(h, x, y, ntok, h->hdr.nslice, stream);
 }

@@ -500,7 +500,18 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
   a.N = (ntok + 15) / 16 * 16;
   a.ntile = (d.Rpad + kRows - 1) / kRows;
   const int sms = dev_info().sms;
-  a.nsplit = std::max(1, std::min(a.S, sms / std::max(1, a.ntile)));
+  // K split: one CTA per SM at a time, so the makespan is (waves of CTAs) x
+  // (slices per CTA + about one slice of prologue and epilogue)
+  long best = -1;
+  for (int ns = 1; ns <= a.S; ++ns) {
+    const long ctas = (long)a.ntile * ns;
+    const long waves = (ctas + sms - 1) / sms;
+    const long cost = waves * ((a.S + ns - 1) / ns + 1);
+    if (best < 0 || cost < best) {
+      best = cost;
+      a.nsplit = ns;
+    }
+  }
   const int smem = Sh::table + 2 * Sh::tileA + 2 * (a.N / 8) * (int)Sh::sbo + 64;
   int st = launch_pdl(k_tc<FMT>, a, a.ntile * a.nsplit, kThreads, smem, stream);
   if (st) return st;
