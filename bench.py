@@ -40,7 +40,7 @@ L2_BYTES = 126 * 1024 * 1024
 # stack's traffic per launch is that ratio times the stack's algorithmic
 # bytes per launch (traffic scales with the items processed).  Must be reset
 # to None whenever the kernel changes.
-NCU_TRAFFIC_RATIO = {"k_bpdq_b1": 27552768 / 27525120}
+NCU_TRAFFIC_RATIO: dict = {}
 
 
 def _peaks():
@@ -528,7 +528,7 @@ def main():
         extras = per_format(q2, stream, hbm)
 
     achieved = step_bytes / (ms_step * 1e-3) / 1e9
-    kname = "k_bpdq_b1" if args.ntok == 1 else "k_bpdq_mt"
+    kname = "k_bpdq_b1" if args.ntok == 1 else "k_tc"
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,

@@ -15,10 +15,12 @@
 // column-bytes of its row in an order rotated by its lane index, so the 32
 // lanes of a load always hit 32 different banks.
 //
-// Launches use programmatic dependent launch: a CTA prefetches its first
-// weights, then waits for the previous kernel on the stream (griddepcontrol)
-// before it touches x or the workspace, and lets the dependent reduction and
-// the next GEMV's CTAs get scheduled while it runs.
+// One CTA of 16 warps per SM (grid = SM count; each CTA asks for more than
+// half of the SM's shared memory so no SM ever holds two).  Launches use
+// programmatic dependent launch: a CTA prefetches its weights into L2 and
+// its first items into registers, then waits for the previous kernel on the
+// stream (griddepcontrol) before it touches x or the workspace, and lets the
+// dependent reduction and the next GEMV's CTAs get scheduled while it runs.
 #include <cuda_fp16.h>
 
 #include <mutex>
@@ -33,8 +35,6 @@ extern "C" int q2_launch_reduce(const q2_handle* h, const void* x, void* y, int 
 namespace q2 {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
 
 // T lookup for byte b of word at rotated position P (see build_table).
 __device__ __forceinline__ float tl(uint32_t lane4, uint32_t word, int b, int P) {
@@ -88,11 +88,94 @@ __device__ __forceinline__ void prefetch_rows(const void* base, int elem_bytes, 
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) k_bpdq_b1(BpdqArgs a) {
-  float* T = reinterpret_cast<float*>(q2_smem);
-  float* gsum = T + (kBuildBytes - 16) / 4;
+// ------------------------------------------------------- pipelined items
+// run_items drives every subset-sum kernel.  The CTA walks its contiguous
+// item range one slice at a time: item it of a slice goes to warp
+// (it - first item) mod W, and each warp keeps AHEAD items beyond the one
+// it is summing in flight in registers (F::load), so a CTA has
+// (AHEAD + 1) x W items of weights outstanding.  The first AHEAD loads of a
+// slice are issued before the CTA waits on the previous kernel (weights do
+// not depend on it); F::slice then builds the slice's x tables, F::ready
+// reads what every item of the slice shares, and F::compute sums one item
+// and stores its partials.
+template <int W, int AHEAD, class F>
+__device__ __forceinline__ void run_items(F& f, int nrb, int i0, int i1) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t lane4 = lane * 4u;
+  bool waited = false;
+  for (int s0 = i0; s0 < i1;) {
+    const int g = s0 / nrb;
+    const int s1 = min(i1, (g + 1) * nrb);
+    typename F::Item buf[AHEAD + 1];
+    const int it0 = s0 + warp;
+#pragma unroll
+    for (int d = 0; d < AHEAD; ++d)
+      if (it0 + d * W < s1) f.load(it0 + d * W, g, lane, buf[d]);
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
+    __syncthreads();                              // every warp is done with the previous tables
+    f.slice(g);
+    __syncthreads();
+    f.ready();
+    // the AHEAD + 1 buffers are indexed statically: AHEAD + 1 items per trip
+    for (int base = it0; base < s1; base += (AHEAD + 1) * W) {
+#pragma unroll
+      for (int u = 0; u <= AHEAD; ++u) {
+        const int it = base + u * W;
+        if (it < s1) {
+          const int nx = it + AHEAD * W;
+          if (nx < s1) f.load(nx, g, lane, buf[(u + AHEAD) % (AHEAD + 1)]);
+          f.compute(it, g, lane, buf[u]);
+        }
+      }
+    }
+    s0 = s1;
+  }
+}
+
+// Launch shapes, measured on GB300: BPDQ 16 warps with 2 items ahead (the
+// 8B stack); Leech, whose items are 1.5x larger, 8 warps with 3 ahead (the
+// 14B layers).
+constexpr int kBpdqWarps = 16, kBpdqAhead = 2;
+constexpr int kLeechWarps = 8, kLeechAhead = 3;
+
+// ------------------------------------------------------------------- BPDQ
+template <int NT>
+struct BpdqF {
+  struct Item {
+    uint4 w[4];          // 64 bytes of planes: two uint4 per plane
+    uint32_t c01;        // c0 | c1 << 16 (fp16)
+    unsigned short off;  // fp16
+  };
+  const BpdqArgs& a;
+  float* T;
+  float* gsum;
+  float xs = 0.f;        // sum of x over the slice
+  __device__ void load(int it, int g, int lane, Item& b) const {
+    ld_item4(a.bits, it, lane, b.w);
+    const size_t r = (size_t)g * a.rd.Rpad + (size_t)(it - g * a.nrb) * 32 + lane;
+    b.c01 = __ldg(reinterpret_cast<const unsigned int*>(a.c01) + r);
+    b.off = __ldg(reinterpret_cast<const unsigned short*>(a.off) + r);
+  }
+  __device__ void slice(int g) {
+    build_table<NT>(a.x + (size_t)g * Q2_SLICE, Q2_SLICE, T, gsum);
+  }
+  __device__ void ready() { xs = *gsum; }
+  __device__ void compute(int it, int g, int lane, const Item& b) {
+    const uint32_t lane4 = lane * 4u;
+    const float S0 = plane_sum(lane4, b.w[0], b.w[1]);
+    const float S1 = plane_sum(lane4, b.w[2], b.w[3]);
+    const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&b.c01));
+    const float of = __half2float(__ushort_as_half(b.off));
+    const int row = (it - g * a.nrb) * 32 + lane;
+    a.rd.partial[(size_t)g * a.rd.Rpad + row] = fmaf(c.x, S0, fmaf(c.y, S1, of * xs));
+  }
+};
+
+template <int W, int AHEAD>
+__global__ void __launch_bounds__(W * 32, 1) k_bpdq_b1(BpdqArgs a) {
   int i0, i1;
   cta_range(a.rd.nslice * a.nrb, i0, i1);
   if (threadIdx.x == 0) {
@@ -100,35 +183,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_bpdq_b1(BpdqArgs a) {
     prefetch_rows(a.c01, 4, a.nrb, a.rd.Rpad, i0, i1);
     prefetch_rows(a.off, 2, a.nrb, a.rd.Rpad, i0, i1);
   }
-  bool waited = false;
-  for (int s0 = i0; s0 < i1;) {
-    const int g = s0 / a.nrb;
-    const int s1 = min(i1, (g + 1) * a.nrb);
-    int it = s0 + warp;
-    uint4 wa[4];
-    if (it < s1) ld_item4(a.bits, it, lane, wa);
-    if (!waited) {
-      pdl_wait();
-      pdl_trigger();
-      waited = true;
-    }
-    __syncthreads();
-    build_table<kThreads>(a.x + (size_t)g * Q2_SLICE, Q2_SLICE, T, gsum);
-    const float xg = *gsum;
-    for (; it < s1; it += kWarps) {
-      uint4 wb[4];
-      if (it + kWarps < s1) ld_item4(a.bits, it + kWarps, lane, wb);
-      const int row = (it - g * a.nrb) * 32 + lane;
-      const float S0 = plane_sum(lane4, wa[0], wa[1]);
-      const float S1 = plane_sum(lane4, wa[2], wa[3]);
-      const float2 c = __half22float2(a.c01[(size_t)g * a.rd.Rpad + row]);
-      const float of = __half2float(a.off[(size_t)g * a.rd.Rpad + row]);
-      a.rd.partial[(size_t)g * a.rd.Rpad + row] = fmaf(c.x, S0, fmaf(c.y, S1, of * xg));
-#pragma unroll
-      for (int k = 0; k < 4; ++k) wa[k] = wb[k];
-    }
-    s0 = s1;
-  }
+  float* T = reinterpret_cast<float*>(q2_smem);
+  BpdqF<W * 32> f{a, T, T + (kBuildBytes - 16) / 4};
+  run_items<W, AHEAD>(f, a.nrb, i0, i1);
 }
 
 // ------------------------------------------------------------------ Leech
@@ -152,91 +209,97 @@ __device__ __forceinline__ void ld_item6(const unsigned char* base, int it, int 
   for (int k = 0; k < 6; ++k) w[k] = ldg_stream(p + k * 512);
 }
 
-__global__ void __launch_bounds__(kThreads, 2) k_leech_b1(LeechArgs a) {
-  float* T = reinterpret_cast<float*>(q2_smem);
-  float* gsum = T + (kBuildBytes - 16) / 4;
-  float* xb = reinterpret_cast<float*>(q2_smem + kBuildBytes);   // block sums of x, <= 11
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t lane4 = lane * 4u;
+// The three planes hold the two's-complement bits of u = (v - p)/2 per
+// weight (p = the block's parity bit), so v = p + 2*b0 + 4*b1 - 8*b2: three
+// subset sums plus, per 24-column block of the slice, the block sum of x
+// when the row's parity bit for the block is set.
+template <int NT>
+struct LeechF {
+  struct Item {
+    uint4 w[6];
+    uint32_t pw;         // parity bits of the slice's blocks for this row
+  };
+  const LeechArgs& a;
+  float* T;
+  float* gsum;
+  float* xb;             // block sums of x in the slice, <= 11
+  int nbk;
+  __device__ void load(int it, int g, int lane, Item& b) const {
+    ld_item6(a.planes, it, lane, b.w);
+    b.pw = __ldg(a.parity + (size_t)g * a.rd.Rpad + (size_t)(it - g * a.nrb) * 32 + lane);
+  }
+  __device__ void slice(int g) {
+    const int bfirst = (g * Q2_SLICE + 23) / 24;
+    const int blast = min(a.nblock - 1, (g * Q2_SLICE + Q2_SLICE + 23) / 24 - 1);
+    nbk = max(0, blast - bfirst + 1);
+    if ((int)threadIdx.x < nbk) {
+      const __half* xp = a.x + (size_t)(bfirst + threadIdx.x) * 24;
+      float v = 0.f;
+      for (int i = 0; i < 24; ++i) v += __half2float(xp[i]);
+      xb[threadIdx.x] = v;
+    }
+    build_table<NT>(a.x + (size_t)g * Q2_SLICE, min(Q2_SLICE, a.C - g * Q2_SLICE), T, gsum);
+  }
+  __device__ void ready() {}
+  __device__ void compute(int it, int g, int lane, const Item& b) {
+    const uint32_t lane4 = lane * 4u;
+    const float P0 = plane_sum(lane4, b.w[0], b.w[1]);
+    const float P1 = plane_sum(lane4, b.w[2], b.w[3]);
+    const float P2 = plane_sum(lane4, b.w[4], b.w[5]);
+    float pacc = 0.f;
+    for (int j = 0; j < nbk; ++j) pacc += ((b.pw >> j) & 1u) ? xb[j] : 0.f;
+    const int row = (it - g * a.nrb) * 32 + lane;
+    a.rd.partial[(size_t)g * a.rd.Rpad + row] = fmaf(2.f, P0, fmaf(4.f, P1, fmaf(-8.f, P2, pacc)));
+  }
+};
+
+template <int W, int AHEAD>
+__global__ void __launch_bounds__(W * 32, 1) k_leech_b1(LeechArgs a) {
   int i0, i1;
   cta_range(a.rd.nslice * a.nrb, i0, i1);
   if (threadIdx.x == 0) {
     prefetch_items(a.planes, Q2_ITEM_BYTES_LEECH, i0, i1);
     prefetch_rows(a.parity, 2, a.nrb, a.rd.Rpad, i0, i1);
   }
-  bool waited = false;
-  for (int s0 = i0; s0 < i1;) {
-    const int sl = s0 / a.nrb;
-    const int s1 = min(i1, (sl + 1) * a.nrb);
-    const int bfirst = (sl * Q2_SLICE + 23) / 24;
-    const int blast = min(a.nblock - 1, (sl * Q2_SLICE + Q2_SLICE + 23) / 24 - 1);
-    const int nbk = max(0, blast - bfirst + 1);
-    int it = s0 + warp;
-    uint4 wa[6];
-    if (it < s1) ld_item6(a.planes, it, lane, wa);
-    if (!waited) {
-      pdl_wait();
-      pdl_trigger();
-      waited = true;
-    }
-    __syncthreads();
-    if (threadIdx.x < nbk) {
-      const __half* xp = a.x + (size_t)(bfirst + threadIdx.x) * 24;
-      float v = 0.f;
-      for (int i = 0; i < 24; ++i) v += __half2float(xp[i]);
-      xb[threadIdx.x] = v;
-    }
-    const int ncols = min(Q2_SLICE, a.C - sl * Q2_SLICE);
-    build_table<kThreads>(a.x + (size_t)sl * Q2_SLICE, ncols, T, gsum);
-    for (; it < s1; it += kWarps) {
-      uint4 wn[6];
-      if (it + kWarps < s1) ld_item6(a.planes, it + kWarps, lane, wn);
-      const int row = (it - sl * a.nrb) * 32 + lane;
-      const float P0 = plane_sum(lane4, wa[0], wa[1]);
-      const float P1 = plane_sum(lane4, wa[2], wa[3]);
-      const float P2 = plane_sum(lane4, wa[4], wa[5]);
-      const uint32_t pw = a.parity[(size_t)sl * a.rd.Rpad + row];
-      float pacc = 0.f;
-      for (int j = 0; j < nbk; ++j) pacc += ((pw >> j) & 1u) ? xb[j] : 0.f;
-      // v = p + 2*b0 + 4*b1 - 8*b2 per weight
-      a.rd.partial[(size_t)sl * a.rd.Rpad + row] = fmaf(2.f, P0, fmaf(4.f, P1, fmaf(-8.f, P2, pacc)));
-#pragma unroll
-      for (int k = 0; k < 6; ++k) wa[k] = wn[k];
-    }
-    s0 = s1;
-  }
+  float* T = reinterpret_cast<float*>(q2_smem);
+  LeechF<W * 32> f{a, T, T + (kBuildBytes - 16) / 4, reinterpret_cast<float*>(q2_smem + kBuildBytes), 0};
+  run_items<W, AHEAD>(f, a.nrb, i0, i1);
 }
 
 // ------------------------------------------------------- no-weights control
-// Same grid, PDL, table build, per-lane lookups and handoff as k_bpdq_b1;
+// Same grid, PDL, table build, per-lane lookups and reduction as k_bpdq_b1;
 // the "weight" words are derived from the lane and item index instead of
-// being loaded, so the kernel reads x and writes y and the workspace only.
-__global__ void __launch_bounds__(kThreads, 2) k_noweights_b1(BpdqArgs a) {
-  float* T = reinterpret_cast<float*>(q2_smem);
-  float* gsum = T + (kBuildBytes - 16) / 4;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t lane4 = lane * 4u;
+// being loaded, so the kernel reads x and writes the workspace and y only.
+template <int NT>
+struct NoWeightsF {
+  struct Item {
+    uint32_t h;
+  };
+  const BpdqArgs& a;
+  float* T;
+  float* gsum;
+  __device__ void load(int it, int, int lane, Item& b) const { b.h = (uint32_t)it * 0x9E3779B9u ^ (lane * 0x85EBCA6Bu); }
+  float xs = 0.f;
+  __device__ void slice(int g) { build_table<NT>(a.x + (size_t)g * Q2_SLICE, Q2_SLICE, T, gsum); }
+  __device__ void ready() { xs = *gsum; }
+  __device__ void compute(int it, int g, int lane, const Item& b) {
+    const uint32_t h = b.h, lane4 = lane * 4u;
+    const uint4 w0 = make_uint4(h, h ^ 0x5bd1e995u, h * 3u, h * 5u);
+    const uint4 w1 = make_uint4(h * 7u, h ^ 0x27d4eb2fu, h * 11u, h * 13u);
+    const float S0 = plane_sum(lane4, w0, w1);
+    const float S1 = plane_sum(lane4, w1, w0);
+    const int row = (it - g * a.nrb) * 32 + lane;
+    a.rd.partial[(size_t)g * a.rd.Rpad + row] = fmaf(0.02f, S0, fmaf(0.01f, S1, 0.01f * xs));
+  }
+};
+
+template <int W>
+__global__ void __launch_bounds__(W * 32, 1) k_noweights_b1(BpdqArgs a) {
   int i0, i1;
   cta_range(a.rd.nslice * a.nrb, i0, i1);
-  pdl_wait();
-  pdl_trigger();
-  for (int s0 = i0; s0 < i1;) {
-    const int g = s0 / a.nrb;
-    const int s1 = min(i1, (g + 1) * a.nrb);
-    __syncthreads();
-    build_table<kThreads>(a.x + (size_t)g * Q2_SLICE, Q2_SLICE, T, gsum);
-    const float xg = *gsum;
-    for (int it = s0 + warp; it < s1; it += kWarps) {
-      const uint32_t h = (uint32_t)it * 0x9E3779B9u ^ (lane4 * 0x85EBCA6Bu);
-      const uint4 w0 = make_uint4(h, h ^ 0x5bd1e995u, h * 3u, h * 5u);
-      const uint4 w1 = make_uint4(h * 7u, h ^ 0x27d4eb2fu, h * 11u, h * 13u);
-      const int row = (it - g * a.nrb) * 32 + lane;
-      const float S0 = plane_sum(lane4, w0, w1);
-      const float S1 = plane_sum(lane4, w1, w0);
-      a.rd.partial[(size_t)g * a.rd.Rpad + row] = fmaf(0.02f, S0, fmaf(0.01f, S1, 0.01f * xg));
-    }
-    s0 = s1;
-  }
+  float* T = reinterpret_cast<float*>(q2_smem);
+  NoWeightsF<W * 32> f{a, T, T + (kBuildBytes - 16) / 4};
+  run_items<W, 1>(f, a.nrb, i0, i1);
 }
 
 // ---------------------------------------------------------------- trellis
@@ -263,29 +326,26 @@ __device__ __forceinline__ void ld_trl(const unsigned char* base, int it, int la
   for (int k = 0; k < 4; ++k) w[k] = ldg_stream(p + k * 512);
 }
 
-__global__ void __launch_bounds__(kThreads, 2) k_trellis_b1(TrellisArgs a) {
-  uint32_t* tab = reinterpret_cast<uint32_t*>(q2_smem);                 // 16 KiB
-  uint32_t* xs = reinterpret_cast<uint32_t*>(q2_smem + 4096 * 4);      // x as half2, C/2 words
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int i0, i1;
-  cta_range(a.rd.nslice * a.nrb, i0, i1);
-  if (threadIdx.x == 0) prefetch_items(a.stream, Q2_ITEM_BYTES_TRL, i0, i1);
-  int it = i0 + warp;
-  uint4 wa[4];
-  if (it < i1) ld_trl(a.stream, it, lane, wa);
-  for (int i = threadIdx.x; i < 4096; i += kThreads) tab[i] = a.table[i];
-  pdl_wait();
-  pdl_trigger();
-  const uint32_t* xg = reinterpret_cast<const uint32_t*>(a.x);
-  for (int i = threadIdx.x; i < a.C / 2; i += kThreads) xs[i] = xg[i];
-  __syncthreads();
-  for (; it < i1; it += kWarps) {
-    uint4 wb[4];
-    if (it + kWarps < i1) ld_trl(a.stream, it + kWarps, lane, wb);
+// Items of every segment in one pass: x and the table stay in shared memory
+// for the whole kernel, so the "slice" step of run_items only copies x.
+template <int NT>
+struct TrellisF {
+  struct Item {
+    uint4 w[4];
+  };
+  const TrellisArgs& a;
+  const uint32_t* tab;
+  uint32_t* xs;
+  __device__ void load(int it, int, int lane, Item& b) const { ld_trl(a.stream, it, lane, b.w); }
+  __device__ void slice(int) {
+    const uint32_t* xg = reinterpret_cast<const uint32_t*>(a.x);
+    for (int i = threadIdx.x; i < a.C / 2; i += NT) xs[i] = xg[i];
+  }
+  __device__ void ready() {}
+  __device__ void compute(int it, int, int lane, const Item& b) {
     const int sg = it / a.nrb, rb = it - sg * a.nrb;
-    const int row = rb * 32 + lane;
-    const uint32_t W[16] = {wa[0].x, wa[0].y, wa[0].z, wa[0].w, wa[1].x, wa[1].y, wa[1].z, wa[1].w,
-                            wa[2].x, wa[2].y, wa[2].z, wa[2].w, wa[3].x, wa[3].y, wa[3].z, wa[3].w};
+    const uint32_t W[16] = {b.w[0].x, b.w[0].y, b.w[0].z, b.w[0].w, b.w[1].x, b.w[1].y, b.w[1].z, b.w[1].w,
+                            b.w[2].x, b.w[2].y, b.w[2].z, b.w[2].w, b.w[3].x, b.w[3].y, b.w[3].z, b.w[3].w};
     const uint4* xv = reinterpret_cast<const uint4*>(xs + sg * 128);
     float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
@@ -309,17 +369,37 @@ __global__ void __launch_bounds__(kThreads, 2) k_trellis_b1(TrellisArgs a) {
         }
       }
     }
-    a.rd.partial[(size_t)sg * a.rd.Rpad + row] = acc0 + acc1;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) wa[k] = wb[k];
+    a.rd.partial[(size_t)sg * a.rd.Rpad + rb * 32 + lane] = acc0 + acc1;
   }
+};
+
+constexpr int kTrellisWarps = 16, kTrellisAhead = 1;
+
+template <int W, int AHEAD>
+__global__ void __launch_bounds__(W * 32, 1) k_trellis_b1(TrellisArgs a) {
+  uint32_t* tab = reinterpret_cast<uint32_t*>(q2_smem);                 // 16 KiB
+  uint32_t* xs = reinterpret_cast<uint32_t*>(q2_smem + 4096 * 4);      // x as half2, C/2 words
+  int i0, i1;
+  cta_range(a.rd.nslice * a.nrb, i0, i1);
+  if (threadIdx.x == 0) prefetch_items(a.stream, Q2_ITEM_BYTES_TRL, i0, i1);
+  for (int i = threadIdx.x; i < 4096; i += W * 32) tab[i] = a.table[i];
+  TrellisF<W * 32> f{a, tab, xs};
+  run_items<W, AHEAD>(f, 1 << 30, i0, i1);         // one pass over all segments
 }
+
+// Batch-1 kernels ask for more than half of an SM's shared memory, so an SM
+// never holds two CTAs of them.  Under programmatic dependent launch the
+// next GEMV's CTAs are placed while the current GEMV drains; an SM whose
+// CTA has already left could otherwise take two CTAs of the same grid (and
+// another SM none), and those two would set the GEMV's end.
+constexpr int kOneCtaSmem = 116 * 1024;
+static_assert(kBuildBytes + 64 <= kOneCtaSmem, "batch-1 tables fit the one-CTA footprint");
 
 template <typename A>
 int launch(const q2_handle* h, void (*kernel)(A), const A& args, int smem, int items, const void* x, void* y,
-           void* stream) {
+           void* stream, int threads) {
   const int grid = max(1, min(items, dev_info().sms));
-  const int st = launch_pdl(kernel, args, grid, kThreads, smem, stream);
+  const int st = launch_pdl(kernel, args, grid, threads, smem, stream);
   return st ? st : q2_launch_reduce(h, x, y, 1, stream);
 }
 
@@ -347,7 +427,8 @@ extern "C" int q2_b1_bpdq(const q2_handle* h, const void* x, void* y, void* stre
   a.rd = make_reduce(h);
   a.R = d.R;
   a.nrb = q2_nrb(d);
-  return launch(h, k_bpdq_b1, a, kBuildBytes, d.nslice * a.nrb, x, y, stream);
+  return launch(h, k_bpdq_b1<kBpdqWarps, kBpdqAhead>, a, kOneCtaSmem, d.nslice * a.nrb, x, y, stream,
+                kBpdqWarps * 32);
 }
 
 extern "C" int q2_b1_noweights(const q2_handle* h, const void* x, void* y, void* stream) {
@@ -358,7 +439,7 @@ extern "C" int q2_b1_noweights(const q2_handle* h, const void* x, void* y, void*
   a.rd = make_reduce(h);
   a.R = d.R;
   a.nrb = q2_nrb(d);
-  return launch(h, k_noweights_b1, a, kBuildBytes, d.nslice * a.nrb, x, y, stream);
+  return launch(h, k_noweights_b1<kBpdqWarps>, a, kOneCtaSmem, d.nslice * a.nrb, x, y, stream, kBpdqWarps * 32);
 }
 
 extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* stream) {
@@ -380,7 +461,8 @@ extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* str
   a.tail_n = d.tail;
   a.tailpad = d.tailpad;
   a.inv_sqrt8 = d.inv_sqrt8;
-  return launch(h, k_leech_b1, a, kBuildBytes + 64, d.nslice * a.nrb, x, y, stream);
+  return launch(h, k_leech_b1<kLeechWarps, kLeechAhead>, a, kOneCtaSmem, d.nslice * a.nrb, x, y, stream,
+                kLeechWarps * 32);
 }
 
 extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* stream) {
@@ -395,8 +477,9 @@ extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* s
   a.R = d.R;
   a.C = d.C;
   a.nrb = q2_nrb(d);
-  const int smem = 4096 * 4 + d.C * 2;
-  return launch(h, k_trellis_b1, a, smem, d.nslice * a.nrb, x, y, stream);
+  const int smem = std::max(4096 * 4 + d.C * 2, kOneCtaSmem);
+  return launch(h, k_trellis_b1<kTrellisWarps, kTrellisAhead>, a, smem, d.nslice * a.nrb, x, y, stream,
+                kTrellisWarps * 32);
 }
 
 // ---------------------------------------------------------------------------

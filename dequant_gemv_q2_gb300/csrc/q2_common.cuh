@@ -47,6 +47,33 @@ __device__ __forceinline__ float fma_h(unsigned short a, unsigned short b, float
 __device__ __forceinline__ unsigned short lo16(uint32_t v) { return (unsigned short)(v & 0xffffu); }
 __device__ __forceinline__ unsigned short hi16(uint32_t v) { return (unsigned short)(v >> 16); }
 
+// -------------------------------------------------------------- mbarriers
+constexpr long long kSpinLimit = 1ll << 24;   // bounded mbarrier waits
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Wait for the phase with the given parity to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (long long i = 0; i < kSpinLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
 // ------------------------------------------------------- subset-sum tables
 // For one 256-column slice of x, T[v][b] = sum of x[8b + i] over the set bits
 // i of the byte v (b = 0..31), stored twice per v (columns b and b + 32) so a
@@ -55,7 +82,8 @@ __device__ __forceinline__ unsigned short hi16(uint32_t v) { return (unsigned sh
 // nibble h) tasks loads the 8 x values of byte b, forms the 16 sums of its
 // low nibble by doubling, adds the sum selected by h, and writes the 16
 // entries T[16h + l][b] (consecutive b across a warp: conflict-free stores).
-// Also returns the slice sum of x in *gsum.
+// Also returns the slice sum of x in *gsum.  The caller synchronises the
+// building threads before any of them reads T.
 constexpr int kTableBytes = 256 * 64 * 4;
 constexpr int kBuildBytes = kTableBytes + 16;
 
@@ -104,7 +132,6 @@ __device__ __forceinline__ void build_table(const __half* __restrict__ xg, int n
       if (b == 0) *gsum = v;
     }
   }
-  __syncthreads();
 }
 
 // ---------------------------------------------------- split-K reduction

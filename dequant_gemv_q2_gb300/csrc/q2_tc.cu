@@ -38,11 +38,6 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kRows = 128;                    // M of the MMA
 constexpr int kTileA = kRows * 256 * 2;       // 64 KiB per A buffer
 constexpr uint32_t kLBO = 128, kSBO = 4096;   // core-matrix strides (bytes)
-constexpr long long kSpinLimit = 1ll << 24;   // bounded mbarrier waits
-
-__device__ __forceinline__ uint32_t saddr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
 
 // Shared-memory matrix descriptor (tcgen05): start >> 4 in bits 0-13,
 // leading byte offset >> 4 in 16-29, stride byte offset >> 4 in 32-45,
@@ -60,26 +55,6 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
 // (7-9, 10-12 = 0), both K-major (15, 16 = 0), N >> 3 in 17-22, M >> 4 in 24-28.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-// Wait for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (long long i = 0; i < kSpinLimit; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
