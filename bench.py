@@ -40,7 +40,7 @@ L2_BYTES = 126 * 1024 * 1024
 # stack's traffic per launch is that ratio times the stack's algorithmic
 # bytes per launch (traffic scales with the items processed).  Must be reset
 # to None whenever the kernel changes.
-NCU_TRAFFIC_RATIO: dict = {}
+NCU_TRAFFIC_RATIO = {"k_bpdq_b1": 27559680 / 27525120}
 
 
 def _peaks():
@@ -395,7 +395,7 @@ def run_reference(args, ws, rank):
 
 
 def profile_case(fmt: str, launches: int = 4, ntok: int = 1):
-    """A few launches of one config-shaped matrix per format, for ncu captures
+    """A few launches of one layer-shaped matrix per format, for ncu captures
     (no timing): bpdq 24576x4096 and 4096x12288, trellis 12288x4096, leech
     17408x5120, fp16 4096x4096, noweights 24576x4096."""
     import torch
