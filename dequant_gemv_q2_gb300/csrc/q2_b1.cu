@@ -58,7 +58,8 @@ struct BpdqArgs {
   const __half* x;
   __half* y;
   Reduce rd;
-  int R, nrb;
+  int R, C, nrb;
+  int ntok;            // tokens (the multi-token kernel; 1 elsewhere)
 };
 
 __device__ __forceinline__ void ld_item4(const unsigned char* base, int it, int lane, uint4 (&w)[4]) {
@@ -302,6 +303,159 @@ __global__ void __launch_bounds__(W * 32, 1) k_noweights_b1(BpdqArgs a) {
   run_items<W, 1>(f, a.nrb, i0, i1);
 }
 
+// ------------------------------------------------- BPDQ, 2 to 6 tokens
+// The subset-sum method for several tokens at once.  For the token pair
+// (2p, 2p+1) the slice's table holds float2 entries
+//   E_p[v][b] = (sum of x_2p over the set bits of byte v at column-byte b,
+//                the same for x_2p+1)
+// at byte offset p*64 KiB + v*256 + b*8, with no duplicated columns: a lane
+// at rotated position P reads column-byte b = (P + lane) mod 32, whose
+// address byte b*8 it keeps in one of 11 lane-constant registers (three
+// positions each), so one byte permute still forms v*256 + b*8.  Each
+// lookup is then one 8-byte shared load and one packed fp32 add per token
+// pair; a half-warp's 16 lanes read 16 different column-bytes (conflict-free).
+constexpr int kMtMaxTok = 6;
+constexpr int kPairBytes = 256 * 32 * 8;                   // 64 KiB per token pair
+
+template <int NT, int NP>
+__device__ __forceinline__ void build_pairs(const __half* __restrict__ x, int ntok, int ldx, int col0, float* T,
+                                            float* gsum) {
+  for (int e = threadIdx.x; e < 512 * NP; e += NT) {
+    const int p = e >> 9, h = (e >> 5) & 15, b = e & 31;
+    float xa[8], xb[8];
+    {
+      const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)(2 * p) * ldx + col0 + 8 * b);
+      const __half2* hv = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __half22float2(hv[k]);
+        xa[2 * k] = f.x;
+        xa[2 * k + 1] = f.y;
+      }
+    }
+    if (2 * p + 1 < ntok) {                            // an odd count leaves the last pair half empty
+      const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)(2 * p + 1) * ldx + col0 + 8 * b);
+      const __half2* hv = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __half22float2(hv[k]);
+        xb[2 * k] = f.x;
+        xb[2 * k + 1] = f.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xb[i] = 0.f;
+    }
+    float2 hs = make_float2(0.f, 0.f);                  // sums selected by the high nibble h
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if ((h >> i) & 1) {
+        hs.x += xa[4 + i];
+        hs.y += xb[4 + i];
+      }
+    float2 sv[16];
+    sv[0] = hs;
+#pragma unroll
+    for (int n = 1; n < 16; ++n) {
+      const int low = n & -n;
+      const int i = (low == 1) ? 0 : (low == 2) ? 1 : (low == 4) ? 2 : 3;
+      sv[n] = make_float2(sv[n ^ low].x + xa[i], sv[n ^ low].y + xb[i]);
+    }
+    float2* col = reinterpret_cast<float2*>(reinterpret_cast<char*>(T) + p * kPairBytes) + (h * 16) * 32 + b;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) col[n * 32] = sv[n];
+    if (h == 15) {                                      // this warp holds the 32 bytes' full sums
+      float va = sv[15].x, vb = sv[15].y;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        va += __shfl_xor_sync(0xffffffffu, va, o);
+        vb += __shfl_xor_sync(0xffffffffu, vb, o);
+      }
+      if (b == 0) {
+        gsum[2 * p] = va;
+        gsum[2 * p + 1] = vb;
+      }
+    }
+  }
+}
+
+template <int NT, int NP>
+struct BpdqMtF {
+  struct Item {
+    uint4 w[4];
+    uint32_t c01;
+    unsigned short off;
+  };
+  const BpdqArgs& a;
+  float* T;
+  float* gsum;
+  uint32_t rot[11];      // byte j of rot[k]: ((3k + j + lane) mod 32) * 8; byte 3 = 0
+  float xs[2 * NP];      // per-token sums of x over the slice
+  __device__ void init(int lane) {
+#pragma unroll
+    for (int k = 0; k < 11; ++k) {
+      uint32_t r = 0;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) r |= (uint32_t)(((3 * k + j + lane) & 31) * 8) << (8 * j);
+      rot[k] = r;
+    }
+  }
+  __device__ void load(int it, int g, int lane, Item& b) const {
+    ld_item4(a.bits, it, lane, b.w);
+    const size_t r = (size_t)g * a.rd.Rpad + (size_t)(it - g * a.nrb) * 32 + lane;
+    b.c01 = __ldg(reinterpret_cast<const unsigned int*>(a.c01) + r);
+    b.off = __ldg(reinterpret_cast<const unsigned short*>(a.off) + r);
+  }
+  __device__ void slice(int g) { build_pairs<NT, NP>(a.x, a.ntok, a.C, g * Q2_SLICE, T, gsum); }
+  __device__ void ready() {
+#pragma unroll
+    for (int t = 0; t < 2 * NP; ++t) xs[t] = gsum[t];
+  }
+  __device__ void plane(const uint4& c0, const uint4& c1, float2 (&S)[NP]) const {
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const char* base = reinterpret_cast<const char*>(T);
+#pragma unroll
+    for (int P = 0; P < 32; ++P) {
+      const uint32_t sel = (4u + (uint32_t)(P % 3)) | ((uint32_t)(P & 3) << 4) | 0x7700u;
+      const uint32_t ad = __byte_perm(w[P >> 2], rot[P / 3], sel);
+#pragma unroll
+      for (int p = 0; p < NP; ++p) S[p] = __fadd2_rn(S[p], *reinterpret_cast<const float2*>(base + p * kPairBytes + ad));
+    }
+  }
+  __device__ void compute(int it, int g, int lane, const Item& b) {
+    float2 S0[NP], S1[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) S0[p] = S1[p] = make_float2(0.f, 0.f);
+    plane(b.w[0], b.w[1], S0);
+    plane(b.w[2], b.w[3], S1);
+    const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&b.c01));
+    const float of = __half2float(__ushort_as_half(b.off));
+    const int row = (it - g * a.nrb) * 32 + lane;
+    float* out = a.rd.partial + (size_t)g * a.rd.Rpad + row;
+    const size_t tstride = (size_t)a.rd.nslice * a.rd.Rpad;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      out[(2 * p) * tstride] = fmaf(c.x, S0[p].x, fmaf(c.y, S1[p].x, of * xs[2 * p]));
+      if (2 * p + 1 < a.ntok) out[(2 * p + 1) * tstride] = fmaf(c.x, S0[p].y, fmaf(c.y, S1[p].y, of * xs[2 * p + 1]));
+    }
+  }
+};
+
+template <int W, int AHEAD, int NP>
+__global__ void __launch_bounds__(W * 32, 1) k_bpdq_mt(BpdqArgs a) {
+  int i0, i1;
+  cta_range(a.rd.nslice * a.nrb, i0, i1);
+  if (threadIdx.x == 0) {
+    prefetch_items(a.bits, Q2_ITEM_BYTES_BPDQ, i0, i1);
+    prefetch_rows(a.c01, 4, a.nrb, a.rd.Rpad, i0, i1);
+    prefetch_rows(a.off, 2, a.nrb, a.rd.Rpad, i0, i1);
+  }
+  float* T = reinterpret_cast<float*>(q2_smem);
+  BpdqMtF<W * 32, NP> f{a, T, reinterpret_cast<float*>(q2_smem + NP * kPairBytes)};
+  f.init(threadIdx.x & 31);
+  run_items<W, AHEAD>(f, a.nrb, i0, i1);
+}
+
 // ---------------------------------------------------------------- trellis
 // Lane = row, item = (segment, 32 rows).  The 16 KiB table and all of x sit
 // in shared memory for the whole kernel.  Step k of a segment reads the
@@ -397,10 +551,10 @@ static_assert(kBuildBytes + 64 <= kOneCtaSmem, "batch-1 tables fit the one-CTA f
 
 template <typename A>
 int launch(const q2_handle* h, void (*kernel)(A), const A& args, int smem, int items, const void* x, void* y,
-           void* stream, int threads) {
+           void* stream, int threads, int ntok = 1) {
   const int grid = max(1, min(items, dev_info().sms));
   const int st = launch_pdl(kernel, args, grid, threads, smem, stream);
-  return st ? st : q2_launch_reduce(h, x, y, 1, stream);
+  return st ? st : q2_launch_reduce(h, x, y, ntok, stream);
 }
 
 Reduce make_reduce(const q2_handle* h) {
@@ -426,9 +580,38 @@ extern "C" int q2_b1_bpdq(const q2_handle* h, const void* x, void* y, void* stre
   a.y = static_cast<__half*>(y);
   a.rd = make_reduce(h);
   a.R = d.R;
+  a.C = d.C;
   a.nrb = q2_nrb(d);
+  a.ntok = 1;
   return launch(h, k_bpdq_b1<kBpdqWarps, kBpdqAhead>, a, kOneCtaSmem, d.nslice * a.nrb, x, y, stream,
                 kBpdqWarps * 32);
+}
+
+// BPDQ at 2..6 tokens on CUDA cores (x is [ntok][C]; partials [ntok][nslice][Rpad]).
+extern "C" int q2_mt_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
+  const q2_blob_header& d = h->hdr;
+  BpdqArgs a;
+  a.bits = h->dev + d.off[SEC_BPDQ_BITS];
+  a.c01 = reinterpret_cast<const __half2*>(h->dev + d.off[SEC_BPDQ_C01]);
+  a.off = reinterpret_cast<const __half*>(h->dev + d.off[SEC_BPDQ_OFF]);
+  a.x = static_cast<const __half*>(x);
+  a.y = static_cast<__half*>(y);
+  a.rd = make_reduce(h);
+  a.R = d.R;
+  a.C = d.C;
+  a.nrb = q2_nrb(d);
+  a.ntok = ntok;
+  if (ntok < 2 || ntok > kMtMaxTok) return Q2_ENTOK;
+  const int items = d.nslice * a.nrb;
+  constexpr int W = 16;
+  const int np = (ntok + 1) / 2;
+  const int smem = std::max(kOneCtaSmem, np * kPairBytes + 64);
+  switch (np) {
+    case 1: return launch(h, k_bpdq_mt<W, 2, 1>, a, smem, items, x, y, stream, W * 32, ntok);
+    case 2: return launch(h, k_bpdq_mt<W, 1, 2>, a, smem, items, x, y, stream, W * 32, ntok);
+    case 3: return launch(h, k_bpdq_mt<W, 1, 3>, a, smem, items, x, y, stream, W * 32, ntok);
+    default: return Q2_ENTOK;
+  }
 }
 
 extern "C" int q2_b1_noweights(const q2_handle* h, const void* x, void* y, void* stream) {
@@ -438,7 +621,9 @@ extern "C" int q2_b1_noweights(const q2_handle* h, const void* x, void* y, void*
   a.y = static_cast<__half*>(y);
   a.rd = make_reduce(h);
   a.R = d.R;
+  a.C = d.C;
   a.nrb = q2_nrb(d);
+  a.ntok = 1;
   return launch(h, k_noweights_b1<kBpdqWarps>, a, kOneCtaSmem, d.nslice * a.nrb, x, y, stream, kBpdqWarps * 32);
 }
 

@@ -12,6 +12,7 @@ extern "C" int q2_b1_bpdq(const q2_handle* h, const void* x, void* y, void* stre
 extern "C" int q2_b1_noweights(const q2_handle* h, const void* x, void* y, void* stream);
 extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* stream);
 extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* stream);
+extern "C" int q2_mt_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
 extern "C" int q2_tc_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
 extern "C" int q2_tc_trellis(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
 extern "C" int q2_tc_leech(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
@@ -58,8 +59,12 @@ int set_smem(const void* fn, int bytes) {
 
 extern "C" {
 
+// BPDQ: batch 1 and 2..6 tokens on CUDA cores (subset-sum tables), 7..64 on
+// the tensor cores.
 int q2_launch_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
-  return ntok == 1 ? q2_b1_bpdq(h, x, y, stream) : q2_tc_bpdq(h, x, y, ntok, stream);
+  if (ntok == 1) return q2_b1_bpdq(h, x, y, stream);
+  if (ntok <= 6) return q2_mt_bpdq(h, x, y, ntok, stream);
+  return q2_tc_bpdq(h, x, y, ntok, stream);
 }
 
 int q2_launch_trellis(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {

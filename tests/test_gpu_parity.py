@@ -47,7 +47,7 @@ def _check(y, w64, x, rows=None):
 
 # ------------------------------------------------------------------- BPDQ
 @pytest.mark.parametrize("R,C,seed", [(1024, 1024, 0), (70, 768, 1), (32, 256, 2), (1, 512, 3)])
-@pytest.mark.parametrize("ntok", [1, 2, 5, 16, 64])
+@pytest.mark.parametrize("ntok", [1, 2, 3, 4, 5, 6, 7, 16, 64])
 def test_bpdq_parity(q2, R, C, seed, ntok):
     d = synth.bpdq(R, C, seed)
     x = synth.activations(ntok, C, seed)
@@ -66,6 +66,33 @@ def test_bpdq_tensor_path_shapes_and_error_word(q2, ntok):
         w = obpdq.decode_f64(d["plane0"][rows], d["plane1"][rows], d["coef"][:, rows])
         _check(y, w, x, rows)
     assert q2.device_errors() == 0
+
+
+@pytest.mark.parametrize("ntok", [2, 3, 6])
+def test_bpdq_multitoken_subset_sum_full_size(q2, ntok):
+    # 8B-shaped rows and columns through the 2..6-token CUDA-core path, sampled rows
+    for R, C, seed in [(24576, 4096, 21), (4096, 12288, 22)]:
+        d = synth.bpdq(R, C, seed)
+        x = synth.activations(ntok, C, seed)
+        _, y = _run(q2, q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]), x)
+        rows = _sampled_rows(R, seed=seed)
+        w = obpdq.decode_f64(d["plane0"][rows], d["plane1"][rows], d["coef"][:, rows])
+        _check(y, w, x, rows)
+
+
+def test_bpdq_multitoken_matches_single_token_runs(q2):
+    # each token of a 4-token call equals the same token run alone, to the
+    # parity tolerance (the two paths sum in different orders)
+    d = synth.bpdq(512, 2048, 23)
+    x = synth.activations(4, 2048, 23)
+    pk = q2.Packed(q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]))
+    y4 = pk.gemv(torch.from_numpy(x).cuda()).cpu().numpy()
+    w = obpdq.decode_f64(d["plane0"], d["plane1"], d["coef"])
+    bound = matvec.abs_bound(w, x)
+    for t in range(4):
+        y1 = pk.gemv(torch.from_numpy(x[t:t + 1].copy()).cuda()).cpu().numpy()
+        diff = np.abs(y4[t].astype(np.float64) - y1[0].astype(np.float64))
+        assert (diff <= 2 * TOL * bound[t]).all()
 
 
 def test_bpdq_decode_bit_exact(q2):
