@@ -38,9 +38,9 @@ L2_BYTES = 126 * 1024 * 1024
 # profiles/bpdq_b1_qwen3_8b_stack.md: (dram__bytes_read.sum +
 # dram__bytes_write.sum) / algorithmic bytes on a 24576x4096 launch.  The
 # stack's traffic per launch is that ratio times the stack's algorithmic
-# bytes per launch (traffic scales with the items processed).  Must be reset
-# to None whenever the kernel changes.
-NCU_TRAFFIC_RATIO = {"k_bpdq_b1": 27559680 / 27525120}
+# bytes per launch (traffic scales with the items processed).  None until
+# the current kernel has been captured.
+NCU_TRAFFIC_RATIO = {"k_bpdq_b1": None}
 
 
 def _peaks():
@@ -528,7 +528,8 @@ def main():
         extras = per_format(q2, stream, hbm)
 
     achieved = step_bytes / (ms_step * 1e-3) / 1e9
-    kname = "k_bpdq_b1" if args.ntok == 1 else "k_tc"
+    kname = "k_bpdq_b1" if args.ntok == 1 else ("k_bpdq_mt" if args.ntok <= 6 else "k_tc")
+    launches_per_gemv = 1 if args.ntok <= 6 else 2
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
@@ -537,14 +538,15 @@ def main():
             "data": "synthetic (seeded BPDQ weights and N(0,1) fp16 activations of the Qwen3-8B shapes)",
             "config": {"workload": "BPDQ Qwen3-8B-shaped decode stack: 36 layers x (qkv 4096->6144, o 4096->4096, "
                                    "gate_up 4096->24576, down 12288->4096), linears only",
-                       "ntok": args.ntok, "launches_per_step": len(lin), "bytes_per_step": step_bytes,
+                       "ntok": args.ntok, "launches_per_step": len(lin) * launches_per_gemv,
+                       "bytes_per_step": step_bytes,
                        "l2": "weights 1.9 GB > L2, no flush", "parallelism": "replicas" if ws > 1 else "single"},
             "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                          "traffic": (round(NCU_TRAFFIC_RATIO[kname] * step_bytes / len(lin))
                                      if NCU_TRAFFIC_RATIO.get(kname) else None),
                          "traffic_unit": "bytes per launch"},
-            "gpu_launches": len(lin) * args.steps,
+            "gpu_launches": len(lin) * launches_per_gemv * args.steps,
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "us_per_gemv_avg": round(ms_step * 1e3 / len(lin), 3),

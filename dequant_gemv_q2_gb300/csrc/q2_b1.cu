@@ -1,10 +1,20 @@
 // Batch-1 kernels (ntok == 1) for the packed formats and the no-weights
-// control.  One lane owns one output row; a warp owns 32 rows of one
-// 256-column slice (an "item").  CTAs take contiguous, equal shares of the
-// items in slice-major order and keep the x-dependent tables of the current
-// slice in shared memory.  Per-slice partial sums go to the workspace with
-// plain stores; a second launch (q2_reduce.cu) sums them in slice order
-// (deterministic) and writes y.
+// control, and BPDQ at 2..6 tokens.  One lane owns one output row; a warp
+// owns 32 rows of one 256-column slice (an "item").  CTAs take contiguous,
+// equal shares of the items in slice-major order, so a CTA touches one or a
+// few slices; it builds the x-dependent table of each slice in shared
+// memory and streams the slice's items.
+//
+// The split-K reduction happens inside the launch and needs no fence and no
+// second pass: each lane adds its fp32 slice partial, converted to a 48-bit
+// fixed-point integer (scale 2^F, F chosen per matrix so that no partial of
+// any fp16 x can overflow), together with an arrival count of one, to the
+// 64-bit accumulator word of its (token, row) with a single atomic.
+// Integer addition is associative, so the sum is the same whatever order
+// the slices arrive in (deterministic); the lane whose addition brings the
+// count to the number of slices holds the complete sum in the atomic's
+// return value, converts it back, applies the format's epilogue, writes y
+// and resets the word to zero.  Nothing ever waits on another CTA.
 //
 // BPDQ and Leech use subset-sum tables in place of a per-weight decode: for
 // each 8-column byte of a bit-plane the table holds the sum of the x values
@@ -15,14 +25,16 @@
 // column-bytes of its row in an order rotated by its lane index, so the 32
 // lanes of a load always hit 32 different banks.
 //
-// One CTA of 16 warps per SM (grid = SM count; each CTA asks for more than
-// half of the SM's shared memory so no SM ever holds two).  Launches use
-// programmatic dependent launch: a CTA prefetches its weights into L2 and
-// its first items into registers, then waits for the previous kernel on the
-// stream (griddepcontrol) before it touches x or the workspace, and lets the
-// dependent reduction and the next GEMV's CTAs get scheduled while it runs.
+// One 16-warp CTA per SM (grid = SM count; each CTA asks for more than half
+// of the SM's shared memory).  Launches use programmatic dependent launch: a
+// CTA loads its first items into registers, then waits for the previous
+// kernel on the stream (griddepcontrol.wait) before it touches x, y or the
+// workspace, and triggers its own dependents right after.  Measured on
+// GB300: bulk L2 prefetches of the CTA's weights (or of the next GEMV's)
+// issued before the wait made every shape slower, so there are none.
 #include <cuda_fp16.h>
 
+#include <cmath>
 #include <mutex>
 #include <vector>
 
@@ -30,119 +42,294 @@
 
 extern __shared__ __align__(1024) unsigned char q2_smem[];
 
-extern "C" int q2_launch_reduce(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
-
 namespace q2 {
 namespace {
 
-
-// T lookup for byte b of word at rotated position P (see build_table).
-__device__ __forceinline__ float tl(uint32_t lane4, uint32_t word, int b, int P) {
-  const uint32_t a = __byte_perm(word, lane4, 0x5504u | ((uint32_t)b << 4));
-  return *reinterpret_cast<const float*>(q2_smem + a + P * 4);
-}
-
-// Sum of the table entries selected by 32 rotated bytes (two uint4 chunks).
-__device__ __forceinline__ float plane_sum(uint32_t lane4, const uint4& c0, const uint4& c1) {
-  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int P = 0; P < 32; ++P) s[P & 3] += tl(lane4, w[P >> 2], P & 3, P);
-  return (s[0] + s[1]) + (s[2] + s[3]);
-}
-
-struct BpdqArgs {
-  const unsigned char* bits;
-  const __half2* c01;
-  const __half* off;
-  const __half* x;
-  __half* y;
-  Reduce rd;
-  int R, C, nrb;
-  int ntok;            // tokens (the multi-token kernel; 1 elsewhere)
+// ------------------------------------------------------------ shared state
+struct B1 {
+  const __half* x;              // [ntok][C]
+  __half* y;                    // [ntok][R]
+  unsigned long long* acc;      // [ntok][Rpad] accumulator words (zero between calls)
+  float fscale, finv;           // 2^F and 2^-F of the fixed-point partials
+  int R, C, Rpad, nrb, nslice, ntok;
 };
 
-__device__ __forceinline__ void ld_item4(const unsigned char* base, int it, int lane, uint4 (&w)[4]) {
-  const unsigned char* p = base + (size_t)it * Q2_ITEM_BYTES_BPDQ + lane * 16;
+// Shared memory of the single-token table kernels: a small tail at the
+// start of dynamic shared memory (slice sums of x, Leech block sums, staged
+// x: up to kStageBytes / (512 * ntok) slices at once), then the table of the
+// current slice, placed at shared-window address kTabAddr so that the byte
+// permute of a lookup forms the final shared address by itself.
+constexpr int kTab = 64 * 1024;        // one slice's table (duplicated columns)
+constexpr uint32_t kTabAddr = 65536;   // shared-window address of the table
+constexpr int kTabSmem = 2 * kTab;     // dynamic smem that reaches past kTabAddr + kTab
+constexpr int kTailGsum = 0;           // float [8]
+constexpr int kTailXb = 128;           // float [kStageMax][12], Leech block sums
+constexpr int kTailX = 512;            // fp16 staged x [slice][tok][256]
+constexpr int kStageBytes = 4096;
+constexpr int kStageMax = kStageBytes / 512;
+constexpr int kTailFixed = kTailX + kStageBytes;
+
+// x of slices [g0, g0 + nt) for tokens 0..ntok-1 into smem, as fp16
+// [t][tok][256] (columns past C read as zero); one 16-byte load per thread.
+template <int NT>
+__device__ __forceinline__ void stage_x(const B1& c, int g0, int nt, __half* xs) {
+  const int per_slice = c.ntok * 32;
+  for (int i = threadIdx.x; i < nt * per_slice; i += NT) {
+    const int t = i / per_slice, r = i - t * per_slice;
+    const int tok = r >> 5;
+    const int col = (g0 + t) * Q2_SLICE + (r & 31) * 8;
+    const __half* src = c.x + (size_t)tok * c.C + col;
+    uint4 v;
+    if (col + 8 <= c.C) {
+      v = *reinterpret_cast<const uint4*>(src);
+    } else {
+      __half hv[8];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) w[k] = ldg_stream(p + k * 512);
-}
-
-// The CTA's items are contiguous in the bit stream, and the coefficients of a
-// slice's row blocks are contiguous too: thread 0 prefetches all of them
-// into L2 before waiting on the previous kernel, so the weight stream of
-// this GEMV overlaps the tail of the previous one.
-__device__ __forceinline__ void prefetch_items(const unsigned char* base, int item_bytes, int i0, int i1) {
-  if (i1 > i0) prefetch_l2(base + (size_t)i0 * item_bytes, (size_t)(i1 - i0) * item_bytes);
-}
-
-__device__ __forceinline__ void prefetch_rows(const void* base, int elem_bytes, int nrb, int Rpad, int i0, int i1) {
-  // rows of items i0..i1-1 in [slice][Rpad] arrays: one contiguous run per slice
-  for (int s0 = i0; s0 < i1;) {
-    const int g = s0 / nrb, s1 = min(i1, (g + 1) * nrb);
-    const size_t first = (size_t)g * Rpad + (size_t)(s0 - g * nrb) * 32;
-    const size_t n = (size_t)(s1 - s0) * 32 * elem_bytes;
-    const size_t a0 = (first * elem_bytes) & ~(size_t)15;
-    const size_t a1 = (first * elem_bytes + n + 15) & ~(size_t)15;
-    prefetch_l2(static_cast<const char*>(base) + a0, a1 - a0);
-    s0 = s1;
+      for (int k = 0; k < 8; ++k) hv[k] = (col + k < c.C) ? src[k] : __float2half_rn(0.f);
+      v = *reinterpret_cast<const uint4*>(hv);
+    }
+    reinterpret_cast<uint4*>(xs)[i] = v;
   }
 }
 
+// Subset-sum table of one staged slice.  T[v][b] = sum of x[8b + i] over
+// the set bits i of the byte v (b = 0..31), stored twice per v (columns b
+// and b + 32) so a lane at rotated position P reads column P + lane without
+// a modulo: byte address v*256 + lane*4 + P*4.  Each of 512 (column-byte b,
+// high nibble h) tasks forms the 16 sums of its low nibble by doubling, adds
+// the sum selected by h, and writes the 16 entries T[16h + l][b]
+// (consecutive b across a warp: conflict-free stores).  The h = 15 warp also
+// reduces the slice sum of x into *gsum.
+template <int NT>
+__device__ __forceinline__ void build_table(const __half* xs, float* T, float* gsum) {
+  for (int e = threadIdx.x; e < 512; e += NT) {
+    const int h = e >> 5, b = e & 31;
+    const uint4 raw = *reinterpret_cast<const uint4*>(xs + 8 * b);
+    const __half2* hv = reinterpret_cast<const __half2*>(&raw);
+    float x8[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __half22float2(hv[k]);
+      x8[2 * k] = f.x;
+      x8[2 * k + 1] = f.y;
+    }
+    float hs = 0.f;                              // sum selected by the high nibble h (bits 4..7)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) hs += ((h >> i) & 1) ? x8[4 + i] : 0.f;
+    float s[16];
+    s[0] = hs;
+#pragma unroll
+    for (int n = 1; n < 16; ++n) {
+      const int low = n & -n;
+      const int i = (low == 1) ? 0 : (low == 2) ? 1 : (low == 4) ? 2 : 3;
+      s[n] = s[n ^ low] + x8[i];
+    }
+    float* col = T + (h * 16) * 64 + b;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      col[n * 64] = s[n];
+      col[n * 64 + 32] = s[n];
+    }
+    if (h == 15) {                               // this warp holds all 32 bytes' full sums
+      float v = s[15];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (b == 0) *gsum = v;
+    }
+  }
+}
+
+// The table of the single-token kernels, at shared address kTabAddr (the
+// dynamic shared memory starts below it: the window's reserved bytes plus
+// the tail).
+__device__ __forceinline__ float* tab1() {
+  return reinterpret_cast<float*>(q2_smem + (kTabAddr - (uint32_t)__cvta_generic_to_shared(q2_smem)));
+}
+
+// Table lookup for the byte at rotated position P (byte P & 3 of `word`).
+// lane4 holds lane*4 in byte 0 and kTabAddr >> 16 in byte 2, so the permute
+// gives the shared address kTabAddr + v*256 + lane*4 and the load adds P*4.
+template <int P>
+__device__ __forceinline__ float tl(uint32_t lane4, uint32_t word) {
+  const uint32_t a = __byte_perm(word, lane4, 0x7604u | ((uint32_t)(P & 3) << 4));
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(a), "n"(P * 4));
+  return v;
+}
+constexpr uint32_t kLane4Hi = kTabAddr;   // OR-ed into lane*4
+
+// Lookups P and P + 1 into one of two packed fp32 accumulators, then the rest.
+template <int P>
+__device__ __forceinline__ void plane_steps(uint32_t lane4, const uint32_t (&w)[8], float2 (&s)[2]) {
+  if constexpr (P < 32) {
+    const float2 v = make_float2(tl<P>(lane4, w[P >> 2]), tl<P + 1>(lane4, w[(P + 1) >> 2]));
+    s[(P >> 1) & 1] = __fadd2_rn(s[(P >> 1) & 1], v);
+    plane_steps<P + 2>(lane4, w, s);
+  }
+}
+
+// Sum of the table entries selected by 32 rotated bytes (two uint4 chunks),
+// accumulated two lookups at a time with packed fp32 adds.
+__device__ __forceinline__ float plane_sum(uint32_t lane4, const uint4& c0, const uint4& c1) {
+  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  float2 s[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  plane_steps<0>(lane4, w, s);
+  const float2 t = __fadd2_rn(s[0], s[1]);
+  return t.x + t.y;
+}
+
+// ------------------------------------------- fixed-point accumulation
+// Accumulator word: bits 56..63 count the slices added so far; bits 0..55
+// hold the sum of (q + 2^47) over those slices, q = round(partial * 2^F) in
+// [-(2^47 - 1), 2^47 - 1].  At most Q2_MAX_SPLIT (255) biased terms of at
+// most 2^48 each sum below 2^56, so the value never carries into the count.
+constexpr unsigned long long kBias = 1ull << 47;
+constexpr unsigned long long kCountOne = 1ull << 56;
+constexpr unsigned long long kValueMask = kCountOne - 1;
+
+__device__ __forceinline__ unsigned long long fx_term(float p, float fscale) {
+  long long q = __float2ll_rn(p * fscale);
+  q = max(min(q, (long long)kBias - 1), -(long long)kBias + 1);   // NaN/inf partials stay in range
+  return kCountOne + (unsigned long long)(q + (long long)kBias);
+}
+
+// The value of a complete accumulator word (all nslice terms added).
+__device__ __forceinline__ float fx_value(unsigned long long w, int nslice, float finv) {
+  const long long v = (long long)(w & kValueMask) - (long long)nslice * (long long)kBias;
+  return (float)v * finv;
+}
+
+// Atomics a lane has issued for one item (NT tokens), settled one item later
+// so the atomic's round trip overlaps the next item's work.
+template <int NT>
+struct Pending {
+  unsigned long long old[NT], add[NT];
+  int row = -1;
+};
+
+template <int NT>
+__device__ __forceinline__ void acc_issue(Pending<NT>& pd, const B1& c, int row, const float (&p)[NT]) {
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+    if (t < c.ntok) {
+      pd.add[t] = fx_term(p[t], c.fscale);
+      pd.old[t] = atomicAdd(c.acc + (size_t)t * c.Rpad + row, pd.add[t]);
+    }
+  pd.row = row;
+}
+
+template <int NT, class F>
+__device__ __forceinline__ void acc_settle(Pending<NT>& pd, const B1& c, const F& f) {
+  if (pd.row < 0) return;
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+    if (t < c.ntok) {
+      const unsigned long long w = pd.old[t] + pd.add[t];
+      if ((int)(w >> 56) == c.nslice) {                // this lane completed the row
+        if (pd.row < c.R) f.finish(t, pd.row, fx_value(w, c.nslice, c.finv));
+        c.acc[(size_t)t * c.Rpad + pd.row] = 0ull;
+      }
+    }
+  pd.row = -1;
+}
+
 // ------------------------------------------------------- pipelined items
-// run_items drives every subset-sum kernel.  The CTA walks its contiguous
-// item range one slice at a time: item it of a slice goes to warp
-// (it - first item) mod W, and each warp keeps AHEAD items beyond the one
-// it is summing in flight in registers (F::load), so a CTA has
-// (AHEAD + 1) x W items of weights outstanding.  The first AHEAD loads of a
-// slice are issued before the CTA waits on the previous kernel (weights do
-// not depend on it); F::slice then builds the slice's x tables, F::ready
-// reads what every item of the slice shares, and F::compute sums one item
-// and stores its partials.
+// run_b1 drives every split-K kernel.  The CTA's contiguous item range is
+// cut into groups: one slice per group for the table kernels (F::kGroup ==
+// 1), one group for everything in the trellis kernel.  x is staged into
+// shared memory for up to kStageMax / ntok slices at a time (F::kStaged);
+// per group the CTA builds the slice's table (F::tables) and streams the
+// group's items: item j0 + warp + k*W goes to warp `warp`, which keeps AHEAD
+// items beyond the one it is summing in flight in registers (F::load).  The
+// first group's loads are issued before the CTA waits on the previous
+// kernel (weights do not depend on it).  F::compute sums one item into a
+// partial per token, which the lane adds to the row's accumulator word.
 template <int W, int AHEAD, class F>
-__device__ __forceinline__ void run_items(F& f, int nrb, int i0, int i1) {
+__device__ __forceinline__ void run_b1(F& f, const B1& c, unsigned char* tail) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int i0, i1;
+  cta_range(c.nslice * c.nrb, i0, i1);
+  const int glast = (i1 - 1) / c.nrb;
+  __half* xs = reinterpret_cast<__half*>(tail + kTailX);
+  const int stage_n = max(1, kStageMax / c.ntok);
+  int sg0 = 0, sgn = 0;                          // staged slices [sg0, sg0 + sgn)
   bool waited = false;
-  for (int s0 = i0; s0 < i1;) {
-    const int g = s0 / nrb;
-    const int s1 = min(i1, (g + 1) * nrb);
+  Pending<F::kTok> pd;
+  for (int j0 = i0; j0 < i1;) {
+    const int gA = j0 / c.nrb;
+    const int gB = min(glast, gA + F::kGroup - 1);
+    const int j1 = min(i1, (gB + 1) * c.nrb);
     typename F::Item buf[AHEAD + 1];
-    const int it0 = s0 + warp;
+    const int it0 = j0 + warp;
+    // the slice of an item: gA for one-slice groups, else a division
+    auto slice_of = [&](int it) { return F::kGroup == 1 ? gA : it / c.nrb; };
 #pragma unroll
     for (int d = 0; d < AHEAD; ++d)
-      if (it0 + d * W < s1) f.load(it0 + d * W, g, lane, buf[d]);
+      if (it0 + d * W < j1) f.load(it0 + d * W, slice_of(it0 + d * W), lane, buf[d]);
     if (!waited) {
       pdl_wait();
       pdl_trigger();
       waited = true;
+    } else {
+      __syncthreads();                           // the previous group's table is no longer read
     }
-    __syncthreads();                              // every warp is done with the previous tables
-    f.slice(g);
+    if (F::kStaged && gA >= sg0 + sgn) {
+      sg0 = gA;
+      sgn = min(stage_n, glast - gA + 1);
+      stage_x<W * 32>(c, sg0, sgn, xs);
+      f.stage_extra(sg0, sgn, tail);
+      __syncthreads();
+    }
+    f.tables(gA, xs + (size_t)(gA - sg0) * c.ntok * Q2_SLICE, tail);
     __syncthreads();
-    f.ready();
     // the AHEAD + 1 buffers are indexed statically: AHEAD + 1 items per trip
-    for (int base = it0; base < s1; base += (AHEAD + 1) * W) {
+    for (int base = it0; base < j1; base += (AHEAD + 1) * W) {
 #pragma unroll
       for (int u = 0; u <= AHEAD; ++u) {
         const int it = base + u * W;
-        if (it < s1) {
+        if (it < j1) {
           const int nx = it + AHEAD * W;
-          if (nx < s1) f.load(nx, g, lane, buf[(u + AHEAD) % (AHEAD + 1)]);
-          f.compute(it, g, lane, buf[u]);
+          if (nx < j1) f.load(nx, slice_of(nx), lane, buf[(u + AHEAD) % (AHEAD + 1)]);
+          const int g = slice_of(it);
+          float p[F::kTok];
+          f.compute(it, g, lane, buf[u], p);
+          acc_settle(pd, c, f);
+          acc_issue(pd, c, (it - g * c.nrb) * 32 + lane, p);
         }
       }
     }
-    s0 = s1;
+    j0 = j1;
   }
+  if (!waited) {
+    pdl_wait();
+    pdl_trigger();
+  }
+  acc_settle(pd, c, f);
 }
 
-// Launch shapes, measured on GB300: BPDQ 16 warps with 2 items ahead (the
-// 8B stack); Leech, whose items are 1.5x larger, 8 warps with 3 ahead (the
-// 14B layers).
-constexpr int kBpdqWarps = 16, kBpdqAhead = 2;
-constexpr int kLeechWarps = 8, kLeechAhead = 3;
+__device__ __forceinline__ void ld_item(const unsigned char* base, int item_bytes, int it, int lane, uint4* w,
+                                        int n) {
+  const unsigned char* p = base + (size_t)it * item_bytes + lane * 16;
+  for (int k = 0; k < n; ++k) w[k] = ldg_stream(p + k * 512);
+}
+
+// Launch shapes: 8 warps and <= 128 registers per thread, two CTAs per SM.
+// BPDQ keeps 2 items ahead per warp; Leech, whose items are 1.5x larger, 1.
+constexpr int kWarps = 16;
+// CTAs per SM the single-token kernels are built for: two at 8 warps
+// (<= 128 registers), one at 16.
+constexpr int kMinBlocks = kWarps <= 8 ? 2 : 1;
+constexpr int kBpdqAhead = 2;
+constexpr int kLeechAhead = 1;
 
 // ------------------------------------------------------------------- BPDQ
+struct BpdqArgs {
+  B1 c;
+  const unsigned char* bits;
+  const __half2* c01;
+  const __half* off;
+};
+
 template <int NT>
 struct BpdqF {
   struct Item {
@@ -150,157 +337,172 @@ struct BpdqF {
     uint32_t c01;        // c0 | c1 << 16 (fp16)
     unsigned short off;  // fp16
   };
+  static constexpr bool kStaged = true;
+  static constexpr int kGroup = 1;
+  static constexpr int kTok = 1;
   const BpdqArgs& a;
-  float* T;
-  float* gsum;
-  float xs = 0.f;        // sum of x over the slice
   __device__ void load(int it, int g, int lane, Item& b) const {
-    ld_item4(a.bits, it, lane, b.w);
-    const size_t r = (size_t)g * a.rd.Rpad + (size_t)(it - g * a.nrb) * 32 + lane;
+    ld_item(a.bits, Q2_ITEM_BYTES_BPDQ, it, lane, b.w, 4);
+    const size_t r = (size_t)g * a.c.Rpad + (size_t)(it - g * a.c.nrb) * 32 + lane;
     b.c01 = __ldg(reinterpret_cast<const unsigned int*>(a.c01) + r);
     b.off = __ldg(reinterpret_cast<const unsigned short*>(a.off) + r);
   }
-  __device__ void slice(int g) {
-    build_table<NT>(a.x + (size_t)g * Q2_SLICE, Q2_SLICE, T, gsum);
+  __device__ void stage_extra(int, int, unsigned char*) {}
+  __device__ void tables(int, const __half* xs, unsigned char* tail) const {
+    build_table<NT>(xs, tab1(), reinterpret_cast<float*>(tail + kTailGsum));
   }
-  __device__ void ready() { xs = *gsum; }
-  __device__ void compute(int it, int g, int lane, const Item& b) {
-    const uint32_t lane4 = lane * 4u;
+  __device__ void compute(int, int, int lane, const Item& b, float (&p)[1]) const {
+    const uint32_t lane4 = (uint32_t)lane * 4u | kLane4Hi;
     const float S0 = plane_sum(lane4, b.w[0], b.w[1]);
     const float S1 = plane_sum(lane4, b.w[2], b.w[3]);
-    const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&b.c01));
+    const float2 cf = __half22float2(*reinterpret_cast<const __half2*>(&b.c01));
     const float of = __half2float(__ushort_as_half(b.off));
-    const int row = (it - g * a.nrb) * 32 + lane;
-    a.rd.partial[(size_t)g * a.rd.Rpad + row] = fmaf(c.x, S0, fmaf(c.y, S1, of * xs));
+    const float xs = *reinterpret_cast<const float*>(q2_smem + kTailGsum);
+    p[0] = fmaf(cf.x, S0, fmaf(cf.y, S1, of * xs));
   }
+  __device__ void finish(int tok, int row, float v) const { a.c.y[(size_t)tok * a.c.R + row] = __float2half_rn(v); }
 };
 
+// The tail sits at the start of dynamic shared memory for every
+// single-token table kernel.
+__device__ __forceinline__ unsigned char* tail1() { return q2_smem; }
+
 template <int W, int AHEAD>
-__global__ void __launch_bounds__(W * 32, 1) k_bpdq_b1(BpdqArgs a) {
-  int i0, i1;
-  cta_range(a.rd.nslice * a.nrb, i0, i1);
-  if (threadIdx.x == 0) {
-    prefetch_items(a.bits, Q2_ITEM_BYTES_BPDQ, i0, i1);
-    prefetch_rows(a.c01, 4, a.nrb, a.rd.Rpad, i0, i1);
-    prefetch_rows(a.off, 2, a.nrb, a.rd.Rpad, i0, i1);
-  }
-  float* T = reinterpret_cast<float*>(q2_smem);
-  BpdqF<W * 32> f{a, T, T + (kBuildBytes - 16) / 4};
-  run_items<W, AHEAD>(f, a.nrb, i0, i1);
+__global__ void __launch_bounds__(W * 32, kMinBlocks) k_bpdq_b1(BpdqArgs a) {
+  if ((uint32_t)__cvta_generic_to_shared(q2_smem) + kTailFixed > kTabAddr) return;   // layout needs a low window base
+  BpdqF<W * 32> f{a};
+  run_b1<W, AHEAD>(f, a.c, tail1());
 }
 
 // ------------------------------------------------------------------ Leech
 struct LeechArgs {
+  B1 c;
   const unsigned char* planes;
   const uint16_t* parity;     // [nslice][Rpad]
   const __half* scale;        // [Rpad]
   const __half* tail;         // [Rpad][tailpad]
   const uint32_t* excptr;     // [Rpad + 1]
   const uint32_t* exccol;
-  const __half* x;
-  __half* y;
-  Reduce rd;
-  int R, C, nrb, nblock, tail_n, tailpad;
+  int nblock, tail_n, tailpad;
   float inv_sqrt8;
 };
 
-__device__ __forceinline__ void ld_item6(const unsigned char* base, int it, int lane, uint4 (&w)[6]) {
-  const unsigned char* p = base + (size_t)it * Q2_ITEM_BYTES_LEECH + lane * 16;
-#pragma unroll
-  for (int k = 0; k < 6; ++k) w[k] = ldg_stream(p + k * 512);
+// Blocks of 24 columns whose first column lies in slice g.
+__device__ __forceinline__ void leech_blocks(int g, int nblock, int& bfirst, int& nbk) {
+  bfirst = (g * Q2_SLICE + 23) / 24;
+  const int blast = min(nblock - 1, (g * Q2_SLICE + Q2_SLICE + 23) / 24 - 1);
+  nbk = max(0, blast - bfirst + 1);
 }
 
 // The three planes hold the two's-complement bits of u = (v - p)/2 per
 // weight (p = the block's parity bit), so v = p + 2*b0 + 4*b1 - 8*b2: three
-// subset sums plus, per 24-column block of the slice, the block sum of x
-// when the row's parity bit for the block is set.
+// subset sums plus, per 24-column block starting in the slice, the block sum
+// of x when the row's parity bit for the block is set.  The epilogue adds
+// 16 x[col] for each v = +8 exception, multiplies by scale_r / sqrt(8) and
+// adds the fp16 tail ("Tetra", section 5.1: the row scale after the block
+// dot product, then the unquantised tail).
 template <int NT>
 struct LeechF {
   struct Item {
     uint4 w[6];
     uint32_t pw;         // parity bits of the slice's blocks for this row
   };
+  static constexpr bool kStaged = true;
+  static constexpr int kGroup = 1;
+  static constexpr int kTok = 1;
   const LeechArgs& a;
-  float* T;
-  float* gsum;
-  float* xb;             // block sums of x in the slice, <= 11
-  int nbk;
+  int sg0 = 0;           // first staged slice (block sums in the tail are per staged slice)
   __device__ void load(int it, int g, int lane, Item& b) const {
-    ld_item6(a.planes, it, lane, b.w);
-    b.pw = __ldg(a.parity + (size_t)g * a.rd.Rpad + (size_t)(it - g * a.nrb) * 32 + lane);
+    ld_item(a.planes, Q2_ITEM_BYTES_LEECH, it, lane, b.w, 6);
+    b.pw = __ldg(a.parity + (size_t)g * a.c.Rpad + (size_t)(it - g * a.c.nrb) * 32 + lane);
   }
-  __device__ void slice(int g) {
-    const int bfirst = (g * Q2_SLICE + 23) / 24;
-    const int blast = min(a.nblock - 1, (g * Q2_SLICE + Q2_SLICE + 23) / 24 - 1);
-    nbk = max(0, blast - bfirst + 1);
-    if ((int)threadIdx.x < nbk) {
-      const __half* xp = a.x + (size_t)(bfirst + threadIdx.x) * 24;
-      float v = 0.f;
-      for (int i = 0; i < 24; ++i) v += __half2float(xp[i]);
-      xb[threadIdx.x] = v;
+  // block sums of x for the blocks that start in each staged slice (<= 11
+  // each; a block may run into the next slice, so they are read from x)
+  __device__ void stage_extra(int s0, int sn, unsigned char* tail) {
+    sg0 = s0;
+    float* xb = reinterpret_cast<float*>(tail + kTailXb);
+    for (int i = threadIdx.x; i < sn * 12; i += NT) {
+      const int t = i / 12, j = i - t * 12;
+      int bfirst, nbk;
+      leech_blocks(s0 + t, a.nblock, bfirst, nbk);
+      if (j < nbk) {
+        const __half* xp = a.c.x + (size_t)(bfirst + j) * 24;
+        float v = 0.f;
+#pragma unroll
+        for (int k = 0; k < 24; ++k) v += __half2float(xp[k]);
+        xb[i] = v;
+      }
     }
-    build_table<NT>(a.x + (size_t)g * Q2_SLICE, min(Q2_SLICE, a.C - g * Q2_SLICE), T, gsum);
   }
-  __device__ void ready() {}
-  __device__ void compute(int it, int g, int lane, const Item& b) {
-    const uint32_t lane4 = lane * 4u;
+  __device__ void tables(int, const __half* xs, unsigned char* tail) const {
+    build_table<NT>(xs, tab1(), reinterpret_cast<float*>(tail + kTailGsum));
+  }
+  __device__ void compute(int, int g, int lane, const Item& b, float (&p)[1]) const {
+    const uint32_t lane4 = (uint32_t)lane * 4u | kLane4Hi;
     const float P0 = plane_sum(lane4, b.w[0], b.w[1]);
     const float P1 = plane_sum(lane4, b.w[2], b.w[3]);
     const float P2 = plane_sum(lane4, b.w[4], b.w[5]);
+    int bfirst, nbk;
+    leech_blocks(g, a.nblock, bfirst, nbk);
+    const float* xb = reinterpret_cast<const float*>(q2_smem + kTailXb) + (g - sg0) * 12;
     float pacc = 0.f;
     for (int j = 0; j < nbk; ++j) pacc += ((b.pw >> j) & 1u) ? xb[j] : 0.f;
-    const int row = (it - g * a.nrb) * 32 + lane;
-    a.rd.partial[(size_t)g * a.rd.Rpad + row] = fmaf(2.f, P0, fmaf(4.f, P1, fmaf(-8.f, P2, pacc)));
+    p[0] = fmaf(2.f, P0, fmaf(4.f, P1, fmaf(-8.f, P2, pacc)));
+  }
+  __device__ void finish(int tok, int row, float v) const {
+    const __half* xt = a.c.x + (size_t)tok * a.c.C;
+    for (uint32_t e = a.excptr[row]; e < a.excptr[row + 1]; ++e) v = fmaf(16.f, __half2float(xt[a.exccol[e]]), v);
+    v *= __half2float(a.scale[row]) * a.inv_sqrt8;
+    const int col0 = a.nblock * 24;
+    for (int j = 0; j < a.tail_n; ++j)
+      v = fmaf(__half2float(a.tail[(size_t)row * a.tailpad + j]), __half2float(xt[col0 + j]), v);
+    a.c.y[(size_t)tok * a.c.R + row] = __float2half_rn(v);
   }
 };
 
 template <int W, int AHEAD>
-__global__ void __launch_bounds__(W * 32, 1) k_leech_b1(LeechArgs a) {
-  int i0, i1;
-  cta_range(a.rd.nslice * a.nrb, i0, i1);
-  if (threadIdx.x == 0) {
-    prefetch_items(a.planes, Q2_ITEM_BYTES_LEECH, i0, i1);
-    prefetch_rows(a.parity, 2, a.nrb, a.rd.Rpad, i0, i1);
-  }
-  float* T = reinterpret_cast<float*>(q2_smem);
-  LeechF<W * 32> f{a, T, T + (kBuildBytes - 16) / 4, reinterpret_cast<float*>(q2_smem + kBuildBytes), 0};
-  run_items<W, AHEAD>(f, a.nrb, i0, i1);
+__global__ void __launch_bounds__(W * 32, kMinBlocks) k_leech_b1(LeechArgs a) {
+  if ((uint32_t)__cvta_generic_to_shared(q2_smem) + kTailFixed > kTabAddr) return;   // layout needs a low window base
+  LeechF<W * 32> f{a};
+  run_b1<W, AHEAD>(f, a.c, tail1());
 }
 
 // ------------------------------------------------------- no-weights control
-// Same grid, PDL, table build, per-lane lookups and reduction as k_bpdq_b1;
-// the "weight" words are derived from the lane and item index instead of
-// being loaded, so the kernel reads x and writes the workspace and y only.
+// Same grid, PDL, table build, per-lane lookups and in-launch reduction as
+// k_bpdq_b1; the "weight" words are derived from the lane and item index
+// instead of being loaded, so the kernel reads x and writes the workspace
+// and y only.
 template <int NT>
 struct NoWeightsF {
   struct Item {
     uint32_t h;
   };
+  static constexpr bool kStaged = true;
+  static constexpr int kGroup = 1;
+  static constexpr int kTok = 1;
   const BpdqArgs& a;
-  float* T;
-  float* gsum;
   __device__ void load(int it, int, int lane, Item& b) const { b.h = (uint32_t)it * 0x9E3779B9u ^ (lane * 0x85EBCA6Bu); }
-  float xs = 0.f;
-  __device__ void slice(int g) { build_table<NT>(a.x + (size_t)g * Q2_SLICE, Q2_SLICE, T, gsum); }
-  __device__ void ready() { xs = *gsum; }
-  __device__ void compute(int it, int g, int lane, const Item& b) {
-    const uint32_t h = b.h, lane4 = lane * 4u;
+  __device__ void stage_extra(int, int, unsigned char*) {}
+  __device__ void tables(int, const __half* xs, unsigned char* tail) const {
+    build_table<NT>(xs, tab1(), reinterpret_cast<float*>(tail + kTailGsum));
+  }
+  __device__ void compute(int, int, int lane, const Item& b, float (&p)[1]) const {
+    const uint32_t h = b.h, lane4 = (uint32_t)lane * 4u | kLane4Hi;
     const uint4 w0 = make_uint4(h, h ^ 0x5bd1e995u, h * 3u, h * 5u);
     const uint4 w1 = make_uint4(h * 7u, h ^ 0x27d4eb2fu, h * 11u, h * 13u);
     const float S0 = plane_sum(lane4, w0, w1);
     const float S1 = plane_sum(lane4, w1, w0);
-    const int row = (it - g * a.nrb) * 32 + lane;
-    a.rd.partial[(size_t)g * a.rd.Rpad + row] = fmaf(0.02f, S0, fmaf(0.01f, S1, 0.01f * xs));
+    const float xs = *reinterpret_cast<const float*>(q2_smem + kTailGsum);
+    p[0] = fmaf(0.02f, S0, fmaf(0.01f, S1, 0.01f * xs));
   }
+  __device__ void finish(int tok, int row, float v) const { a.c.y[(size_t)tok * a.c.R + row] = __float2half_rn(v); }
 };
 
 template <int W>
-__global__ void __launch_bounds__(W * 32, 1) k_noweights_b1(BpdqArgs a) {
-  int i0, i1;
-  cta_range(a.rd.nslice * a.nrb, i0, i1);
-  float* T = reinterpret_cast<float*>(q2_smem);
-  NoWeightsF<W * 32> f{a, T, T + (kBuildBytes - 16) / 4};
-  run_items<W, 1>(f, a.nrb, i0, i1);
+__global__ void __launch_bounds__(W * 32, kMinBlocks) k_noweights_b1(BpdqArgs a) {
+  if ((uint32_t)__cvta_generic_to_shared(q2_smem) + kTailFixed > kTabAddr) return;   // layout needs a low window base
+  NoWeightsF<W * 32> f{a};
+  run_b1<W, 1>(f, a.c, tail1());
 }
 
 // ------------------------------------------------- BPDQ, 2 to 6 tokens
@@ -314,17 +516,17 @@ __global__ void __launch_bounds__(W * 32, 1) k_noweights_b1(BpdqArgs a) {
 // positions each), so one byte permute still forms v*256 + b*8.  Each
 // lookup is then one 8-byte shared load and one packed fp32 add per token
 // pair; a half-warp's 16 lanes read 16 different column-bytes (conflict-free).
+// The CTA holds one slice's tables at a time (groups of one slice).
 constexpr int kMtMaxTok = 6;
 constexpr int kPairBytes = 256 * 32 * 8;                   // 64 KiB per token pair
 
 template <int NT, int NP>
-__device__ __forceinline__ void build_pairs(const __half* __restrict__ x, int ntok, int ldx, int col0, float* T,
-                                            float* gsum) {
+__device__ __forceinline__ void build_pairs(const __half* xs, int ntok, float* T, float* gsum) {
   for (int e = threadIdx.x; e < 512 * NP; e += NT) {
     const int p = e >> 9, h = (e >> 5) & 15, b = e & 31;
     float xa[8], xb[8];
     {
-      const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)(2 * p) * ldx + col0 + 8 * b);
+      const uint4 raw = *reinterpret_cast<const uint4*>(xs + (2 * p) * Q2_SLICE + 8 * b);
       const __half2* hv = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -334,7 +536,7 @@ __device__ __forceinline__ void build_pairs(const __half* __restrict__ x, int nt
       }
     }
     if (2 * p + 1 < ntok) {                            // an odd count leaves the last pair half empty
-      const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)(2 * p + 1) * ldx + col0 + 8 * b);
+      const uint4 raw = *reinterpret_cast<const uint4*>(xs + (2 * p + 1) * Q2_SLICE + 8 * b);
       const __half2* hv = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -386,11 +588,12 @@ struct BpdqMtF {
     uint32_t c01;
     unsigned short off;
   };
+  static constexpr bool kStaged = true;
+  static constexpr int kGroup = 1;
+  static constexpr int kTok = 2 * NP;
   const BpdqArgs& a;
-  float* T;
-  float* gsum;
+  unsigned char* tail;
   uint32_t rot[11];      // byte j of rot[k]: ((3k + j + lane) mod 32) * 8; byte 3 = 0
-  float xs[2 * NP];      // per-token sums of x over the slice
   __device__ void init(int lane) {
 #pragma unroll
     for (int k = 0; k < 11; ++k) {
@@ -401,19 +604,18 @@ struct BpdqMtF {
     }
   }
   __device__ void load(int it, int g, int lane, Item& b) const {
-    ld_item4(a.bits, it, lane, b.w);
-    const size_t r = (size_t)g * a.rd.Rpad + (size_t)(it - g * a.nrb) * 32 + lane;
+    ld_item(a.bits, Q2_ITEM_BYTES_BPDQ, it, lane, b.w, 4);
+    const size_t r = (size_t)g * a.c.Rpad + (size_t)(it - g * a.c.nrb) * 32 + lane;
     b.c01 = __ldg(reinterpret_cast<const unsigned int*>(a.c01) + r);
     b.off = __ldg(reinterpret_cast<const unsigned short*>(a.off) + r);
   }
-  __device__ void slice(int g) { build_pairs<NT, NP>(a.x, a.ntok, a.C, g * Q2_SLICE, T, gsum); }
-  __device__ void ready() {
-#pragma unroll
-    for (int t = 0; t < 2 * NP; ++t) xs[t] = gsum[t];
+  __device__ void stage_extra(int, int, unsigned char*) {}
+  __device__ void tables(int, const __half* xs, unsigned char* tl) const {
+    build_pairs<NT, NP>(xs, a.c.ntok, reinterpret_cast<float*>(q2_smem), reinterpret_cast<float*>(tl + kTailGsum));
   }
   __device__ void plane(const uint4& c0, const uint4& c1, float2 (&S)[NP]) const {
     const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    const char* base = reinterpret_cast<const char*>(T);
+    const char* base = reinterpret_cast<const char*>(q2_smem);
 #pragma unroll
     for (int P = 0; P < 32; ++P) {
       const uint32_t sel = (4u + (uint32_t)(P % 3)) | ((uint32_t)(P & 3) << 4) | 0x7700u;
@@ -422,82 +624,67 @@ struct BpdqMtF {
       for (int p = 0; p < NP; ++p) S[p] = __fadd2_rn(S[p], *reinterpret_cast<const float2*>(base + p * kPairBytes + ad));
     }
   }
-  __device__ void compute(int it, int g, int lane, const Item& b) {
+  __device__ void compute(int, int, int, const Item& b, float (&p)[2 * NP]) const {
     float2 S0[NP], S1[NP];
 #pragma unroll
-    for (int p = 0; p < NP; ++p) S0[p] = S1[p] = make_float2(0.f, 0.f);
+    for (int q = 0; q < NP; ++q) S0[q] = S1[q] = make_float2(0.f, 0.f);
     plane(b.w[0], b.w[1], S0);
     plane(b.w[2], b.w[3], S1);
-    const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&b.c01));
+    const float2 cf = __half22float2(*reinterpret_cast<const __half2*>(&b.c01));
     const float of = __half2float(__ushort_as_half(b.off));
-    const int row = (it - g * a.nrb) * 32 + lane;
-    float* out = a.rd.partial + (size_t)g * a.rd.Rpad + row;
-    const size_t tstride = (size_t)a.rd.nslice * a.rd.Rpad;
+    const float* xs = reinterpret_cast<const float*>(tail + kTailGsum);
 #pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      out[(2 * p) * tstride] = fmaf(c.x, S0[p].x, fmaf(c.y, S1[p].x, of * xs[2 * p]));
-      if (2 * p + 1 < a.ntok) out[(2 * p + 1) * tstride] = fmaf(c.x, S0[p].y, fmaf(c.y, S1[p].y, of * xs[2 * p + 1]));
+    for (int q = 0; q < NP; ++q) {
+      p[2 * q] = fmaf(cf.x, S0[q].x, fmaf(cf.y, S1[q].x, of * xs[2 * q]));
+      p[2 * q + 1] = fmaf(cf.x, S0[q].y, fmaf(cf.y, S1[q].y, of * xs[2 * q + 1]));
     }
   }
+  __device__ void finish(int tok, int row, float v) const { a.c.y[(size_t)tok * a.c.R + row] = __float2half_rn(v); }
 };
 
 template <int W, int AHEAD, int NP>
-__global__ void __launch_bounds__(W * 32, 1) k_bpdq_mt(BpdqArgs a) {
-  int i0, i1;
-  cta_range(a.rd.nslice * a.nrb, i0, i1);
-  if (threadIdx.x == 0) {
-    prefetch_items(a.bits, Q2_ITEM_BYTES_BPDQ, i0, i1);
-    prefetch_rows(a.c01, 4, a.nrb, a.rd.Rpad, i0, i1);
-    prefetch_rows(a.off, 2, a.nrb, a.rd.Rpad, i0, i1);
-  }
-  float* T = reinterpret_cast<float*>(q2_smem);
-  BpdqMtF<W * 32, NP> f{a, T, reinterpret_cast<float*>(q2_smem + NP * kPairBytes)};
+__global__ void __launch_bounds__(W * 32, NP == 1 ? kMinBlocks : 1) k_bpdq_mt(BpdqArgs a) {
+  unsigned char* tail = q2_smem + (size_t)NP * kPairBytes;
+  BpdqMtF<W * 32, NP> f{a, tail};
   f.init(threadIdx.x & 31);
-  run_items<W, AHEAD>(f, a.nrb, i0, i1);
+  run_b1<W, AHEAD>(f, a.c, tail);
 }
 
 // ---------------------------------------------------------------- trellis
 // Lane = row, item = (segment, 32 rows).  The 16 KiB table and all of x sit
-// in shared memory for the whole kernel.  Step k of a segment reads the
-// 16-bit state at bit offset 4*(127 - k) of the lane's 512-bit packet (a
-// funnel shift of two words), hashes it, loads one fp16 pair, flips both
-// signs by state bit 0 and accumulates two fp32 FMAs.
+// in shared memory for the whole kernel (one group spanning every segment).
+// Step k of a segment reads the 16-bit state at bit offset 4*(127 - k) of
+// the lane's 512-bit packet (a funnel shift of two words), hashes it, loads
+// one fp16 pair, flips both signs by state bit 0 and accumulates two fp32
+// FMAs.  The epilogue multiplies by the row scale.
 struct TrellisArgs {
+  B1 c;
   const unsigned char* stream;
   const uint32_t* table;     // 4096 half2
   const __half* scale;
-  const __half* x;
-  __half* y;
-  Reduce rd;
-  int R, C, nrb;
 };
 
 constexpr uint32_t kHashHi = 0x9E37u << 16;   // (s*0x9E37 mod 2^16) lands in bits 16..31
+constexpr int kTrlTail = 4096 * 4;           // x (C/2 words) follows the table; then the tail
 
-__device__ __forceinline__ void ld_trl(const unsigned char* base, int it, int lane, uint4 (&w)[4]) {
-  const unsigned char* p = base + (size_t)it * Q2_ITEM_BYTES_TRL + lane * 16;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) w[k] = ldg_stream(p + k * 512);
-}
-
-// Items of every segment in one pass: x and the table stay in shared memory
-// for the whole kernel, so the "slice" step of run_items only copies x.
 template <int NT>
 struct TrellisF {
   struct Item {
     uint4 w[4];
   };
+  static constexpr bool kStaged = false;
+  static constexpr int kGroup = 1 << 30;   // one group: x and the table stay for every segment
+  static constexpr int kTok = 1;
   const TrellisArgs& a;
   const uint32_t* tab;
   uint32_t* xs;
-  __device__ void load(int it, int, int lane, Item& b) const { ld_trl(a.stream, it, lane, b.w); }
-  __device__ void slice(int) {
-    const uint32_t* xg = reinterpret_cast<const uint32_t*>(a.x);
-    for (int i = threadIdx.x; i < a.C / 2; i += NT) xs[i] = xg[i];
+  __device__ void load(int it, int, int lane, Item& b) const { ld_item(a.stream, Q2_ITEM_BYTES_TRL, it, lane, b.w, 4); }
+  __device__ void stage_extra(int, int, unsigned char*) {}
+  __device__ void tables(int, const __half*, unsigned char*) const {
+    const uint32_t* xg = reinterpret_cast<const uint32_t*>(a.c.x);
+    for (int i = threadIdx.x; i < a.c.C / 2; i += NT) xs[i] = xg[i];
   }
-  __device__ void ready() {}
-  __device__ void compute(int it, int, int lane, const Item& b) {
-    const int sg = it / a.nrb, rb = it - sg * a.nrb;
+  __device__ void compute(int, int sg, int, const Item& b, float (&p)[1]) const {
     const uint32_t W[16] = {b.w[0].x, b.w[0].y, b.w[0].z, b.w[0].w, b.w[1].x, b.w[1].y, b.w[1].z, b.w[1].w,
                             b.w[2].x, b.w[2].y, b.w[2].z, b.w[2].w, b.w[3].x, b.w[3].y, b.w[3].z, b.w[3].w};
     const uint4* xv = reinterpret_cast<const uint4*>(xs + sg * 128);
@@ -523,46 +710,76 @@ struct TrellisF {
         }
       }
     }
-    a.rd.partial[(size_t)sg * a.rd.Rpad + rb * 32 + lane] = acc0 + acc1;
+    p[0] = acc0 + acc1;
+  }
+  __device__ void finish(int tok, int row, float v) const {
+    a.c.y[(size_t)tok * a.c.R + row] = __float2half_rn(v * __half2float(a.scale[row]));
   }
 };
 
-constexpr int kTrellisWarps = 16, kTrellisAhead = 1;
+constexpr int kTrellisAhead = 1;
 
 template <int W, int AHEAD>
-__global__ void __launch_bounds__(W * 32, 1) k_trellis_b1(TrellisArgs a) {
+__global__ void __launch_bounds__(W * 32, kMinBlocks) k_trellis_b1(TrellisArgs a) {
   uint32_t* tab = reinterpret_cast<uint32_t*>(q2_smem);                 // 16 KiB
-  uint32_t* xs = reinterpret_cast<uint32_t*>(q2_smem + 4096 * 4);      // x as half2, C/2 words
-  int i0, i1;
-  cta_range(a.rd.nslice * a.nrb, i0, i1);
-  if (threadIdx.x == 0) prefetch_items(a.stream, Q2_ITEM_BYTES_TRL, i0, i1);
+  uint32_t* xs = reinterpret_cast<uint32_t*>(q2_smem + kTrlTail);       // x as half2, C/2 words
   for (int i = threadIdx.x; i < 4096; i += W * 32) tab[i] = a.table[i];
   TrellisF<W * 32> f{a, tab, xs};
-  run_items<W, AHEAD>(f, 1 << 30, i0, i1);         // one pass over all segments
+  unsigned char* tail = q2_smem + kTrlTail + ((a.c.C * 2 + 15) / 16) * 16;
+  run_b1<W, AHEAD>(f, a.c, tail);                  // one group over all segments
 }
 
-// Batch-1 kernels ask for more than half of an SM's shared memory, so an SM
-// never holds two CTAs of them.  Under programmatic dependent launch the
-// next GEMV's CTAs are placed while the current GEMV drains; an SM whose
-// CTA has already left could otherwise take two CTAs of the same grid (and
-// another SM none), and those two would set the GEMV's end.
+// ------------------------------------------------------------ host side
+// The 8-warp kernels ask for more than a third of an SM's shared memory, so
+// an SM holds at most two of their CTAs: while a GEMV runs, every SM holds
+// one of its CTAs and has room for exactly one CTA of the next GEMV, which
+// therefore spreads one per SM.  The kernels for 3..6 tokens (two or three
+// token-pair tables) need more than half and run one per SM, with the whole
+// register file.
 constexpr int kOneCtaSmem = 116 * 1024;
-static_assert(kBuildBytes + 64 <= kOneCtaSmem, "batch-1 tables fit the one-CTA footprint");
+constexpr int kTwoCtaSmem = kMinBlocks == 2 ? 80 * 1024 : kOneCtaSmem;
+
+struct Geo {
+  int grid;      // CTAs
+};
+
+Geo geometry(const q2_blob_header& d) {
+  const int items = d.nslice * q2_nrb(d);
+  Geo g;
+  g.grid = std::max(1, std::min(items, dev_info().sms));
+  return g;
+}
+
+// The accumulator words hold at most Q2_MAX_SPLIT slices per row, and the
+// workspace at most Q2_MAX_ROWS rows per token.
+bool b1_shape_ok(const q2_blob_header& d) { return d.nslice >= 1 && d.nslice <= Q2_MAX_SPLIT && d.Rpad <= Q2_MAX_ROWS; }
+
+B1 make_b1(const q2_handle* h, const void* x, void* y, int ntok) {
+  const q2_blob_header& d = h->hdr;
+  B1 c;
+  c.x = static_cast<const __half*>(x);
+  c.y = static_cast<__half*>(y);
+  c.acc = static_cast<unsigned long long*>(h->ws);
+  // fixed-point scale 2^F with |partial| * 2^F < 2^46 for every fp16 x
+  int e = 0;
+  if (h->pbound > 0.0) std::frexp(h->pbound, &e);    // pbound < 2^e
+  const int F = std::max(-100, std::min(100, 46 - e));
+  c.fscale = std::ldexp(1.0f, F);
+  c.finv = std::ldexp(1.0f, -F);
+  c.R = d.R;
+  c.C = d.C;
+  c.Rpad = d.Rpad;
+  c.nrb = q2_nrb(d);
+  c.nslice = d.nslice;
+  c.ntok = ntok;
+  return c;
+}
 
 template <typename A>
-int launch(const q2_handle* h, void (*kernel)(A), const A& args, int smem, int items, const void* x, void* y,
-           void* stream, int threads, int ntok = 1) {
-  const int grid = max(1, min(items, dev_info().sms));
-  const int st = launch_pdl(kernel, args, grid, threads, smem, stream);
-  return st ? st : q2_launch_reduce(h, x, y, ntok, stream);
-}
-
-Reduce make_reduce(const q2_handle* h) {
-  Reduce r;
-  r.partial = static_cast<float*>(h->ws);
-  r.nslice = h->hdr.nslice;
-  r.Rpad = h->hdr.Rpad;
-  return r;
+int launch1(void (*kernel)(A), const A& args, const Geo& g, int threads, int table_bytes, void* stream,
+            int min_smem = kTwoCtaSmem) {
+  const int smem = std::max(min_smem, table_bytes + kTailFixed);
+  return launch_pdl(kernel, args, g.grid, threads, smem, stream);
 }
 
 }  // namespace
@@ -572,99 +789,70 @@ using namespace q2;
 
 extern "C" int q2_b1_bpdq(const q2_handle* h, const void* x, void* y, void* stream) {
   const q2_blob_header& d = h->hdr;
+  if (!b1_shape_ok(d)) return Q2_ESHAPE;
   BpdqArgs a;
+  a.c = make_b1(h, x, y, 1);
   a.bits = h->dev + d.off[SEC_BPDQ_BITS];
   a.c01 = reinterpret_cast<const __half2*>(h->dev + d.off[SEC_BPDQ_C01]);
   a.off = reinterpret_cast<const __half*>(h->dev + d.off[SEC_BPDQ_OFF]);
-  a.x = static_cast<const __half*>(x);
-  a.y = static_cast<__half*>(y);
-  a.rd = make_reduce(h);
-  a.R = d.R;
-  a.C = d.C;
-  a.nrb = q2_nrb(d);
-  a.ntok = 1;
-  return launch(h, k_bpdq_b1<kBpdqWarps, kBpdqAhead>, a, kOneCtaSmem, d.nslice * a.nrb, x, y, stream,
-                kBpdqWarps * 32);
+  return launch1(k_bpdq_b1<kWarps, kBpdqAhead>, a, geometry(d), kWarps * 32, kTabSmem, stream);
 }
 
 // BPDQ at 2..6 tokens on CUDA cores (x is [ntok][C]; partials [ntok][nslice][Rpad]).
 extern "C" int q2_mt_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
   const q2_blob_header& d = h->hdr;
+  if (ntok < 2 || ntok > kMtMaxTok) return Q2_ENTOK;
+  if (!b1_shape_ok(d)) return Q2_ESHAPE;
   BpdqArgs a;
+  a.c = make_b1(h, x, y, ntok);
   a.bits = h->dev + d.off[SEC_BPDQ_BITS];
   a.c01 = reinterpret_cast<const __half2*>(h->dev + d.off[SEC_BPDQ_C01]);
   a.off = reinterpret_cast<const __half*>(h->dev + d.off[SEC_BPDQ_OFF]);
-  a.x = static_cast<const __half*>(x);
-  a.y = static_cast<__half*>(y);
-  a.rd = make_reduce(h);
-  a.R = d.R;
-  a.C = d.C;
-  a.nrb = q2_nrb(d);
-  a.ntok = ntok;
-  if (ntok < 2 || ntok > kMtMaxTok) return Q2_ENTOK;
-  const int items = d.nslice * a.nrb;
-  constexpr int W = 16;
   const int np = (ntok + 1) / 2;
-  const int smem = std::max(kOneCtaSmem, np * kPairBytes + 64);
+  const Geo g = geometry(d);
   switch (np) {
-    case 1: return launch(h, k_bpdq_mt<W, 2, 1>, a, smem, items, x, y, stream, W * 32, ntok);
-    case 2: return launch(h, k_bpdq_mt<W, 1, 2>, a, smem, items, x, y, stream, W * 32, ntok);
-    case 3: return launch(h, k_bpdq_mt<W, 1, 3>, a, smem, items, x, y, stream, W * 32, ntok);
+    case 1: return launch1(k_bpdq_mt<kWarps, 2, 1>, a, g, kWarps * 32, 1 * kPairBytes, stream);
+    case 2: return launch1(k_bpdq_mt<8, 1, 2>, a, g, 8 * 32, 2 * kPairBytes, stream, kOneCtaSmem);
+    case 3: return launch1(k_bpdq_mt<8, 1, 3>, a, g, 8 * 32, 3 * kPairBytes, stream, kOneCtaSmem);
     default: return Q2_ENTOK;
   }
 }
 
 extern "C" int q2_b1_noweights(const q2_handle* h, const void* x, void* y, void* stream) {
-  const q2_blob_header& d = h->hdr;
+  if (!b1_shape_ok(h->hdr)) return Q2_ESHAPE;
   BpdqArgs a = {};
-  a.x = static_cast<const __half*>(x);
-  a.y = static_cast<__half*>(y);
-  a.rd = make_reduce(h);
-  a.R = d.R;
-  a.C = d.C;
-  a.nrb = q2_nrb(d);
-  a.ntok = 1;
-  return launch(h, k_noweights_b1<kBpdqWarps>, a, kOneCtaSmem, d.nslice * a.nrb, x, y, stream, kBpdqWarps * 32);
+  a.c = make_b1(h, x, y, 1);
+  return launch1(k_noweights_b1<kWarps>, a, geometry(h->hdr), kWarps * 32, kTabSmem, stream);
 }
 
 extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* stream) {
   const q2_blob_header& d = h->hdr;
+  if (!b1_shape_ok(d)) return Q2_ESHAPE;
   LeechArgs a;
+  a.c = make_b1(h, x, y, 1);
   a.planes = h->dev + d.off[SEC_LEECH_PLANES];
   a.parity = reinterpret_cast<const uint16_t*>(h->dev + d.off[SEC_LEECH_PARITY]);
   a.scale = reinterpret_cast<const __half*>(h->dev + d.off[SEC_LEECH_SCALE]);
   a.tail = reinterpret_cast<const __half*>(h->dev + d.off[SEC_LEECH_TAIL]);
   a.excptr = reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_LEECH_EXCPTR]);
   a.exccol = reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_LEECH_EXCCOL]);
-  a.x = static_cast<const __half*>(x);
-  a.y = static_cast<__half*>(y);
-  a.rd = make_reduce(h);
-  a.R = d.R;
-  a.C = d.C;
-  a.nrb = q2_nrb(d);
   a.nblock = d.nblock;
   a.tail_n = d.tail;
   a.tailpad = d.tailpad;
   a.inv_sqrt8 = d.inv_sqrt8;
-  return launch(h, k_leech_b1<kLeechWarps, kLeechAhead>, a, kOneCtaSmem, d.nslice * a.nrb, x, y, stream,
-                kLeechWarps * 32);
+  return launch1(k_leech_b1<kWarps, kLeechAhead>, a, geometry(d), kWarps * 32, kTabSmem, stream);
 }
 
 extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* stream) {
   const q2_blob_header& d = h->hdr;
+  if (!b1_shape_ok(d)) return Q2_ESHAPE;
   TrellisArgs a;
+  a.c = make_b1(h, x, y, 1);
   a.stream = h->dev + d.off[SEC_TRL_STREAM];
   a.table = reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_TRL_TABLE]);
   a.scale = reinterpret_cast<const __half*>(h->dev + d.off[SEC_TRL_SCALE]);
-  a.x = static_cast<const __half*>(x);
-  a.y = static_cast<__half*>(y);
-  a.rd = make_reduce(h);
-  a.R = d.R;
-  a.C = d.C;
-  a.nrb = q2_nrb(d);
-  const int smem = std::max(4096 * 4 + d.C * 2, kOneCtaSmem);
-  return launch(h, k_trellis_b1<kTrellisWarps, kTrellisAhead>, a, smem, d.nslice * a.nrb, x, y, stream,
-                kTrellisWarps * 32);
+  return launch1(k_trellis_b1<kWarps, kTrellisAhead>, a, geometry(d), kWarps * 32,
+                 kTrlTail + (d.C * 2 + 15) / 16 * 16, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -675,15 +863,18 @@ extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* s
 // is not permitted there), plugins whose host framework owns all device
 // memory and offers them no allocator, and real-time decode loops that must
 // not touch the allocator after start-up.  q2_gemv_bpdq_noalloc serves them:
-// the split-K partial sums that q2_gemv keeps in a caller-bound workspace go
-// to a scratch array that belongs to this library instead, so the caller
-// passes only the handle, x, y and a stream.  Every GPU that loads the
-// library holds the array (Q2_NOALLOC_SCRATCH_BYTES) until the process exits.
+// the split-K accumulator words that q2_gemv keeps in a caller-bound
+// workspace go to a scratch array that belongs to this library instead, so
+// the caller passes only the handle, x, y and a stream.  Every
+// GPU that loads the library holds the array (Q2_NOALLOC_SCRATCH_BYTES)
+// until the process exits.
 
 namespace {
 
-// Device memory for the partial sums; host code must never hand this symbol
-// to a kernel (on the host it only stands in for the device address).
+// Device memory for the accumulator words; host code must never hand this
+// symbol to a kernel (on the host it only stands in for the device
+// address).  Zero-initialised when the module loads; every completed call
+// leaves the words it used at zero again.
 static __device__ __align__(256) unsigned char q2_noalloc_scratch[Q2_NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_noalloc_mu;
@@ -717,13 +908,13 @@ extern "C" int q2_gemv_bpdq_noalloc(const q2_handle* h, const void* x, void* y, 
   if (!h || !x || !y) return Q2_EINVAL;
   if (h->hdr.fmt != Q2_BPDQ) return Q2_EFMT;
   if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(y) % 16) return Q2_EALIGN;
-  const size_t need = (size_t)h->hdr.nslice * h->hdr.Rpad * 4;
+  const size_t need = (size_t)h->hdr.Rpad * 8;           // one accumulator word per row
   if (need > (size_t)Q2_NOALLOC_SCRATCH_BYTES) return Q2_ESCRATCH;
   void* scratch = nullptr;
   const int st = noalloc_scratch(&scratch);
   if (st) return st;
-  // the same two launches as q2_gemv at ntok = 1, with the scratch in place
-  // of the caller's workspace; nothing in the scratch needs to start at zero
+  // the same launch as q2_gemv at ntok = 1, with the scratch in place of the
+  // caller's workspace
   q2_handle view = *h;
   view.ws = scratch;
   view.ws_bytes = Q2_NOALLOC_SCRATCH_BYTES;

@@ -334,6 +334,36 @@ int q2_pack_noweights(int R, int C, void* out, size_t* out_bytes) {
   return finish(b, out, out_bytes, &fill);
 }
 
+// Bound on |one slice's partial sum| over any fp16 x (|x| <= 65504), from
+// the largest per-weight magnitude of the matrix: 256 columns x 65504 x
+// max |w| (before the row scale, which the epilogue applies).
+static double partial_bound(const unsigned char* blob, const q2_blob_header& d) {
+  double k = 0.0;
+  switch (d.fmt) {
+    case Q2_BPDQ: {
+      const uint16_t* c01 = reinterpret_cast<const uint16_t*>(blob + d.off[SEC_BPDQ_C01]);
+      const uint16_t* off = reinterpret_cast<const uint16_t*>(blob + d.off[SEC_BPDQ_OFF]);
+      const size_t n = (size_t)d.nslice * d.Rpad;
+      for (size_t i = 0; i < n; ++i) {
+        const double v = std::fabs(half_to_double(c01[2 * i])) + std::fabs(half_to_double(c01[2 * i + 1])) +
+                         std::fabs(half_to_double(off[i]));
+        if (v > k) k = v;
+      }
+      break;
+    }
+    case Q2_TRELLIS: {
+      const uint16_t* t = reinterpret_cast<const uint16_t*>(blob + d.off[SEC_TRL_TABLE]);
+      for (int i = 0; i < 4096 * 2; ++i) k = std::fmax(k, std::fabs(half_to_double(t[i])));
+      break;
+    }
+    case Q2_LEECH: k = 8.0; break;          // |v| <= 8 per coordinate
+    case Q2_NOWEIGHTS: k = 0.04; break;     // the control's synthetic coefficients
+    default: k = 0.0;
+  }
+  if (!(k < 1e30)) k = 1e30;                // inf / nan coefficients: keep the scale finite
+  return k * 256.0 * 65504.0;
+}
+
 int q2_bind(const void* blob_host, const void* blob_dev, q2_handle** h) {
   if (!blob_host || !blob_dev || !h) return Q2_EINVAL;
   if (reinterpret_cast<uintptr_t>(blob_dev) % kAlign) return Q2_EALIGN;
@@ -351,6 +381,7 @@ int q2_bind(const void* blob_host, const void* blob_dev, q2_handle** h) {
   p->dev = static_cast<const unsigned char*>(blob_dev);
   p->ws = nullptr;
   p->ws_bytes = 0;
+  p->pbound = partial_bound(static_cast<const unsigned char*>(blob_host), hdr);
   *h = p;
   return Q2_OK;
 }
@@ -364,7 +395,12 @@ int q2_workspace_bytes(const q2_handle* h, int ntok, size_t* bytes) {
     *bytes = 0;
     return Q2_OK;
   }
-  *bytes = (size_t)h->hdr.nslice * ntok * h->hdr.Rpad * 4;
+  const int fmt = h->hdr.fmt;
+  const bool cuda_core = ntok == 1 || (fmt == Q2_BPDQ && ntok <= Q2_MAX_ACC_TOK);
+  if (cuda_core)
+    *bytes = (size_t)ntok * h->hdr.Rpad * 8;                 // accumulators
+  else
+    *bytes = Q2_WS_PARTIAL_OFFSET + (size_t)h->hdr.nslice * ntok * h->hdr.Rpad * 4;
   return Q2_OK;
 }
 
@@ -434,6 +470,7 @@ int q2_gemv(q2_fmt fmt, const q2_handle* h, const void* x, void* y, int ntok, q2
   int st = q2_workspace_bytes(h, ntok, &need);
   if (st) return st;
   if (need && (!h->ws || h->ws_bytes < need)) return Q2_EWORKSPACE;
+  if (h->hdr.Rpad > Q2_MAX_ROWS || h->hdr.nslice > Q2_MAX_SPLIT) return Q2_ESHAPE;
   void* s = static_cast<void*>(stream);
   switch (h->hdr.fmt) {
     case Q2_FP16: return q2_launch_fp16(h, x, y, ntok, s);

@@ -8,11 +8,11 @@ struct q2_handle {
   const unsigned char* dev;  // device copy of the blob (caller-owned)
   void* ws;                  // split-K workspace (caller-owned), may be null
   size_t ws_bytes;
+  double pbound;             // |partial of one 256-column slice| <= pbound for any fp16 x
 };
 
 static inline int q2_nrb(const q2_blob_header& h) { return h.Rpad / Q2_ROWS; }
 
-// Workspace layout: fp32 partials [ntok][nslice][Rpad].
 
 #ifdef __cplusplus
 extern "C" {

@@ -12,6 +12,17 @@
 #define Q2_ITEM_BYTES_LEECH 3072  // 32 lanes x (3 planes x 32 bytes)
 #define Q2_MAX_SECTIONS 8
 
+// Workspace layout.  The CUDA-core paths (1..6 tokens) keep one 64-bit
+// accumulator per (token, row) at offset 0: [ntok][Rpad] words, zero between
+// calls (see q2_b1.cu).  The tensor-core path keeps fp32 partial sums
+// [ntok][nsplit][Rpad] at offset Q2_WS_PARTIAL_OFFSET, which lies past the
+// largest accumulator region any handle can have, so one workspace can
+// serve every handle without a partial sum ever landing on an accumulator.
+#define Q2_MAX_ROWS 524288
+#define Q2_MAX_ACC_TOK 6
+#define Q2_WS_PARTIAL_OFFSET ((size_t)Q2_MAX_ACC_TOK * Q2_MAX_ROWS * 8)
+#define Q2_MAX_SPLIT 255          // count field of the accumulator word
+
 // Section indices per format.
 enum { SEC_FP16_W = 0 };
 enum { SEC_BPDQ_BITS = 0, SEC_BPDQ_C01 = 1, SEC_BPDQ_OFF = 2, SEC_BPDQ_VTAB = 3 };

@@ -1,6 +1,7 @@
-// Split-K reduction and epilogue: y[t][r] = epilogue(sum over slices s, in
-// order, of partial[t][s][r]).  Runs as the second launch of a GEMV, chained
-// to the main kernel by programmatic dependent launch: its CTAs may start
+// Split-K reduction and epilogue of the tensor-core path: y[t][r] =
+// epilogue(sum over K splits s, in order, of partial[t][s][r]).  Runs as the
+// second launch of a GEMV, chained to the main kernel by programmatic
+// dependent launch: its CTAs may start
 // while the main kernel drains and wait (griddepcontrol.wait) until every
 // partial is visible.  One thread per output, consecutive threads on
 // consecutive rows, so every slice's partials are read as coalesced lines.
@@ -75,7 +76,7 @@ using namespace q2;
 extern "C" int q2_launch_reduce_n(const q2_handle* h, const void* x, void* y, int ntok, int nsplit, void* stream) {
   const q2_blob_header& d = h->hdr;
   RedArgs a = {};
-  a.partial = static_cast<const float*>(h->ws);
+  a.partial = reinterpret_cast<const float*>(static_cast<const unsigned char*>(h->ws) + Q2_WS_PARTIAL_OFFSET);
   a.nslice = nsplit;
   a.Rpad = d.Rpad;
   a.R = d.R;
@@ -102,7 +103,3 @@ extern "C" int q2_launch_reduce_n(const q2_handle* h, const void* x, void* y, in
   return launch_pdl(k_reduce, a, max(grid, 1), kThreads, 0, stream);
 }
 
-// Second launch of every batch-1 GEMV, whose partials are one per 256-column slice.
-extern "C" int q2_launch_reduce(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
-  return q2_launch_reduce_n(h, x, y, ntok, h->hdr.nslice, stream);
-}

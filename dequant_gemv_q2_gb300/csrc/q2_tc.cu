@@ -465,7 +465,7 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
   }
   a.x = static_cast<const __half*>(x);
   a.y = static_cast<__half*>(y);
-  a.partial = static_cast<float*>(h->ws);
+  a.partial = reinterpret_cast<float*>(static_cast<unsigned char*>(h->ws) + Q2_WS_PARTIAL_OFFSET);
   a.R = d.R;
   a.C = d.C;
   a.Rpad = d.Rpad;

@@ -119,10 +119,19 @@ int q2_pack_noweights(int R, int C, void* out, size_t* out_bytes);
 int q2_bind(const void* blob_host, const void* blob_dev, q2_handle** h);
 void q2_unbind(q2_handle* h);
 
-/* Split-K workspace: device memory owned by the caller (fp32 partial sums,
- * nslice x ntok x Rpad floats; no initial contents needed).  One workspace
- * may serve many handles whose calls are ordered on one stream; calls that
- * overlap on the GPU must use different workspaces. */
+/* Split-K workspace: device memory owned by the caller, 256-byte aligned.
+ * The CUDA-core paths (BPDQ at 1..6 tokens, trellis and Leech at 1 token)
+ * use its first ntok x Rpad 64-bit words as split-K accumulators: each
+ * 256-column slice's partial sum of a row is added as a fixed-point integer
+ * together with an arrival count, in one atomic, and the addition that
+ * completes the count writes y and resets the word.  These words must be
+ * zero when the workspace is first used (allocate it zero-filled); every
+ * completed call leaves them at zero again.  The tensor-core path keeps
+ * fp32 partial sums (nslice x ntok x Rpad floats) at byte offset
+ * 6 x 524288 x 8 (24 MiB), past any handle's accumulators, so one
+ * workspace may serve many handles whose calls are ordered on one stream;
+ * calls that overlap on the GPU must use different workspaces.  Limits:
+ * R <= 524288 rows; on the CUDA-core paths C <= 255 x 256 columns. */
 int q2_workspace_bytes(const q2_handle* h, int ntok, size_t* bytes);
 int q2_set_workspace(q2_handle* h, void* ws_dev, size_t ws_bytes);
 
@@ -136,9 +145,18 @@ int q2_bytes(const q2_handle* h, int ntok, size_t* weight_bytes_read_per_call);
  * [ntok][C]; y: device fp16 [ntok][R]; both 16-byte aligned; 1 <= ntok <= 64.
  * Asynchronous and ordered on `stream`; never synchronises.  Needs the
  * workspace of q2_workspace_bytes(h, ntok) bound first (0 bytes for fp16).
- * The packed formats run as two launches (partial sums, then an in-order
- * reduction with the epilogue), chained by programmatic dependent launch.
- * Returns Q2_ECUDA if a launch fails. */
+ * The packed formats at 1..6 tokens (BPDQ) or 1 token (trellis, Leech) run
+ * as one launch that reduces its split-K partial sums itself, through the
+ * workspace's fixed-point accumulator words (integer sums: the result does
+ * not depend on the order in which slices arrive); the tensor-core path
+ * (7..64 tokens, or 2..64 for trellis and Leech) adds a second, in-order
+ * reduction launch.  The fixed-point scale 2^F is chosen per matrix from its
+ * largest weight magnitude so that no fp16 x can overflow it; each slice's
+ * partial then carries an absolute rounding error of at most 2^-(F+1),
+ * about 1e-8 for weights of magnitude 0.05.  Launches use programmatic dependent launch: weights are
+ * fetched before the previous kernel on the stream has finished; x, y and
+ * the workspace are touched only after it has.  Returns Q2_ECUDA if a
+ * launch fails. */
 int q2_gemv(q2_fmt fmt, const q2_handle* h, const void* x, void* y, int ntok, q2_stream stream);
 
 /* Allocation-free y = W x for a BPDQ handle at one token (no counterpart on
@@ -146,14 +164,15 @@ int q2_gemv(q2_fmt fmt, const q2_handle* h, const void* x, void* y, int ntok, q2
  * allocate device memory when they run the GEMV: code running under CUDA
  * stream capture, plugins whose host framework owns the device memory, and
  * real-time loops that must not call the allocator.  It does what q2_gemv
- * does at ntok == 1, but keeps the split-K partial sums in a scratch array
+ * does at ntok == 1, but keeps the split-K accumulator words in a scratch
+ * array
  * that the library owns (a file-scope __device__ array of
- * Q2_NOALLOC_SCRATCH_BYTES = 4 MiB, held on every GPU that loads the
+ * Q2_NOALLOC_SCRATCH_BYTES = 1 MiB, held on every GPU that loads the
  * library until the process exits) instead of a workspace bound with
  * q2_set_workspace.  It calls no cudaMalloc or cudaFree.
  *   - x: device fp16 [C]; y: device fp16 [R]; both 16-byte aligned.
- *   - Needs nslice * Rpad * 4 bytes of scratch (C/256 groups x R rounded up
- *     to 32 rows); larger problems return Q2_ESCRATCH.  Every Qwen3-8B and
+ *   - Needs Rpad * 8 bytes (one word per row, R rounded up to 32), so R up
+ *     to 131072; larger problems return Q2_ESCRATCH.  Every Qwen3-8B and
  *     -14B linear fits.
  *   - The first call on a device looks up the scratch's device address
  *     (cudaGetSymbolAddress, once per device); make that first call before
@@ -161,9 +180,9 @@ int q2_gemv(q2_fmt fmt, const q2_handle* h, const void* x, void* y, int ntok, q2
  *   - All calls in a process share the one scratch array of a GPU: two
  *     calls that can run at the same time on that GPU (streams with no
  *     ordering between them) race and corrupt each other's results, so
- *     order them on one stream.  Nothing in the scratch needs to start at
- *     zero; it keeps the last call's partial sums. */
-#define Q2_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)
+ *     order them on one stream.  The words are zero when the library loads
+ *     and every completed call leaves them at zero. */
+#define Q2_NOALLOC_SCRATCH_BYTES (1024 * 1024)
 int q2_gemv_bpdq_noalloc(const q2_handle* h, const void* x, void* y, q2_stream stream);
 
 /* Debug decode to the canonical form (all formats but Q2_NOWEIGHTS):

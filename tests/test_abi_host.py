@@ -134,7 +134,12 @@ def test_status_codes(q2):
     assert L.q2_bind(blob.ctypes.data, ctypes.c_void_p((1 << 20) + 16), ctypes.byref(h)) == -3
     assert L.q2_bind(blob.ctypes.data, fake_dev, ctypes.byref(h)) == 0
     ws = ctypes.c_size_t(0)
-    assert L.q2_workspace_bytes(h, 1, ctypes.byref(ws)) == 0 and ws.value > 0
+    assert L.q2_workspace_bytes(h, 1, ctypes.byref(ws)) == 0
+    assert ws.value == 1 * 32 * 8                             # one 64-bit accumulator word per (token, row)
+    assert L.q2_workspace_bytes(h, 3, ctypes.byref(ws)) == 0 and ws.value == 3 * 32 * 8
+    # tensor-core path: fp32 partials [ntok][nslice][Rpad] after the 24 MiB accumulator reserve
+    assert L.q2_workspace_bytes(h, 7, ctypes.byref(ws)) == 0 and ws.value == 6 * 524288 * 8 + 7 * 1 * 32 * 4
+
     assert L.q2_workspace_bytes(h, 65, ctypes.byref(ws)) == -5
     x = ctypes.c_void_p(1 << 21)
     assert L.q2_gemv(2, h, x, x, 1, None) == -4                              # fmt mismatch

@@ -3,7 +3,7 @@
 It exists for callers that cannot allocate device memory when they run the
 GEMV (code under CUDA stream capture, plugins whose host framework owns the
 device memory, real-time loops that must not call the allocator): the split-K
-partial sums live in a scratch array owned by the library instead of a
+accumulator words live in a scratch array owned by the library instead of a
 caller-bound workspace.  This test calls it through the C ABI twice in a row,
 on different activations, and checks each result against q2_gemv (the entry
 point with a workspace) within the tolerance the parity tests use,
@@ -61,8 +61,8 @@ def test_noalloc_matches_workspace_entry_point(q2, R, C, seed):
 
 
 def test_noalloc_refuses_problems_larger_than_the_scratch(q2):
-    # 52 groups x 20480 rows x 4 bytes = 4.26 MB > Q2_NOALLOC_SCRATCH_BYTES (4 MiB)
-    R, C = 20480, 52 * 256
+    # 131104 rows x 8 bytes = 1,048,832 bytes > Q2_NOALLOC_SCRATCH_BYTES (1 MiB)
+    R, C = 131104, 256
     d = synth.bpdq(R, C, 7200)
     pk = q2.Packed(q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]), ntok_max=1)
     x = torch.zeros((1, C), dtype=torch.float16, device="cuda")
