@@ -52,6 +52,7 @@ struct B1 {
   unsigned long long* acc;      // [ntok][Rpad] accumulator words (zero between calls)
   float fscale, finv;           // 2^F and 2^-F of the fixed-point partials
   int R, C, Rpad, nrb, nslice, ntok;
+  int aligned;                  // 1: slice-aligned CTA ranges, 0: equal contiguous ranges
 };
 
 // Shared memory of the single-token table kernels: a small tail at the
@@ -233,8 +234,35 @@ __device__ __forceinline__ void acc_settle(Pending<NT>& pd, const B1& c, const F
   pd.row = -1;
 }
 
+// ------------------------------------------------------- work split
+// The CTA's contiguous range [i0, i1) of items in slice-major order.
+// Equal shares (c.aligned == 0) balance the item counts, but a CTA whose
+// share crosses a slice boundary builds a second table.  Slice-aligned
+// shares (c.aligned == 1): with at least as many CTAs as slices, slice g
+// gets the CTAs b with floor(b*ns/G) == g (floor(G/ns) or ceil(G/ns) of
+// them), which split its nrb row blocks evenly, so no CTA builds a second
+// table; with fewer CTAs than slices, each CTA takes whole slices
+// [floor(b*ns/G), floor((b+1)*ns/G)).  BPDQ items are cheap enough that the
+// second table costs more than the few extra items of the aligned split;
+// Leech and trellis items are not (measured on GB300).
+__device__ __forceinline__ void b1_range(const B1& c, int& i0, int& i1) {
+  const long long G = gridDim.x, b = blockIdx.x, ns = c.nslice, nrb = c.nrb;
+  if (!c.aligned) {
+    cta_range(c.nslice * c.nrb, i0, i1);
+  } else if (ns <= G) {
+    const long long g = b * ns / G;
+    const long long first = (g * G + ns - 1) / ns, last = ((g + 1) * G + ns - 1) / ns;
+    const long long k = b - first, kc = last - first;
+    i0 = (int)(g * nrb + k * nrb / kc);
+    i1 = (int)(g * nrb + (k + 1) * nrb / kc);
+  } else {
+    i0 = (int)(b * ns / G * nrb);
+    i1 = (int)((b + 1) * ns / G * nrb);
+  }
+}
+
 // ------------------------------------------------------- pipelined items
-// run_b1 drives every split-K kernel.  The CTA's contiguous item range is
+// run_b1 drives every split-K kernel.  The CTA's item range (b1_range) is
 // cut into groups: one slice per group for the table kernels (F::kGroup ==
 // 1), one group for everything in the trellis kernel.  x is staged into
 // shared memory for up to kStageMax / ntok slices at a time (F::kStaged);
@@ -248,7 +276,7 @@ template <int W, int AHEAD, class F>
 __device__ __forceinline__ void run_b1(F& f, const B1& c, unsigned char* tail) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int i0, i1;
-  cta_range(c.nslice * c.nrb, i0, i1);
+  b1_range(c, i0, i1);
   const int glast = (i1 - 1) / c.nrb;
   __half* xs = reinterpret_cast<__half*>(tail + kTailX);
   const int stage_n = max(1, kStageMax / c.ntok);
@@ -757,6 +785,7 @@ bool b1_shape_ok(const q2_blob_header& d) { return d.nslice >= 1 && d.nslice <= 
 B1 make_b1(const q2_handle* h, const void* x, void* y, int ntok) {
   const q2_blob_header& d = h->hdr;
   B1 c;
+  c.aligned = (d.fmt == Q2_BPDQ || d.fmt == Q2_NOWEIGHTS) ? 1 : 0;
   c.x = static_cast<const __half*>(x);
   c.y = static_cast<__half*>(y);
   c.acc = static_cast<unsigned long long*>(h->ws);
