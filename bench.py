@@ -38,9 +38,9 @@ L2_BYTES = 126 * 1024 * 1024
 # profiles/bpdq_b1_qwen3_8b_stack.md: (dram__bytes_read.sum +
 # dram__bytes_write.sum) / algorithmic bytes on a 24576x4096 launch.  The
 # stack's traffic per launch is that ratio times the stack's algorithmic
-# bytes per launch (traffic scales with the items processed).  None until
-# the current kernel has been captured.
-NCU_TRAFFIC_RATIO = {"k_bpdq_b1": None}
+# bytes per launch (traffic scales with the items processed).  Must be reset
+# to None whenever the kernel changes.
+NCU_TRAFFIC_RATIO = {"k_bpdq_b1": 27754496 / 27525120}
 
 
 def _peaks():

@@ -58,11 +58,11 @@ struct B1 {
 // Shared memory of the single-token table kernels: a small tail at the
 // start of dynamic shared memory (slice sums of x, Leech block sums, staged
 // x: up to kStageBytes / (512 * ntok) slices at once), then the table of the
-// current slice, placed at shared-window address kTabAddr so that the byte
-// permute of a lookup forms the final shared address by itself.
+// current slice at the fixed shared-window address kTabAddr, so that a
+// lookup's address is the byte permute's result plus an immediate offset.
 constexpr int kTab = 64 * 1024;        // one slice's table (duplicated columns)
-constexpr uint32_t kTabAddr = 65536;   // shared-window address of the table
-constexpr int kTabSmem = 2 * kTab;     // dynamic smem that reaches past kTabAddr + kTab
+constexpr uint32_t kTabAddr = 0x2000;  // shared-window address of the table
+constexpr int kTabSmem = kTabAddr + kTab;   // dynamic smem reaching kTabAddr + kTab from any window base
 constexpr int kTailGsum = 0;           // float [8]
 constexpr int kTailXb = 128;           // float [kStageMax][12], Leech block sums
 constexpr int kTailX = 512;            // fp16 staged x [slice][tok][256]
@@ -148,35 +148,33 @@ __device__ __forceinline__ float* tab1() {
 }
 
 // Table lookup for the byte at rotated position P (byte P & 3 of `word`).
-// lane4 holds lane*4 in byte 0 and kTabAddr >> 16 in byte 2, so the permute
-// gives the shared address kTabAddr + v*256 + lane*4 and the load adds P*4.
+// lane4 = lane*4, so the permute gives v*256 + lane*4 and the load adds
+// kTabAddr + P*4 as its immediate offset.
 template <int P>
 __device__ __forceinline__ float tl(uint32_t lane4, uint32_t word) {
-  const uint32_t a = __byte_perm(word, lane4, 0x7604u | ((uint32_t)(P & 3) << 4));
+  const uint32_t a = __byte_perm(word, lane4, 0x5504u | ((uint32_t)(P & 3) << 4));
   float v;
-  asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(a), "n"(P * 4));
+  asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(a), "n"(kTabAddr + P * 4));
   return v;
 }
-constexpr uint32_t kLane4Hi = kTabAddr;   // OR-ed into lane*4
+constexpr uint32_t kLane4Hi = 0;          // nothing to OR into lane*4
 
-// Lookups P and P + 1 into one of two packed fp32 accumulators, then the rest.
+// Lookup P into accumulator P mod 4, then the rest.
 template <int P>
-__device__ __forceinline__ void plane_steps(uint32_t lane4, const uint32_t (&w)[8], float2 (&s)[2]) {
+__device__ __forceinline__ void plane_steps(uint32_t lane4, const uint32_t (&w)[8], float (&s)[4]) {
   if constexpr (P < 32) {
-    const float2 v = make_float2(tl<P>(lane4, w[P >> 2]), tl<P + 1>(lane4, w[(P + 1) >> 2]));
-    s[(P >> 1) & 1] = __fadd2_rn(s[(P >> 1) & 1], v);
-    plane_steps<P + 2>(lane4, w, s);
+    s[P & 3] += tl<P>(lane4, w[P >> 2]);
+    plane_steps<P + 1>(lane4, w, s);
   }
 }
 
 // Sum of the table entries selected by 32 rotated bytes (two uint4 chunks),
-// accumulated two lookups at a time with packed fp32 adds.
+// in four independent fp32 accumulators.
 __device__ __forceinline__ float plane_sum(uint32_t lane4, const uint4& c0, const uint4& c1) {
   const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  float2 s[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
   plane_steps<0>(lane4, w, s);
-  const float2 t = __fadd2_rn(s[0], s[1]);
-  return t.x + t.y;
+  return (s[0] + s[1]) + (s[2] + s[3]);
 }
 
 // ------------------------------------------- fixed-point accumulation
@@ -342,12 +340,17 @@ __device__ __forceinline__ void ld_item(const unsigned char* base, int item_byte
 }
 
 // Launch shapes: 8 warps and <= 128 registers per thread, two CTAs per SM.
-// BPDQ keeps 2 items ahead per warp; Leech, whose items are 1.5x larger, 1.
+// BPDQ and Leech keep 1 item ahead per warp (measured: 2 ahead is slower).
 constexpr int kWarps = 16;
-// CTAs per SM the single-token kernels are built for: two at 8 warps
-// (<= 128 registers), one at 16.
-constexpr int kMinBlocks = kWarps <= 8 ? 2 : 1;
-constexpr int kBpdqAhead = 2;
+// CTAs per SM the BPDQ, no-weights and trellis kernels are built for.  With
+// 2, 16 warps fit in 64 registers and an SM holds one CTA of the running
+// GEMV and one of the GEMV launched after it, whose CTAs are then resident
+// early (no launch ramp): faster for GEMVs of ~20 items per CTA (Qwen3-8B
+// o-proj 2.9 vs 3.6 us), slower for large ones whose weight loads then
+// overlap less (gate_up 9.6 vs 8.3 us) and over the whole 8B stack (measured
+// on GB300).  Leech and the 2-token kernel run one per SM in any case.
+constexpr int kMinBlocks = 1;
+constexpr int kBpdqAhead = 1;
 constexpr int kLeechAhead = 1;
 
 // ------------------------------------------------------------------- BPDQ
@@ -489,7 +492,7 @@ struct LeechF {
 };
 
 template <int W, int AHEAD>
-__global__ void __launch_bounds__(W * 32, kMinBlocks) k_leech_b1(LeechArgs a) {
+__global__ void __launch_bounds__(W * 32, 1) k_leech_b1(LeechArgs a) {
   if ((uint32_t)__cvta_generic_to_shared(q2_smem) + kTailFixed > kTabAddr) return;   // layout needs a low window base
   LeechF<W * 32> f{a};
   run_b1<W, AHEAD>(f, a.c, tail1());
@@ -671,7 +674,7 @@ struct BpdqMtF {
 };
 
 template <int W, int AHEAD, int NP>
-__global__ void __launch_bounds__(W * 32, NP == 1 ? kMinBlocks : 1) k_bpdq_mt(BpdqArgs a) {
+__global__ void __launch_bounds__(W * 32, 1) k_bpdq_mt(BpdqArgs a) {
   unsigned char* tail = q2_smem + (size_t)NP * kPairBytes;
   BpdqMtF<W * 32, NP> f{a, tail};
   f.init(threadIdx.x & 31);
@@ -758,11 +761,12 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks) k_trellis_b1(TrellisArgs a
 }
 
 // ------------------------------------------------------------ host side
-// The 8-warp kernels ask for more than a third of an SM's shared memory, so
-// an SM holds at most two of their CTAs: while a GEMV runs, every SM holds
-// one of its CTAs and has room for exactly one CTA of the next GEMV, which
-// therefore spreads one per SM.  The kernels for 3..6 tokens (two or three
-// token-pair tables) need more than half and run one per SM, with the whole
+// With kMinBlocks == 2 the kernels ask for more than a third of an SM's
+// shared memory, so an SM holds at most two of their CTAs: while a GEMV
+// runs, every SM holds one of its CTAs and has room for exactly one CTA of
+// the next GEMV, which therefore spreads one per SM.  With kMinBlocks == 1
+// they ask for more than half.  The kernels for 3..6 tokens (two or three
+// token-pair tables) need more than half and run one per SM with the whole
 // register file.
 constexpr int kOneCtaSmem = 116 * 1024;
 constexpr int kTwoCtaSmem = kMinBlocks == 2 ? 80 * 1024 : kOneCtaSmem;
