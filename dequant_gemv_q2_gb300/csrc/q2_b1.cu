@@ -244,18 +244,20 @@ __device__ __forceinline__ void acc_settle(Pending<NT>& pd, const B1& c, const F
 // second table costs more than the few extra items of the aligned split;
 // Leech and trellis items are not (measured on GB300).
 __device__ __forceinline__ void b1_range(const B1& c, int& i0, int& i1) {
-  const long long G = gridDim.x, b = blockIdx.x, ns = c.nslice, nrb = c.nrb;
+  // 32-bit arithmetic throughout (b*ns <= 152*255, k*nrb <= 152*16384): the
+  // 64-bit divisions this replaces cost close to a microsecond of prologue
+  const int G = gridDim.x, b = blockIdx.x, ns = c.nslice, nrb = c.nrb;
   if (!c.aligned) {
-    cta_range(c.nslice * c.nrb, i0, i1);
+    cta_range(ns * nrb, i0, i1);
   } else if (ns <= G) {
-    const long long g = b * ns / G;
-    const long long first = (g * G + ns - 1) / ns, last = ((g + 1) * G + ns - 1) / ns;
-    const long long k = b - first, kc = last - first;
-    i0 = (int)(g * nrb + k * nrb / kc);
-    i1 = (int)(g * nrb + (k + 1) * nrb / kc);
+    const int g = b * ns / G;
+    const int first = (g * G + ns - 1) / ns, last = ((g + 1) * G + ns - 1) / ns;
+    const int k = b - first, kc = last - first;
+    i0 = g * nrb + k * nrb / kc;
+    i1 = g * nrb + (k + 1) * nrb / kc;
   } else {
-    i0 = (int)(b * ns / G * nrb);
-    i1 = (int)((b + 1) * ns / G * nrb);
+    i0 = b * ns / G * nrb;
+    i1 = (b + 1) * ns / G * nrb;
   }
 }
 
