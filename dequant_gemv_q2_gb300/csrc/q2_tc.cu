@@ -35,6 +35,8 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
+constexpr int kParts = kWarps / 4;            // warps per 32-row block, each decoding 256/kParts columns
+constexpr int kPartBytes = 32 / kParts;       // rotated column-bytes of one plane per lane and part
 constexpr int kRows = 128;                    // M of the MMA
 constexpr int kTileA = kRows * 256 * 2;       // 64 KiB per A buffer
 constexpr uint32_t kLBO = 128, kSBO = 4096;   // core-matrix strides (bytes)
@@ -197,23 +199,23 @@ __device__ __forceinline__ uint4 decode_leech_q(const Codes4& c) {
   return r;
 }
 
-// Trellis: steps 64*H .. +63 of a segment -> columns 128*H .. +127 of the A
-// row (column-byte = step / 4); H is a template parameter so every window
-// index is static.
+// Trellis: steps (128/kParts)*H .. of a segment -> columns (256/kParts)*H ..
+// of the A row (column-byte = step / 4); H is a template parameter so every
+// window index is static.
 template <int H>
-__device__ __forceinline__ void trellis_half(const uint32_t (&W)[16], const uint32_t* tab, unsigned char* arow) {
+__device__ __forceinline__ void trellis_part(const uint32_t (&W)[16], const uint32_t* tab, unsigned char* arow) {
 #pragma unroll
-  for (int cb = 0; cb < 16; ++cb) {
+  for (int cb = 0; cb < kPartBytes; ++cb) {
     uint32_t e4[4];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const int k = H * 64 + cb * 4 + t;
+      const int k = H * kPartBytes * 4 + cb * 4 + t;
       const int n = 127 - k;
       const uint32_t f = __funnelshift_r(W[n >> 3], W[((n >> 3) + 1) & 15], 4 * (n & 7));
       const uint32_t e = tab[(f * kHashHi) >> 20];
       e4[t] = e ^ ((f & 1u) ? 0x80008000u : 0u);
     }
-    *reinterpret_cast<uint4*>(arow + (H * 16 + cb) * kLBO) = make_uint4(e4[0], e4[1], e4[2], e4[3]);
+    *reinterpret_cast<uint4*>(arow + (H * kPartBytes + cb) * kLBO) = make_uint4(e4[0], e4[1], e4[2], e4[3]);
   }
 }
 
@@ -227,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(TcArgs a) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(B0 + 2 * bbytes);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rbl = warp & 3, half = warp >> 2;        // row block in tile, half of the slice
+  const int rbl = warp & 3, part = warp >> 2;        // row block in tile, part of the slice
   const int tile = blockIdx.x % a.ntile, split = blockIdx.x / a.ntile;
   const int sA = split * a.S / a.nsplit, sB = (split + 1) * a.S / a.nsplit;
   const int rb = tile * 4 + rbl;
@@ -255,8 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(TcArgs a) {
   // zero both B buffers once (padding tokens, unused parity columns)
   for (int i = threadIdx.x; i < 2 * bbytes / 16; i += kThreads) reinterpret_cast<uint4*>(B0)[i] = make_uint4(0, 0, 0, 0);
 
-  // per-lane payload of one slice: BPDQ/Leech the half's chunks of each plane,
-  // trellis the whole 64-byte packet; plus BPDQ's value table / Leech's parity
+  // per-lane payload of one slice: BPDQ/Leech the part's kPartBytes rotated
+  // bytes of each plane (rotated positions part*kPartBytes ..), trellis the
+  // whole 64-byte packet; plus BPDQ's value table / Leech's parity
   constexpr int NP = FMT == Q2_BPDQ ? 2 : FMT == Q2_LEECH ? 3 : 4;
   uint4 pl[NP];
   uint2 vt = make_uint2(0, 0);
@@ -266,9 +269,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(TcArgs a) {
     if (FMT == Q2_TRELLIS) {
 #pragma unroll
       for (int k = 0; k < NP; ++k) d[k] = __ldg(reinterpret_cast<const uint4*>(ip + k * 512));
-    } else {
+    } else if (kParts == 2) {
 #pragma unroll
-      for (int k = 0; k < NP; ++k) d[k] = ldg_stream(ip + (2 * k + half) * 512);
+      for (int k = 0; k < NP; ++k) d[k] = ldg_stream(ip + (2 * k + part) * 512);
+    } else {                                  // kParts == 4: 8 bytes of a chunk
+#pragma unroll
+      for (int k = 0; k < NP; ++k) {
+        const uint2 h = __ldg(reinterpret_cast<const uint2*>(ip + (2 * k + (part >> 1)) * 512 + (part & 1) * 8));
+        d[k] = make_uint4(h.x, h.y, 0u, 0u);
+      }
     }
     if (FMT == Q2_BPDQ) v = a.vtab[(size_t)s * a.Rpad + row];
     if (FMT == Q2_LEECH) pw = a.parity[(size_t)s * a.Rpad + row];
@@ -345,17 +354,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(TcArgs a) {
       if (FMT == Q2_TRELLIS) {
         const uint32_t W[16] = {pl[0].x, pl[0].y, pl[0].z, pl[0].w, pl[1].x, pl[1].y, pl[1].z, pl[1].w,
                                 pl[2].x, pl[2].y, pl[2].z, pl[2].w, pl[3].x, pl[3].y, pl[3].z, pl[3].w};
-        if (half == 0) trellis_half<0>(W, tab, arow);
-        else trellis_half<1>(W, tab, arow);
+        if (part == 0) trellis_part<0>(W, tab, arow);
+        else if (part == 1) trellis_part<1>(W, tab, arow);
+        else if (kParts > 2 && part == 2) trellis_part<(kParts > 2 ? 2 : 0)>(W, tab, arow);
+        else if (kParts > 2) trellis_part<(kParts > 2 ? 3 : 0)>(W, tab, arow);
       } else {
-        const uint32_t rot = (uint32_t)(half * 16 + lane) * kLBO;
+        const uint32_t rot = (uint32_t)(part * kPartBytes + lane) * kLBO;
+        constexpr int NW = kPartBytes / 4;      // 32-bit words of a plane per lane and part
         if (FMT == Q2_BPDQ) {
           const uint32_t tlo = __byte_perm(vt.x, vt.y, 0x6420u);
           const uint32_t thi = __byte_perm(vt.x, vt.y, 0x7531u);
           const uint32_t w0[4] = {pl[0].x, pl[0].y, pl[0].z, pl[0].w};
           const uint32_t w1[4] = {pl[1].x, pl[1].y, pl[1].z, pl[1].w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < NW; ++j) {
             const Codes4 c = codes4(w0[j], w1[j]);
             *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 0) * kLBO) & 4095u)) = decode_q<0>(c, tlo, thi);
             *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 1) * kLBO) & 4095u)) = decode_q<1>(c, tlo, thi);
@@ -367,14 +379,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(TcArgs a) {
           const uint32_t w1[4] = {pl[1].x, pl[1].y, pl[1].z, pl[1].w};
           const uint32_t w2[4] = {pl[2].x, pl[2].y, pl[2].z, pl[2].w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < NW; ++j) {
             const Codes4 c = codes4x3(w0[j], w1[j], w2[j]);
             *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 0) * kLBO) & 4095u)) = decode_leech_q<0>(c);
             *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 1) * kLBO) & 4095u)) = decode_leech_q<1>(c);
             *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 2) * kLBO) & 4095u)) = decode_leech_q<2>(c);
             *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 3) * kLBO) & 4095u)) = decode_leech_q<3>(c);
           }
-          if (half == 0) {
+          if (part == 0) {
             // parity columns: A = 1.0 where the block starting in this slice is odd
             uint32_t pv[8];
 #pragma unroll
