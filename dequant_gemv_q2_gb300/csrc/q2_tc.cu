@@ -294,55 +294,56 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(TcArgs a) {
   const uint32_t idesc = idesc_f16(kRows, a.N);
   bool ok = true;
 
+  // x tile (and Leech parity columns) of slice s into B buffer Bb: cp.async
+  // copies, waited for before the slice's MMAs are issued
+  auto stage_x = [&](int s, unsigned char* Bb) {
+    const int ncols_s = min(256, a.C - s * 256);     // Leech: the last slice may be short
+    const __half* xs = a.x + (size_t)s * 256;
+    const uint32_t bb0 = saddr(Bb);
+    for (int e = threadIdx.x; e < a.ntok * 32; e += kThreads) {
+      const int n = e >> 5, kc = e & 31;
+      const uint32_t dst = bb0 + (n >> 3) * Sh::sbo + kc * kLBO + (n & 7) * 16;
+      if (kc * 8 + 8 <= ncols_s) {
+        cp_async16(dst, xs + (size_t)n * a.C + kc * 8);
+      } else {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        __half* hv = reinterpret_cast<__half*>(&v);
+        for (int i = 0; i < 8; ++i)
+          if (kc * 8 + i < ncols_s) hv[i] = xs[(size_t)n * a.C + kc * 8 + i];
+        *reinterpret_cast<uint4*>(Bb + (n >> 3) * Sh::sbo + kc * kLBO + (n & 7) * 16) = v;
+      }
+    }
+    if (FMT == Q2_LEECH) {
+      // parity columns: block sums of x for the blocks starting in this slice,
+      // hi part in chunks 32-33, lo part (x - hi) in chunks 34-35
+      const int bfirst = (s * 256 + 23) / 24;
+      const int blast = min(a.nblock - 1, (s * 256 + 256 + 23) / 24 - 1);
+      const int nbk = max(0, blast - bfirst + 1);
+      for (int e = threadIdx.x; e < a.ntok * 16; e += kThreads) {
+        const int n = e >> 4, jb = e & 15;
+        float xsum = 0.f;
+        if (jb < nbk) {
+          const __half* xp = a.x + (size_t)n * a.C + (size_t)(bfirst + jb) * 24;
+          for (int i = 0; i < 24; ++i) xsum += __half2float(xp[i]);
+        }
+        const __half hi = __float2half_rn(xsum);
+        const __half lo = __float2half_rn(xsum - __half2float(hi));
+        unsigned char* bn = Bb + (n >> 3) * Sh::sbo + (n & 7) * 16;
+        reinterpret_cast<__half*>(bn + (32 + (jb >> 3)) * kLBO)[jb & 7] = hi;
+        reinterpret_cast<__half*>(bn + (34 + (jb >> 3)) * kLBO)[jb & 7] = lo;
+      }
+    }
+  };
+  if (sA < sB) stage_x(sA, B0);
+
+  // Slice s: decode the weights into A[buf] while x(s) lands in B[buf], then
+  // one thread issues the MMAs.  Right after, once the MMAs of slice s - 1
+  // have released the other buffers, x(s + 1) is staged into them, so its
+  // L2 round trip overlaps the decode of slice s + 1.
   for (int s = sA; s < sB && ok; ++s) {
     const int buf = (s - sA) & 1;
     unsigned char* Ab = A0 + buf * Sh::tileA;
     unsigned char* Bb = B0 + buf * bbytes;
-    if (s - sA >= 2) {
-      if (!mbar_wait(saddr(&bars[buf]), (uint32_t)(((s - sA) >> 1) - 1) & 1u)) {
-        ok = false;
-        if (threadIdx.x == 0) atomicExch(&q2_tc_error, 1u);
-      }
-    }
-    const int ncols_s = min(256, a.C - s * 256);     // Leech: the last slice may be short
-    if (ok) {
-      // x tile of this slice (zero beyond C), copied asynchronously
-      const __half* xs = a.x + (size_t)s * 256;
-      const uint32_t bb0 = saddr(Bb);
-      for (int e = threadIdx.x; e < a.ntok * 32; e += kThreads) {
-        const int n = e >> 5, kc = e & 31;
-        const uint32_t dst = bb0 + (n >> 3) * Sh::sbo + kc * kLBO + (n & 7) * 16;
-        if (kc * 8 + 8 <= ncols_s) {
-          cp_async16(dst, xs + (size_t)n * a.C + kc * 8);
-        } else {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          __half* hv = reinterpret_cast<__half*>(&v);
-          for (int i = 0; i < 8; ++i)
-            if (kc * 8 + i < ncols_s) hv[i] = xs[(size_t)n * a.C + kc * 8 + i];
-          *reinterpret_cast<uint4*>(Bb + (n >> 3) * Sh::sbo + kc * kLBO + (n & 7) * 16) = v;
-        }
-      }
-      if (FMT == Q2_LEECH) {
-        // parity columns: block sums of x for the blocks starting in this slice,
-        // hi part in chunks 32-33, lo part (x - hi) in chunks 34-35
-        const int bfirst = (s * 256 + 23) / 24;
-        const int blast = min(a.nblock - 1, (s * 256 + 256 + 23) / 24 - 1);
-        const int nbk = max(0, blast - bfirst + 1);
-        for (int e = threadIdx.x; e < a.ntok * 16; e += kThreads) {
-          const int n = e >> 4, jb = e & 15;
-          float xsum = 0.f;
-          if (jb < nbk) {
-            const __half* xp = a.x + (size_t)n * a.C + (size_t)(bfirst + jb) * 24;
-            for (int i = 0; i < 24; ++i) xsum += __half2float(xp[i]);
-          }
-          const __half hi = __float2half_rn(xsum);
-          const __half lo = __float2half_rn(xsum - __half2float(hi));
-          unsigned char* bn = Bb + (n >> 3) * Sh::sbo + (n & 7) * 16;
-          reinterpret_cast<__half*>(bn + (32 + (jb >> 3)) * kLBO)[jb & 7] = hi;
-          reinterpret_cast<__half*>(bn + (34 + (jb >> 3)) * kLBO)[jb & 7] = lo;
-        }
-      }
-    }
     uint4 nx[NP];
     uint2 nvt = vt;
     uint32_t npar = par;
@@ -416,6 +417,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(TcArgs a) {
         mma_f16(tmem, sdesc_s(aa + k * 2 * kLBO, Sh::sbo), sdesc_s(bb + k * 2 * kLBO, Sh::sbo), idesc,
                 (s > sA || k > 0) ? 1u : 0u);
       mma_commit(saddr(&bars[buf]));
+    }
+    if (ok && s + 1 < sB) {
+      const int nb = buf ^ 1;
+      if (s > sA && !mbar_wait(saddr(&bars[nb]), (uint32_t)((s - 1 - sA) >> 1) & 1u)) {
+        ok = false;
+        if (threadIdx.x == 0) atomicExch(&q2_tc_error, 1u);
+      }
+      if (ok) stage_x(s + 1, B0 + nb * bbytes);
     }
 #pragma unroll
     for (int k = 0; k < NP; ++k) pl[k] = nx[k];
