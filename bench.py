@@ -40,7 +40,7 @@ L2_BYTES = 126 * 1024 * 1024
 # stack's traffic per launch is that ratio times the stack's algorithmic
 # bytes per launch (traffic scales with the items processed).  Must be reset
 # to None whenever the kernel changes.
-NCU_TRAFFIC_RATIO = {"k_bpdq_b1": 27754496 / 27525120}
+NCU_TRAFFIC_RATIO = {"k_bpdq_b1": 27751936 / 27525120}
 
 
 def _peaks():
