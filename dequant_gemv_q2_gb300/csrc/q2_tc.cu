@@ -1,26 +1,48 @@
 // Skinny-GEMM path on the 5th-generation tensor cores (tcgen05) for
-// 16 <= padded ntok <= 64: decode once per tile, multiply for every token.
+// 2..64 tokens (padded to N = 16, 32, 48 or 64): decode once per tile,
+// multiply for every token.
 //
 // A CTA owns 128 output rows (four 32-row blocks) and a range of 256-column
-// slices.  For each slice, its 8 warps decode the packed weights of the
-// 128 x 256 tile into fp16 in shared memory (the canonical decoded weights:
-// BPDQ through the per-(group, row) 4-entry value table, one byte permute
-// per two or four weights), the x tile of all tokens is staged next to it,
-// and one thread issues sixteen tcgen05.mma.kind::f16 (M = 128, N = padded
-// ntok, K = 16) that accumulate in a TMEM fp32 tile.  A and B tiles are
-// double-buffered; an mbarrier per buffer, armed by tcgen05.commit, tells
-// the decoders when the tensor core has finished reading a buffer.  At the
-// end each warp reads its 32 TMEM lanes (its 32 rows) and writes fp32
-// partial sums for the split-K reduction kernel, or y directly.
+// slices, and runs them through a ring of kStages stages with three roles:
+//   - 8 decoder warps turn the packed weights of the 128 x 256 tile into
+//     fp16 in registers (BPDQ through the per-(group, row) 4-entry value
+//     table, one byte permute per two or four weights) and store them into
+//     tensor memory with tcgen05.st, one TMEM lane per row (the stage's A);
+//   - one producer lane of the ninth warp loads the x tile of all tokens into
+//     shared memory with four 2D TMA copies (the stage's B);
+//   - the same lane, once a stage's A and B are both complete (one mbarrier
+//     per stage: 8 decoder arrivals plus the TMA bytes), issues sixteen
+//     tcgen05.mma.kind::f16 (M = 128, N, K = 16) reading A from TMEM and B
+//     from shared memory into one fp32 accumulator in TMEM, and commits them
+//     to the stage's "empty" mbarrier, which frees the stage for refilling.
+// No role waits for another except through these barriers, so the decode of
+// slice s + 1, the x copy of slice s + 2 and the MMAs of slice s overlap.
+// At the end the decoder warps read the accumulator (each its 32 TMEM
+// lanes) and write fp32 partial sums for the split-K reduction kernel, or y
+// directly.
 //
-// Operand layout in shared memory: K-major, no swizzle, core matrices of
-// 8 rows x 16 bytes; the byte offset of element (row m, k) is
-// (m / 8) * 4096 + (k / 8) * 128 + (m % 8) * 16 + (k % 8) * 2, i.e. leading
-// (K) byte offset 128 and stride (M/N) byte offset 4096.
+// TMEM columns (all 512 are allocated; one CTA per SM): D at 0 .. N - 1,
+// A of stage st at kAcol0 + st * (4 x K chunks); A column j of a lane holds
+// the fp16 weights k = 2j (low half) and 2j + 1 (high half) of its row.
+//
+// B in shared memory: K-major with the 128-byte swizzle, as the TMA writes
+// it: the slice's K range in atoms of 64 columns, atom a at a * N * 128
+// bytes; inside it token n's 128-byte row at n * 128 with 16-byte chunk c
+// stored at chunk c ^ (n % 8).  The MMA descriptor gives stride 1024 bytes
+// between 8-row groups and steps 32 bytes per K = 16 inside an atom.
+//
+// The BPDQ and Leech planes are stored lane-rotated for the batch-1 kernels
+// (byte j of lane l's 32-byte plane row holds column-byte (j + l) mod 32).
+// Every lane loads its whole rows and undoes the rotation in registers
+// before decoding, because a TMEM store writes the same columns in every
+// lane.
 //
 // Every wait is bounded: a wait that runs out records an error code in
 // q2_tc_error (read back with q2_device_errors) and the kernel skips the
-// rest of its work, then frees its TMEM columns.
+// rest of its work; the producer lane waits for its outstanding copies and
+// MMAs before the CTA frees its TMEM columns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include "q2_common.cuh"
@@ -33,25 +55,16 @@ __device__ unsigned int q2_tc_error = 0;
 namespace q2 {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kParts = kWarps / 4;            // warps per 32-row block, each decoding 256/kParts columns
-constexpr int kPartBytes = 32 / kParts;       // rotated column-bytes of one plane per lane and part
+constexpr int kDecWarps = 8;                  // decoder warps; one more warp copies x and issues MMAs
+constexpr int kThreads = (kDecWarps + 1) * 32;
+constexpr int kStages = 3;                    // slices in flight (A in TMEM, B in shared memory)
+constexpr int kParts = kDecWarps / 4;         // warps per 32-row block, each decoding 256/kParts columns
+constexpr int kPartBytes = 32 / kParts;       // column-bytes of one plane per lane and part
+static_assert(kParts == 2, "the decode splits a row's 32 column-bytes between two warps");
 constexpr int kRows = 128;                    // M of the MMA
-constexpr int kTileA = kRows * 256 * 2;       // 64 KiB per A buffer
-constexpr uint32_t kLBO = 128, kSBO = 4096;   // core-matrix strides (bytes)
-
-// Shared-memory matrix descriptor (tcgen05): start >> 4 in bits 0-13,
-// leading byte offset >> 4 in 16-29, stride byte offset >> 4 in 32-45,
-// descriptor version 1 in 46-47, no swizzle (61-63 = 0).
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr >> 4) & 0x3FFF);
-  d |= (uint64_t)((kLBO >> 4) & 0x3FFF) << 16;
-  d |= (uint64_t)((kSBO >> 4) & 0x3FFF) << 32;
-  d |= (uint64_t)1 << 46;
-  return d;
-}
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAcol0 = 64;               // D takes TMEM columns 0..63
+constexpr int kOneCtaSmem = 116 * 1024;       // two CTAs never share an SM (each holds all of TMEM)
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
 // (7-9, 10-12 = 0), both K-major (15, 16 = 0), N >> 3 in 17-22, M >> 4 in 24-28.
@@ -59,14 +72,51 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                        uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] x B[smem descriptor]
+__device__ __forceinline__ void mma_f16_ta(uint32_t dtmem, uint32_t atmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(dtmem),
+      "r"(atmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane (the warp's 32 lanes).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, uint4 a, uint4 b, uint4 c, uint4 d) {
+  const uint32_t r[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+  tmem_st16(taddr, r);
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Canonical words 4P .. 4P + 3 (column-bytes 16P .. 16P + 15) of one plane
+// row from its 8 lane-rotated words R (rotated byte j = column-byte
+// (j + lane) mod 32).  With lane = 4a + r, canonical word c starts at
+// rotated byte 4(c - a) - r: the word rotation by a runs as three
+// conditional rotations by 1, 2 and 4 words, the byte offset r as a funnel
+// shift (clamped: r = 0 takes the high word whole).
+template <int P>
+__device__ __forceinline__ void unrotate_half(const uint32_t (&R)[8], int lane, uint32_t (&cw)[4]) {
+  const int a = lane >> 2;
+  const uint32_t sh = 32u - 8u * (uint32_t)(lane & 3);
+  uint32_t t[8], u[8], v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) t[i] = (a & 1) ? R[(i + 7) & 7] : R[i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) u[i] = (a & 2) ? t[(i + 6) & 7] : t[i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = (a & 4) ? u[(i + 4) & 7] : u[i];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) cw[c] = __funnelshift_rc(v[(4 * P + c + 7) & 7], v[4 * P + c], sh);
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -130,12 +180,28 @@ __device__ __forceinline__ uint4 decode_q(const Codes4& c, uint32_t tlo, uint32_
   return r;
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// one arrival that also expects `bytes` of asynchronous copies
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// 2D TMA tile load of box (x, y) of the tensor map into shared memory; the
+// bytes are reported to the mbarrier.  x * 2 bytes is a multiple of 128.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void sleep_us(int us) {
+  for (int k = 0; k < us; ++k) __nanosleep(1000);
+}
 
 struct TcArgs {
+  CUtensorMap xmap;            // x [ntok][C] fp16: box 64 columns x N tokens, 128-byte swizzle (use_tma)
   const unsigned char* bits;   // item stream (BPDQ bits, trellis symbols, Leech planes)
   const uint2* vtab;           // BPDQ: [G][Rpad] 4 halves
   const uint32_t* table;       // trellis: 4096 half2
@@ -144,6 +210,7 @@ struct TcArgs {
   __half* y;                   // [ntok][R]  (nsplit == 1, BPDQ only)
   float* partial;              // [ntok][nsplit][Rpad]
   int R, C, Rpad, nrb, S, ntok, N, nsplit, ntile, nblock;
+  int use_tma;                 // 0: x rows not 16-byte aligned, staged with element loads
 };
 
 constexpr uint32_t kHashHi = 0x9E37u << 16;     // trellis: (s*0x9E37 mod 2^16) in bits 16..31
@@ -154,20 +221,24 @@ constexpr uint32_t kHashHi = 0x9E37u << 16;     // trellis: (s*0x9E37 mod 2^16) 
 template <int FMT>
 struct TcShape {
   static constexpr int kch = FMT == Q2_LEECH ? 36 : 32;
-  static constexpr uint32_t sbo = kch * 128;
-  static constexpr int tileA = kRows * kch * 16;
+  static constexpr int kmma = kch / 2;                  // K = 16 steps per slice
+  static constexpr int atoms = (kch + 7) / 8;           // 64-column swizzle atoms of B
+  static constexpr uint32_t acols = kch * 4;            // TMEM columns of one A stage
   static constexpr int table = FMT == Q2_TRELLIS ? 4096 * 4 : 0;
   static constexpr int item = FMT == Q2_BPDQ ? Q2_ITEM_BYTES_BPDQ : FMT == Q2_TRELLIS ? Q2_ITEM_BYTES_TRL
                                                                                      : Q2_ITEM_BYTES_LEECH;
 };
+static_assert(kAcol0 + kStages * TcShape<Q2_LEECH>::acols <= kTmemCols, "A stages exceed TMEM");
 
-__device__ __forceinline__ uint64_t sdesc_s(uint32_t addr, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr >> 4) & 0x3FFF);
-  d |= (uint64_t)((kLBO >> 4) & 0x3FFF) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
-  d |= (uint64_t)1 << 46;
-  return d;
+// Shared-memory matrix descriptor (tcgen05) of a K-major operand with the
+// 128-byte swizzle: start >> 4 in bits 0-13, leading byte offset field 1
+// (not used by swizzled K-major layouts), stride byte offset 1024 >> 4 in
+// 32-45 (8 rows x 128 bytes), version 1 in 46-47, base offset 0, swizzle
+// mode 2 (128-byte) in 61-63.  A K step inside an atom adds its byte offset
+// to the start address.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
 // Leech: 3-bit codes b0 | b1 << 1 | b2 << 2 of the columns of 4 column-bytes
@@ -200,243 +271,303 @@ __device__ __forceinline__ uint4 decode_leech_q(const Codes4& c) {
 }
 
 // Trellis: steps (128/kParts)*H .. of a segment -> columns (256/kParts)*H ..
-// of the A row (column-byte = step / 4); H is a template parameter so every
-// window index is static.
+// of the A row (column-byte = step / 4, four TMEM columns per column-byte);
+// H is a template parameter so every window index is static.
 template <int H>
-__device__ __forceinline__ void trellis_part(const uint32_t (&W)[16], const uint32_t* tab, unsigned char* arow) {
+__device__ __forceinline__ void trellis_part(const uint32_t (&W)[16], const uint32_t* tab, uint32_t ta) {
 #pragma unroll
-  for (int cb = 0; cb < kPartBytes; ++cb) {
-    uint32_t e4[4];
+  for (int g = 0; g < kPartBytes / 4; ++g) {
+    uint32_t e[16];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int k = H * kPartBytes * 4 + cb * 4 + t;
+    for (int t = 0; t < 16; ++t) {
+      const int k = H * kPartBytes * 4 + g * 16 + t;
       const int n = 127 - k;
       const uint32_t f = __funnelshift_r(W[n >> 3], W[((n >> 3) + 1) & 15], 4 * (n & 7));
-      const uint32_t e = tab[(f * kHashHi) >> 20];
-      e4[t] = e ^ ((f & 1u) ? 0x80008000u : 0u);
+      e[t] = tab[(f * kHashHi) >> 20] ^ ((f & 1u) ? 0x80008000u : 0u);
     }
-    *reinterpret_cast<uint4*>(arow + (H * kPartBytes + cb) * kLBO) = make_uint4(e4[0], e4[1], e4[2], e4[3]);
+    tmem_st16(ta + (uint32_t)(H * kPartBytes + g * 4) * 4u, e);
+  }
+}
+
+// BPDQ: column-bytes 16P .. 16P + 15 of one row (planes R0, R1 as loaded,
+// lane-rotated) into TMEM columns 64P .. 64P + 63 at ta.
+template <int P>
+__device__ __forceinline__ void bpdq_part(const uint32_t (&R0)[8], const uint32_t (&R1)[8], int lane, uint32_t tlo,
+                                          uint32_t thi, uint32_t ta) {
+  uint32_t c0[4], c1[4];
+  unrotate_half<P>(R0, lane, c0);
+  unrotate_half<P>(R1, lane, c1);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const Codes4 c = codes4(c0[j], c1[j]);
+    tmem_st16(ta + (uint32_t)(64 * P + 16 * j), decode_q<0>(c, tlo, thi), decode_q<1>(c, tlo, thi),
+              decode_q<2>(c, tlo, thi), decode_q<3>(c, tlo, thi));
+  }
+}
+
+// Leech: the same for the three sign/magnitude planes (values 2u).
+template <int P>
+__device__ __forceinline__ void leech_part(const uint32_t (&R0)[8], const uint32_t (&R1)[8], const uint32_t (&R2)[8],
+                                           int lane, uint32_t ta) {
+  uint32_t c0[4], c1[4], c2[4];
+  unrotate_half<P>(R0, lane, c0);
+  unrotate_half<P>(R1, lane, c1);
+  unrotate_half<P>(R2, lane, c2);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const Codes4 c = codes4x3(c0[j], c1[j], c2[j]);
+    tmem_st16(ta + (uint32_t)(64 * P + 16 * j), decode_leech_q<0>(c), decode_leech_q<1>(c), decode_leech_q<2>(c),
+              decode_leech_q<3>(c));
   }
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, 1) k_tc(TcArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcArgs a) {
   using Sh = TcShape<FMT>;
   uint32_t* tab = reinterpret_cast<uint32_t*>(q2_smem);            // trellis table
-  unsigned char* A0 = q2_smem + Sh::table;
-  unsigned char* B0 = A0 + 2 * Sh::tileA;
-  const int bbytes = (a.N / 8) * (int)Sh::sbo;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(B0 + 2 * bbytes);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+  // kStages B buffers from the first 1024-byte boundary after the table
+  const uint32_t sbase = saddr(q2_smem);
+  unsigned char* B0 = q2_smem + (((sbase + Sh::table + 1023u) & ~1023u) - sbase);
+  const int atom_bytes = a.N * 128;
+  const int bbytes = Sh::atoms * atom_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(B0 + kStages * bbytes);
+  uint64_t* empty = full + kStages;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(empty + kStages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rbl = warp & 3, part = warp >> 2;        // row block in tile, part of the slice
+  const bool producer = warp == kDecWarps;
+  const int rbl = warp & 3, part = (warp >> 2) & 1;  // row block in tile (= TMEM lane quarter), half of the slice
   const int tile = blockIdx.x % a.ntile, split = blockIdx.x / a.ntile;
   const int sA = split * a.S / a.nsplit, sB = (split + 1) * a.S / a.nsplit;
+  const int used = sB - sA;
   const int rb = tile * 4 + rbl;
-  const bool valid = rb < a.nrb;                     // the last tile may be ragged
+  const bool valid = !producer && rb < a.nrb;        // the last tile may be ragged
   const int row = rb * 32 + lane;
-  const int m = rbl * 32 + lane;                     // row inside the tile
-  const uint32_t ncols = a.N <= 32 ? 32u : 64u;
   const int tile_rbs = min(4, a.nrb - tile * 4);
 
   if (threadIdx.x == 0) {
     for (int s = sA; s < sB; ++s)
       prefetch_l2(a.bits + ((size_t)s * a.nrb + tile * 4) * Sh::item, (size_t)tile_rbs * Sh::item);
-    mbar_init(saddr(&bars[0]), 1);
-    mbar_init(saddr(&bars[1]), 1);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(saddr(&full[st]), kDecWarps + 1);
+      mbar_init(saddr(&empty[st]), 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tslot)),
-                 "r"(ncols)
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (FMT == Q2_TRELLIS)
     for (int i = threadIdx.x; i < 4096; i += kThreads) tab[i] = a.table[i];
-  // zero both B buffers once (padding tokens, unused parity columns)
-  for (int i = threadIdx.x; i < 2 * bbytes / 16; i += kThreads) reinterpret_cast<uint4*>(B0)[i] = make_uint4(0, 0, 0, 0);
+  // zero the B buffers once: token rows past ntok of the Leech parity atom
+  // (and of every atom when x is staged without TMA) stay zero
+  for (int i = threadIdx.x; i < kStages * bbytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(B0)[i] = make_uint4(0, 0, 0, 0);
+  fence_async_smem();
 
-  // per-lane payload of one slice: BPDQ/Leech the part's kPartBytes rotated
-  // bytes of each plane (rotated positions part*kPartBytes ..), trellis the
-  // whole 64-byte packet; plus BPDQ's value table / Leech's parity
-  constexpr int NP = FMT == Q2_BPDQ ? 2 : FMT == Q2_LEECH ? 3 : 4;
-  uint4 pl[NP];
-  uint2 vt = make_uint2(0, 0);
-  uint32_t par = 0;
+  // per-lane payload of one slice: the whole 512-byte chunks of the item at
+  // this lane (BPDQ / Leech: chunk 2p + h = half h of plane p, lane-rotated;
+  // trellis: the 64-byte packet); plus BPDQ's value table / Leech's parity
+  constexpr int NP = FMT == Q2_LEECH ? 6 : 4;
+  uint4 pl[NP], n1[NP];
+  uint2 vt = make_uint2(0, 0), v1 = make_uint2(0, 0);
+  uint32_t par = 0, p1 = 0;
   auto load = [&](int s, uint4 (&d)[NP], uint2& v, uint32_t& pw) {
     const unsigned char* ip = a.bits + ((size_t)s * a.nrb + rb) * Sh::item + lane * 16;
-    if (FMT == Q2_TRELLIS) {
 #pragma unroll
-      for (int k = 0; k < NP; ++k) d[k] = __ldg(reinterpret_cast<const uint4*>(ip + k * 512));
-    } else if (kParts == 2) {
-#pragma unroll
-      for (int k = 0; k < NP; ++k) d[k] = ldg_stream(ip + (2 * k + part) * 512);
-    } else {                                  // kParts == 4: 8 bytes of a chunk
-#pragma unroll
-      for (int k = 0; k < NP; ++k) {
-        const uint2 h = __ldg(reinterpret_cast<const uint2*>(ip + (2 * k + (part >> 1)) * 512 + (part & 1) * 8));
-        d[k] = make_uint4(h.x, h.y, 0u, 0u);
-      }
-    }
+    for (int k = 0; k < NP; ++k) d[k] = __ldg(reinterpret_cast<const uint4*>(ip + k * 512));
     if (FMT == Q2_BPDQ) v = a.vtab[(size_t)s * a.Rpad + row];
     if (FMT == Q2_LEECH) pw = a.parity[(size_t)s * a.Rpad + row];
   };
 #pragma unroll
-  for (int k = 0; k < NP; ++k) pl[k] = make_uint4(0, 0, 0, 0);
-  if (valid && sA < sB) load(sA, pl, vt, par);
+  for (int k = 0; k < NP; ++k) pl[k] = n1[k] = make_uint4(0, 0, 0, 0);
+  if (valid && used > 0) load(sA, pl, vt, par);
+  if (valid && used > 1) load(sA + 1, n1, v1, p1);
   pdl_wait();
   pdl_trigger();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t idesc = idesc_f16(kRows, a.N);
+  const uint32_t tlane = tmem + ((uint32_t)(rbl * 32) << 16);     // this warp's lane quarter
   bool ok = true;
 
-  // x tile (and Leech parity columns) of slice s into B buffer Bb: cp.async
-  // copies, waited for before the slice's MMAs are issued
-  auto stage_x = [&](int s, unsigned char* Bb) {
-    const int ncols_s = min(256, a.C - s * 256);     // Leech: the last slice may be short
-    const __half* xs = a.x + (size_t)s * 256;
-    const uint32_t bb0 = saddr(Bb);
-    for (int e = threadIdx.x; e < a.ntok * 32; e += kThreads) {
-      const int n = e >> 5, kc = e & 31;
-      const uint32_t dst = bb0 + (n >> 3) * Sh::sbo + kc * kLBO + (n & 7) * 16;
-      if (kc * 8 + 8 <= ncols_s) {
-        cp_async16(dst, xs + (size_t)n * a.C + kc * 8);
-      } else {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        __half* hv = reinterpret_cast<__half*>(&v);
-        for (int i = 0; i < 8; ++i)
-          if (kc * 8 + i < ncols_s) hv[i] = xs[(size_t)n * a.C + kc * 8 + i];
-        *reinterpret_cast<uint4*>(Bb + (n >> 3) * Sh::sbo + kc * kLBO + (n & 7) * 16) = v;
-      }
-    }
-    if (FMT == Q2_LEECH) {
-      // parity columns: block sums of x for the blocks starting in this slice,
-      // hi part in chunks 32-33, lo part (x - hi) in chunks 34-35
-      const int bfirst = (s * 256 + 23) / 24;
-      const int blast = min(a.nblock - 1, (s * 256 + 256 + 23) / 24 - 1);
-      const int nbk = max(0, blast - bfirst + 1);
-      for (int e = threadIdx.x; e < a.ntok * 16; e += kThreads) {
-        const int n = e >> 4, jb = e & 15;
-        float xsum = 0.f;
-        if (jb < nbk) {
-          const __half* xp = a.x + (size_t)n * a.C + (size_t)(bfirst + jb) * 24;
-          for (int i = 0; i < 24; ++i) xsum += __half2float(xp[i]);
-        }
-        const __half hi = __float2half_rn(xsum);
-        const __half lo = __float2half_rn(xsum - __half2float(hi));
-        unsigned char* bn = Bb + (n >> 3) * Sh::sbo + (n & 7) * 16;
-        reinterpret_cast<__half*>(bn + (32 + (jb >> 3)) * kLBO)[jb & 7] = hi;
-        reinterpret_cast<__half*>(bn + (34 + (jb >> 3)) * kLBO)[jb & 7] = lo;
-      }
-    }
-  };
-  if (sA < sB) stage_x(sA, B0);
-
-  // Slice s: decode the weights into A[buf] while x(s) lands in B[buf], then
-  // one thread issues the MMAs.  Right after, once the MMAs of slice s - 1
-  // have released the other buffers, x(s + 1) is staged into them, so its
-  // L2 round trip overlaps the decode of slice s + 1.
-  for (int s = sA; s < sB && ok; ++s) {
-    const int buf = (s - sA) & 1;
-    unsigned char* Ab = A0 + buf * Sh::tileA;
-    unsigned char* Bb = B0 + buf * bbytes;
-    uint4 nx[NP];
-    uint2 nvt = vt;
-    uint32_t npar = par;
+  if (producer) {
+    // ---- x copies and MMAs (the MMAs and TMA copies are issued by lane 0)
+    const uint32_t idesc = idesc_f16(kRows, a.N);
+    auto produce = [&](int i) {                      // x of slice sA + i into stage i % kStages
+      const int st = i % kStages, s = sA + i;
+      const uint32_t fb = saddr(&full[st]);
+      unsigned char* Bs = B0 + st * bbytes;
+      if (a.use_tma) {
+        if (lane == 0) {
+          mbar_expect_tx(fb, 4u * (uint32_t)atom_bytes);
 #pragma unroll
-    for (int k = 0; k < NP; ++k) nx[k] = pl[k];
-    if (valid && s + 1 < sB) load(s + 1, nx, nvt, npar);
-    if (ok) {
-      unsigned char* arow = Ab + (m >> 3) * Sh::sbo + (m & 7) * 16;
+          for (int at = 0; at < 4; ++at) tma_load_2d(saddr(Bs + at * atom_bytes), &a.xmap, s * 256 + 64 * at, 0, fb);
+        }
+      } else {
+        // x rows not 16-byte aligned: element loads by the warp's 32 lanes
+        for (int e = lane; e < a.ntok * 32; e += 32) {
+          const int n = e >> 5, kc = e & 31, c0 = s * 256 + kc * 8;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          __half* hv = reinterpret_cast<__half*>(&v);
+          for (int k = 0; k < 8; ++k)
+            if (c0 + k < a.C) hv[k] = a.x[(size_t)n * a.C + c0 + k];
+          *reinterpret_cast<uint4*>(Bs + (kc >> 3) * atom_bytes + n * 128 + (((kc & 7) ^ (n & 7)) << 4)) = v;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(fb);
+      }
+    };
+    for (int i = 0; i < min(kStages, used); ++i) produce(i);
+    int issued = 0;
+    for (int i = 0; i < used; ++i) {
+      const int st = i % kStages;
+      if (!__all_sync(~0u, mbar_wait(saddr(&full[st]), (uint32_t)(i / kStages) & 1u))) {
+        ok = false;
+        if (lane == 0) atomicExch(&q2_tc_error, 3u);
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t bs = saddr(B0 + st * bbytes);
+        const uint32_t at = tmem + kAcol0 + (uint32_t)st * Sh::acols;
+#pragma unroll
+        for (int k = 0; k < Sh::kmma; ++k)
+          mma_f16_ta(tmem, at + (uint32_t)(k * 8), sdesc_sw128(bs + (k >> 2) * atom_bytes + (k & 3) * 32), idesc,
+                     (i > 0 || k > 0) ? 1u : 0u);
+        mma_commit(saddr(&empty[st]));
+      }
+      __syncwarp();
+      issued = i + 1;
+      // refill the stage of slice i - 1 (its MMAs precede slice i's) with slice i - 1 + kStages
+      const int j = i - 1 + kStages;
+      if (i >= 1 && j < used) {
+        if (!__all_sync(~0u, mbar_wait(saddr(&empty[(i - 1) % kStages]), (uint32_t)((i - 1) / kStages) & 1u))) {
+          ok = false;
+          if (lane == 0) atomicExch(&q2_tc_error, 4u);
+          break;
+        }
+        produce(j);
+      }
+    }
+    // the last commit covers every MMA issued; on an error, also give the
+    // copies in flight time to land before the CTA exits
+    if (issued > 0 && !mbar_wait(saddr(&empty[(issued - 1) % kStages]), (uint32_t)((issued - 1) / kStages) & 1u)) {
+      ok = false;
+      if (lane == 0) atomicExch(&q2_tc_error, 5u);
+    }
+    if (!ok) sleep_us(50);
+  } else {
+    // ---- decode into TMEM
+    for (int i = 0; i < used; ++i) {
+      const int s = sA + i, st = i % kStages;
+      uint4 n2[NP];
+      uint2 v2 = make_uint2(0, 0);
+      uint32_t p2 = 0;
+#pragma unroll
+      for (int k = 0; k < NP; ++k) n2[k] = make_uint4(0, 0, 0, 0);
+      if (valid && i + 2 < used) load(s + 2, n2, v2, p2);
+      // stage st is free once the MMAs of slice i - kStages have completed
+      if (i >= kStages && !__all_sync(~0u, mbar_wait(saddr(&empty[st]), (uint32_t)(i / kStages - 1) & 1u))) {
+        ok = false;
+        if (lane == 0) atomicExch(&q2_tc_error, 6u);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t ta = tlane + kAcol0 + (uint32_t)st * Sh::acols;
       if (FMT == Q2_TRELLIS) {
         const uint32_t W[16] = {pl[0].x, pl[0].y, pl[0].z, pl[0].w, pl[1].x, pl[1].y, pl[1].z, pl[1].w,
                                 pl[2].x, pl[2].y, pl[2].z, pl[2].w, pl[3].x, pl[3].y, pl[3].z, pl[3].w};
-        if (part == 0) trellis_part<0>(W, tab, arow);
-        else if (part == 1) trellis_part<1>(W, tab, arow);
-        else if (kParts > 2 && part == 2) trellis_part<(kParts > 2 ? 2 : 0)>(W, tab, arow);
-        else if (kParts > 2) trellis_part<(kParts > 2 ? 3 : 0)>(W, tab, arow);
+        if (part == 0) trellis_part<0>(W, tab, ta);
+        else trellis_part<1>(W, tab, ta);
+      } else if (FMT == Q2_BPDQ) {
+        const uint32_t tlo = __byte_perm(vt.x, vt.y, 0x6420u);
+        const uint32_t thi = __byte_perm(vt.x, vt.y, 0x7531u);
+        const uint32_t R0[8] = {pl[0].x, pl[0].y, pl[0].z, pl[0].w, pl[1].x, pl[1].y, pl[1].z, pl[1].w};
+        const uint32_t R1[8] = {pl[2].x, pl[2].y, pl[2].z, pl[2].w, pl[3].x, pl[3].y, pl[3].z, pl[3].w};
+        if (part == 0) bpdq_part<0>(R0, R1, lane, tlo, thi, ta);
+        else bpdq_part<1>(R0, R1, lane, tlo, thi, ta);
       } else {
-        const uint32_t rot = (uint32_t)(part * kPartBytes + lane) * kLBO;
-        constexpr int NW = kPartBytes / 4;      // 32-bit words of a plane per lane and part
-        if (FMT == Q2_BPDQ) {
-          const uint32_t tlo = __byte_perm(vt.x, vt.y, 0x6420u);
-          const uint32_t thi = __byte_perm(vt.x, vt.y, 0x7531u);
-          const uint32_t w0[4] = {pl[0].x, pl[0].y, pl[0].z, pl[0].w};
-          const uint32_t w1[4] = {pl[1].x, pl[1].y, pl[1].z, pl[1].w};
+        const uint32_t R0[8] = {pl[0].x, pl[0].y, pl[0].z, pl[0].w, pl[1].x, pl[1].y, pl[1].z, pl[1].w};
+        const uint32_t R1[8] = {pl[2].x, pl[2].y, pl[2].z, pl[2].w, pl[3].x, pl[3].y, pl[3].z, pl[3].w};
+        const uint32_t R2[8] = {pl[4].x, pl[4].y, pl[4].z, pl[4].w, pl[5].x, pl[5].y, pl[5].z, pl[5].w};
+        if (part == 0) {
+          leech_part<0>(R0, R1, R2, lane, ta);
+          // parity columns (K 256..287, TMEM columns 128..143): A = 1.0 where
+          // the block starting in this slice is odd, once for the hi and
+          // once for the lo part of the block sums
+          uint32_t pv[8];
 #pragma unroll
-          for (int j = 0; j < NW; ++j) {
-            const Codes4 c = codes4(w0[j], w1[j]);
-            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 0) * kLBO) & 4095u)) = decode_q<0>(c, tlo, thi);
-            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 1) * kLBO) & 4095u)) = decode_q<1>(c, tlo, thi);
-            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 2) * kLBO) & 4095u)) = decode_q<2>(c, tlo, thi);
-            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 3) * kLBO) & 4095u)) = decode_q<3>(c, tlo, thi);
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t lo = ((par >> (2 * q)) & 1u) ? 0x3C00u : 0u;
+            const uint32_t hi = ((par >> (2 * q + 1)) & 1u) ? 0x3C000000u : 0u;
+            pv[q] = lo | hi;
           }
+          const uint4 q0 = make_uint4(pv[0], pv[1], pv[2], pv[3]), q1 = make_uint4(pv[4], pv[5], pv[6], pv[7]);
+          tmem_st16(ta + 128u, q0, q1, q0, q1);
         } else {
-          const uint32_t w0[4] = {pl[0].x, pl[0].y, pl[0].z, pl[0].w};
-          const uint32_t w1[4] = {pl[1].x, pl[1].y, pl[1].z, pl[1].w};
-          const uint32_t w2[4] = {pl[2].x, pl[2].y, pl[2].z, pl[2].w};
-#pragma unroll
-          for (int j = 0; j < NW; ++j) {
-            const Codes4 c = codes4x3(w0[j], w1[j], w2[j]);
-            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 0) * kLBO) & 4095u)) = decode_leech_q<0>(c);
-            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 1) * kLBO) & 4095u)) = decode_leech_q<1>(c);
-            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 2) * kLBO) & 4095u)) = decode_leech_q<2>(c);
-            *reinterpret_cast<uint4*>(arow + ((rot + (4 * j + 3) * kLBO) & 4095u)) = decode_leech_q<3>(c);
-          }
-          if (part == 0) {
-            // parity columns: A = 1.0 where the block starting in this slice is odd
-            uint32_t pv[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const uint32_t lo = ((par >> (2 * q)) & 1u) ? 0x3C00u : 0u;
-              const uint32_t hi = ((par >> (2 * q + 1)) & 1u) ? 0x3C000000u : 0u;
-              pv[q] = lo | hi;
-            }
-            const uint4 p0 = make_uint4(pv[0], pv[1], pv[2], pv[3]), p1 = make_uint4(pv[4], pv[5], pv[6], pv[7]);
-            *reinterpret_cast<uint4*>(arow + 32 * kLBO) = p0;
-            *reinterpret_cast<uint4*>(arow + 33 * kLBO) = p1;
-            *reinterpret_cast<uint4*>(arow + 34 * kLBO) = p0;
-            *reinterpret_cast<uint4*>(arow + 35 * kLBO) = p1;
-          }
+          leech_part<1>(R0, R1, R2, lane, ta);
         }
-      }
-    }
-    cp_async_wait_all();
-    fence_async_smem();
-    tc_fence_before();
-    ok = __syncthreads_and(ok);
-    tc_fence_after();
-    if (threadIdx.x == 0 && ok) {
-      const uint32_t aa = saddr(Ab), bb = saddr(Bb);
+        // B side of the parity columns (atom 4): block sums of x for the
+        // blocks starting in this slice, hi part at K 256 + jb, lo part
+        // (sum - hi) at K 272 + jb
+        const int bfirst = (s * 256 + 23) / 24;
+        const int blast = min(a.nblock - 1, (s * 256 + 256 + 23) / 24 - 1);
+        const int nbk = max(0, blast - bfirst + 1);
+        unsigned char* Bp = B0 + st * bbytes + 4 * atom_bytes;
+        for (int e = threadIdx.x; e < a.ntok * 16; e += kDecWarps * 32) {
+          const int n = e >> 4, jb = e & 15;
+          float xsum = 0.f;
+          if (jb < nbk) {
+            const __half* xp = a.x + (size_t)n * a.C + (size_t)(bfirst + jb) * 24;
+            if (a.use_tma) {                         // 48-byte blocks of 16-byte aligned rows
+              const uint4* xv = reinterpret_cast<const uint4*>(xp);
 #pragma unroll
-      for (int k = 0; k < Sh::kch / 2; ++k)
-        mma_f16(tmem, sdesc_s(aa + k * 2 * kLBO, Sh::sbo), sdesc_s(bb + k * 2 * kLBO, Sh::sbo), idesc,
-                (s > sA || k > 0) ? 1u : 0u);
-      mma_commit(saddr(&bars[buf]));
-    }
-    if (ok && s + 1 < sB) {
-      const int nb = buf ^ 1;
-      if (s > sA && !mbar_wait(saddr(&bars[nb]), (uint32_t)((s - 1 - sA) >> 1) & 1u)) {
-        ok = false;
-        if (threadIdx.x == 0) atomicExch(&q2_tc_error, 1u);
-      }
-      if (ok) stage_x(s + 1, B0 + nb * bbytes);
-    }
+              for (int k = 0; k < 3; ++k) {
+                const uint4 r = __ldg(xv + k);
+                const __half2* h2 = reinterpret_cast<const __half2*>(&r);
 #pragma unroll
-    for (int k = 0; k < NP; ++k) pl[k] = nx[k];
-    vt = nvt;
-    par = npar;
-  }
-  const int used = sB - sA;
-  if (ok && used > 0) {
-    const int last = used - 1;
-    if (!mbar_wait(saddr(&bars[last & 1]), (uint32_t)(last >> 1) & 1u)) ok = false;
-    if (ok && used > 1 && !mbar_wait(saddr(&bars[(last - 1) & 1]), (uint32_t)((last - 1) >> 1) & 1u)) ok = false;
-    if (!ok && threadIdx.x == 0) atomicExch(&q2_tc_error, 2u);
+                for (int m = 0; m < 4; ++m) {
+                  const float2 f = __half22float2(h2[m]);
+                  xsum += f.x + f.y;
+                }
+              }
+            } else {
+              for (int k = 0; k < 24; ++k) xsum += __half2float(xp[k]);
+            }
+          }
+          const __half hi = __float2half_rn(xsum);
+          const __half lo = __float2half_rn(xsum - __half2float(hi));
+          unsigned char* rp = Bp + n * 128 + (jb & 7) * 2;
+          *reinterpret_cast<__half*>(rp + ((((jb >> 3) + 0) ^ (n & 7)) << 4)) = hi;
+          *reinterpret_cast<__half*>(rp + ((((jb >> 3) + 2) ^ (n & 7)) << 4)) = lo;
+        }
+        fence_async_smem();
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(saddr(&full[st]));
+#pragma unroll
+      for (int k = 0; k < NP; ++k) {
+        pl[k] = n1[k];
+        n1[k] = n2[k];
+      }
+      vt = v1;
+      v1 = v2;
+      par = p1;
+      p1 = p2;
+    }
+    // the accumulator is final once the last slice's commit has arrived
+    if (ok && warp < 4 && used > 0 &&
+        !__all_sync(~0u, mbar_wait(saddr(&empty[(used - 1) % kStages]), (uint32_t)((used - 1) / kStages) & 1u))) {
+      ok = false;
+      if (lane == 0) atomicExch(&q2_tc_error, 2u);
+    }
   }
   ok = __syncthreads_and(ok);
   tc_fence_after();
@@ -444,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(TcArgs a) {
     const int orow = (tile * 4 + warp) * 32 + lane;
     for (int c0 = 0; c0 < a.N; c0 += 16) {
       float v[16];
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+      tmem_ld16(tlane + (uint32_t)c0, v);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int t = c0 + i;
@@ -461,7 +592,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(TcArgs a) {
   tc_fence_before();
   __syncthreads();
   if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once (null if absent).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      (void)cudaGetLastError();
+      p = nullptr;
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// Tensor map of x [ntok][C] fp16 for the B tiles: box of 64 columns (128
+// bytes, the swizzle span) x N token rows, rows past ntok and columns past C
+// read as zero.  False when the rows are not 16-byte aligned or the driver
+// refuses the map; the kernel then stages x with element loads.
+bool encode_x_map(CUtensorMap* map, const void* x, int C, int ntok, int N) {
+  if (C % 8 || (reinterpret_cast<uintptr_t>(x) & 15)) return false;
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)ntok};
+  const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)N};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Packed formats at 2..64 tokens on the tensor cores (tokens padded to a
@@ -508,7 +671,9 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
       a.nsplit = ns;
     }
   }
-  const int smem = Sh::table + 2 * Sh::tileA + 2 * (a.N / 8) * (int)Sh::sbo + 64;
+  a.use_tma = encode_x_map(&a.xmap, x, d.C, ntok, a.N) ? 1 : 0;
+  // table, 1024-byte alignment slack, kStages B buffers, 2 x kStages mbarriers, TMEM slot
+  const int smem = max(kOneCtaSmem, Sh::table + 1024 + kStages * Sh::atoms * a.N * 128 + 2 * kStages * 8 + 16);
   int st = launch_pdl(k_tc<FMT>, a, a.ntile * a.nsplit, kThreads, smem, stream);
   if (st) return st;
   if (a.nsplit == 1 && FMT == Q2_BPDQ) return Q2_OK;

@@ -102,6 +102,22 @@ def test_bpdq_decode_bit_exact(q2):
     assert np.array_equal(w.view(np.uint16), obpdq.decode_fp16(d["plane0"], d["plane1"], d["coef"]).view(np.uint16))
 
 
+@pytest.mark.parametrize("ntok", [16, 64])
+def test_bpdq_tensor_path_one_hot_columns_bit_exact(q2, ntok):
+    # x[t] = e_{c_t}: y[t][r] = w[r][c_t] exactly (one nonzero product, fp32
+    # accumulation, fp16 result).  The columns c_t cover every column-byte
+    # position of a slice and every bit of a byte, in several slices, so a
+    # wrong byte or word of the lane un-rotation shows up as a mismatch.
+    R, C = 300, 256 * 9
+    d = synth.bpdq(R, C, 9100 + ntok)
+    w16 = obpdq.decode_fp16(d["plane0"], d["plane1"], d["coef"])
+    cols = [(t % 9) * 256 + ((t * 37) % 32) * 8 + (t * 5) % 8 for t in range(ntok)]
+    x = np.zeros((ntok, C), dtype=np.float16)
+    x[np.arange(ntok), cols] = 1.0
+    _, y = _run(q2, q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]), x)
+    assert np.array_equal(y.view(np.uint16), w16[:, cols].T.view(np.uint16))
+
+
 def test_bpdq_deterministic_and_repeatable(q2):
     d = synth.bpdq(4096, 4096, 1001)
     x = torch.from_numpy(synth.activations(1, 4096, 1001)).cuda()
