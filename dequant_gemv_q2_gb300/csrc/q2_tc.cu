@@ -3,23 +3,26 @@
 // multiply for every token.
 //
 // A CTA owns 128 output rows (four 32-row blocks) and a range of 256-column
-// slices, and runs them through a ring of kStages stages with three roles:
-//   - 8 decoder warps turn the packed weights of the 128 x 256 tile into
-//     fp16 in registers (BPDQ through the per-(group, row) 4-entry value
-//     table, one byte permute per two or four weights) and store them into
-//     tensor memory with tcgen05.st, one TMEM lane per row (the stage's A);
-//   - one producer lane of the ninth warp loads the x tile of all tokens into
-//     shared memory with four 2D TMA copies (the stage's B);
-//   - the same lane, once a stage's A and B are both complete (one mbarrier
-//     per stage: 8 decoder arrivals plus the TMA bytes), issues sixteen
-//     tcgen05.mma.kind::f16 (M = 128, N, K = 16) reading A from TMEM and B
-//     from shared memory into one fp32 accumulator in TMEM, and commits them
-//     to the stage's "empty" mbarrier, which frees the stage for refilling.
-// No role waits for another except through these barriers, so the decode of
-// slice s + 1, the x copy of slice s + 2 and the MMAs of slice s overlap.
-// At the end the decoder warps read the accumulator (each its 32 TMEM
-// lanes) and write fp32 partial sums for the split-K reduction kernel, or y
-// directly.
+// slices, and runs them through rings of stages with three roles:
+//   - 16 decoder warps (four per 32-row block, each a quarter of the slice's
+//     columns) turn the packed weights into fp16 in registers (BPDQ through
+//     the per-(group, row) 4-entry value table, one byte permute per two or
+//     four weights) and store them into tensor memory with tcgen05.st, one
+//     TMEM lane per row: the slice's A, in one of kStagesA TMEM stages;
+//   - a helper warp copies the x tile of all tokens into one of kStagesB
+//     shared-memory stages with four 2D TMA copies (the slice's B), waits
+//     until a slice's A and B are complete, and hands the slice to
+//   - the MMA warp, whose lane 0 issues sixteen tcgen05.mma.kind::f16
+//     (M = 128, N, K = 16) reading A from TMEM and B from shared memory into
+//     one fp32 accumulator in TMEM, and commits them to the stages' "empty"
+//     mbarriers, which free the stages for refilling.
+// The handoff is a named barrier with a flag reduction, not a memory
+// access: any memory access by the issuing thread waits for its queue of
+// MMAs to drain and leaves the tensor core idle (about 350 cycles per
+// access on GB300), so the MMA lane touches no memory at all.
+// At the end the decoder warps of the first 32-row quarter group read the
+// accumulator (each its 32 TMEM lanes) and write fp32 partial sums for the
+// split-K reduction kernel, or y directly.
 //
 // TMEM columns (all 512 are allocated; one CTA per SM): D at 0 .. N - 1,
 // A of stage st at kAcol0 + st * (4 x K chunks); A column j of a lane holds
@@ -33,13 +36,13 @@
 //
 // The BPDQ and Leech planes are stored lane-rotated for the batch-1 kernels
 // (byte j of lane l's 32-byte plane row holds column-byte (j + l) mod 32).
-// Every lane loads its whole rows and undoes the rotation in registers
-// before decoding, because a TMEM store writes the same columns in every
-// lane.
+// A TMEM store writes the same columns in every lane, so each lane undoes
+// its rotation: the word part through per-lane load addresses, the byte
+// part with a funnel shift.
 //
 // Every wait is bounded: a wait that runs out records an error code in
 // q2_tc_error (read back with q2_device_errors) and the kernel skips the
-// rest of its work; the producer lane waits for its outstanding copies and
+// rest of its work; the helper warp waits for the outstanding copies and
 // MMAs before the CTA frees its TMEM columns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -55,12 +58,17 @@ __device__ unsigned int q2_tc_error = 0;
 namespace q2 {
 namespace {
 
-constexpr int kDecWarps = 8;                  // decoder warps; one more warp copies x and issues MMAs
-constexpr int kThreads = (kDecWarps + 1) * 32;
-constexpr int kStages = 3;                    // slices in flight (A in TMEM, B in shared memory)
+constexpr int kDecWarps = 16;                 // decoder warps
+constexpr int kMmaWarp = kDecWarps;           // lane 0 issues the MMAs
+constexpr int kHelperWarp = kDecWarps + 1;    // waits on the stage barriers, issues the x copies
+constexpr int kThreads = (kDecWarps + 2) * 32;
+constexpr int kStagesA = 3;                   // slices in flight in TMEM (decoded A)
+constexpr int kStagesB = 4;                   // slices in flight in shared memory (x tiles)
+constexpr int kGroup = 2;                     // slices per handoff to the MMA warp
+static_assert(kStagesB % kGroup == 0 && kStagesB / kGroup == 2, "B stages are freed a group at a time");
 constexpr int kParts = kDecWarps / 4;         // warps per 32-row block, each decoding 256/kParts columns
 constexpr int kPartBytes = 32 / kParts;       // column-bytes of one plane per lane and part
-static_assert(kParts == 2, "the decode splits a row's 32 column-bytes between two warps");
+constexpr int kPartWords = kPartBytes / 4;    // canonical 32-bit words of one plane per lane and part
 constexpr int kRows = 128;                    // M of the MMA
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAcol0 = 64;               // D takes TMEM columns 0..63
@@ -98,26 +106,18 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, uint4 a, uint4 b, uint
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// Canonical words 4P .. 4P + 3 (column-bytes 16P .. 16P + 15) of one plane
-// row from its 8 lane-rotated words R (rotated byte j = column-byte
-// (j + lane) mod 32).  With lane = 4a + r, canonical word c starts at
-// rotated byte 4(c - a) - r: the word rotation by a runs as three
-// conditional rotations by 1, 2 and 4 words, the byte offset r as a funnel
-// shift (clamped: r = 0 takes the high word whole).
-template <int P>
-__device__ __forceinline__ void unrotate_half(const uint32_t (&R)[8], int lane, uint32_t (&cw)[4]) {
-  const int a = lane >> 2;
-  const uint32_t sh = 32u - 8u * (uint32_t)(lane & 3);
-  uint32_t t[8], u[8], v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) t[i] = (a & 1) ? R[(i + 7) & 7] : R[i];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) u[i] = (a & 2) ? t[(i + 6) & 7] : t[i];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = (a & 4) ? u[(i + 4) & 7] : u[i];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) cw[c] = __funnelshift_rc(v[(4 * P + c + 7) & 7], v[4 * P + c], sh);
-}
+// Lane un-rotation.  Lane l = 4a + r stores its 32-byte plane row rotated:
+// rotated byte j holds column-byte (j + l) mod 32, so canonical word c
+// starts at rotated byte 4(c - a) - r.  A lane decoding canonical words
+// c0 .. c0 + n - 1 loads the n + 1 rotated words L[t] = R[(c0 - 1 + t - a)
+// mod 8] (the word rotation is in the load addresses, see rot_word_offset)
+// and joins neighbours with a funnel shift by 32 - 8r (clamped: r = 0 takes
+// the high word whole).
+__device__ __forceinline__ uint32_t unrot(uint32_t lo, uint32_t hi, uint32_t sh) { return __funnelshift_rc(lo, hi, sh); }
+
+// Byte offset, inside the lane's part of an item (after lane * 16), of
+// rotated word w of plane q: half w / 4 of the plane is chunk 2q + w / 4.
+__device__ __forceinline__ int rot_word_offset(int q, int w) { return (2 * q + (w >> 2)) * 512 + (w & 3) * 4; }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -228,7 +228,7 @@ struct TcShape {
   static constexpr int item = FMT == Q2_BPDQ ? Q2_ITEM_BYTES_BPDQ : FMT == Q2_TRELLIS ? Q2_ITEM_BYTES_TRL
                                                                                      : Q2_ITEM_BYTES_LEECH;
 };
-static_assert(kAcol0 + kStages * TcShape<Q2_LEECH>::acols <= kTmemCols, "A stages exceed TMEM");
+static_assert(kAcol0 + kStagesA * TcShape<Q2_LEECH>::acols <= kTmemCols, "A stages exceed TMEM");
 
 // Shared-memory matrix descriptor (tcgen05) of a K-major operand with the
 // 128-byte swizzle: start >> 4 in bits 0-13, leading byte offset field 1
@@ -270,87 +270,99 @@ __device__ __forceinline__ uint4 decode_leech_q(const Codes4& c) {
   return r;
 }
 
-// Trellis: steps (128/kParts)*H .. of a segment -> columns (256/kParts)*H ..
-// of the A row (column-byte = step / 4, four TMEM columns per column-byte);
-// H is a template parameter so every window index is static.
-template <int H>
-__device__ __forceinline__ void trellis_part(const uint32_t (&W)[16], const uint32_t* tab, uint32_t ta) {
+// Trellis: the 32 steps of one part of a segment (column-bytes 8H .. 8H + 7
+// of the A row, four TMEM columns per column-byte).  Lw holds the part's
+// window of the lane's 16 symbol words, Lw[t] = W[(12 - 4H + t) mod 16]:
+// step 32H + kk reads words ((127 - kk) >> 3) - 12 and the next one of Lw,
+// indices that do not depend on H.
+__device__ __forceinline__ void trellis_part(const uint32_t (&Lw)[5], const uint32_t* tab, uint32_t ta) {
 #pragma unroll
   for (int g = 0; g < kPartBytes / 4; ++g) {
     uint32_t e[16];
 #pragma unroll
     for (int t = 0; t < 16; ++t) {
-      const int k = H * kPartBytes * 4 + g * 16 + t;
-      const int n = 127 - k;
-      const uint32_t f = __funnelshift_r(W[n >> 3], W[((n >> 3) + 1) & 15], 4 * (n & 7));
+      const int kk = g * 16 + t;
+      const int n = 127 - kk;
+      const uint32_t f = __funnelshift_r(Lw[(n >> 3) - 12], Lw[(n >> 3) - 11], 4 * (n & 7));
       e[t] = tab[(f * kHashHi) >> 20] ^ ((f & 1u) ? 0x80008000u : 0u);
     }
-    tmem_st16(ta + (uint32_t)(H * kPartBytes + g * 4) * 4u, e);
+    tmem_st16(ta + (uint32_t)(g * 16), e);
   }
 }
 
-// BPDQ: column-bytes 16P .. 16P + 15 of one row (planes R0, R1 as loaded,
-// lane-rotated) into TMEM columns 64P .. 64P + 63 at ta.
-template <int P>
-__device__ __forceinline__ void bpdq_part(const uint32_t (&R0)[8], const uint32_t (&R1)[8], int lane, uint32_t tlo,
-                                          uint32_t thi, uint32_t ta) {
-  uint32_t c0[4], c1[4];
-  unrotate_half<P>(R0, lane, c0);
-  unrotate_half<P>(R1, lane, c1);
+// BPDQ: the part's kPartBytes column-bytes of one row from the loaded
+// rotated words of planes 0 and 1, into TMEM columns from ta.
+__device__ __forceinline__ void bpdq_part(const uint32_t (&L0)[kPartWords + 1], const uint32_t (&L1)[kPartWords + 1],
+                                          uint32_t sh, uint32_t tlo, uint32_t thi, uint32_t ta) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const Codes4 c = codes4(c0[j], c1[j]);
-    tmem_st16(ta + (uint32_t)(64 * P + 16 * j), decode_q<0>(c, tlo, thi), decode_q<1>(c, tlo, thi),
-              decode_q<2>(c, tlo, thi), decode_q<3>(c, tlo, thi));
+  for (int j = 0; j < kPartWords; ++j) {
+    const Codes4 c = codes4(unrot(L0[j], L0[j + 1], sh), unrot(L1[j], L1[j + 1], sh));
+    tmem_st16(ta + (uint32_t)(16 * j), decode_q<0>(c, tlo, thi), decode_q<1>(c, tlo, thi), decode_q<2>(c, tlo, thi),
+              decode_q<3>(c, tlo, thi));
   }
 }
 
 // Leech: the same for the three sign/magnitude planes (values 2u).
-template <int P>
-__device__ __forceinline__ void leech_part(const uint32_t (&R0)[8], const uint32_t (&R1)[8], const uint32_t (&R2)[8],
-                                           int lane, uint32_t ta) {
-  uint32_t c0[4], c1[4], c2[4];
-  unrotate_half<P>(R0, lane, c0);
-  unrotate_half<P>(R1, lane, c1);
-  unrotate_half<P>(R2, lane, c2);
+__device__ __forceinline__ void leech_part(const uint32_t (&L0)[kPartWords + 1], const uint32_t (&L1)[kPartWords + 1],
+                                           const uint32_t (&L2)[kPartWords + 1], uint32_t sh, uint32_t ta) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const Codes4 c = codes4x3(c0[j], c1[j], c2[j]);
-    tmem_st16(ta + (uint32_t)(64 * P + 16 * j), decode_leech_q<0>(c), decode_leech_q<1>(c), decode_leech_q<2>(c),
+  for (int j = 0; j < kPartWords; ++j) {
+    const Codes4 c = codes4x3(unrot(L0[j], L0[j + 1], sh), unrot(L1[j], L1[j + 1], sh), unrot(L2[j], L2[j + 1], sh));
+    tmem_st16(ta + (uint32_t)(16 * j), decode_leech_q<0>(c), decode_leech_q<1>(c), decode_leech_q<2>(c),
               decode_leech_q<3>(c));
   }
+}
+
+// Named barrier 1 between the MMA warp and the helper warp, with an AND of a
+// flag: no memory access, so the MMA lane's queue of tensor-core
+// instructions is not drained by the handoff.
+__device__ __forceinline__ bool handoff(bool in) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, 1, 64, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(in ? 1u : 0u)
+      : "memory");
+  return r != 0;
 }
 
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcArgs a) {
   using Sh = TcShape<FMT>;
   uint32_t* tab = reinterpret_cast<uint32_t*>(q2_smem);            // trellis table
-  // kStages B buffers from the first 1024-byte boundary after the table
+  // kStagesB B buffers from the first 1024-byte boundary after the table
   const uint32_t sbase = saddr(q2_smem);
   unsigned char* B0 = q2_smem + (((sbase + Sh::table + 1023u) & ~1023u) - sbase);
   const int atom_bytes = a.N * 128;
   const int bbytes = Sh::atoms * atom_bytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(B0 + kStages * bbytes);
-  uint64_t* empty = full + kStages;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(empty + kStages);
+  uint64_t* fullA = reinterpret_cast<uint64_t*>(B0 + kStagesB * bbytes);   // decoder arrivals
+  uint64_t* emptyA = fullA + kStagesA;                                      // MMA commits
+  uint64_t* fullB = emptyA + kStagesA;                                      // TMA bytes
+  uint64_t* emptyG = fullB + kStagesB;        // MMA commits per group: the group's B stages are free
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(emptyG + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool producer = warp == kDecWarps;
-  const int rbl = warp & 3, part = (warp >> 2) & 1;  // row block in tile (= TMEM lane quarter), half of the slice
+  const bool decoder = warp < kDecWarps;
+  const int rbl = warp & 3, part = (warp >> 2) & (kParts - 1);   // row block in tile (= TMEM lane quarter), part of the slice
   const int tile = blockIdx.x % a.ntile, split = blockIdx.x / a.ntile;
   const int sA = split * a.S / a.nsplit, sB = (split + 1) * a.S / a.nsplit;
   const int used = sB - sA;
   const int rb = tile * 4 + rbl;
-  const bool valid = !producer && rb < a.nrb;        // the last tile may be ragged
+  const bool valid = decoder && rb < a.nrb;          // the last tile may be ragged
   const int row = rb * 32 + lane;
   const int tile_rbs = min(4, a.nrb - tile * 4);
 
   if (threadIdx.x == 0) {
     for (int s = sA; s < sB; ++s)
       prefetch_l2(a.bits + ((size_t)s * a.nrb + tile * 4) * Sh::item, (size_t)tile_rbs * Sh::item);
-    for (int st = 0; st < kStages; ++st) {
-      mbar_init(saddr(&full[st]), kDecWarps + 1);
-      mbar_init(saddr(&empty[st]), 1);
+    for (int st = 0; st < kStagesA; ++st) {
+      mbar_init(saddr(&fullA[st]), kDecWarps);
+      mbar_init(saddr(&emptyA[st]), 1);
     }
+    for (int st = 0; st < kStagesB; ++st) mbar_init(saddr(&fullB[st]), 1);
+    for (int st = 0; st < 2; ++st) mbar_init(saddr(&emptyG[st]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -361,28 +373,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
   }
   if (FMT == Q2_TRELLIS)
     for (int i = threadIdx.x; i < 4096; i += kThreads) tab[i] = a.table[i];
-  // zero the B buffers once: token rows past ntok of the Leech parity atom
-  // (and of every atom when x is staged without TMA) stay zero
-  for (int i = threadIdx.x; i < kStages * bbytes / 16; i += kThreads)
-    reinterpret_cast<uint4*>(B0)[i] = make_uint4(0, 0, 0, 0);
+  // zero what the TMA does not write: the Leech parity atom (token rows past
+  // ntok stay zero), or every atom when x is staged without TMA
+  {
+    const int z0 = a.use_tma ? 4 * atom_bytes : 0;
+    for (int st = 0; st < kStagesB; ++st)
+      for (int i = threadIdx.x * 16 + z0; i < bbytes; i += kThreads * 16)
+        *reinterpret_cast<uint4*>(B0 + st * bbytes + i) = make_uint4(0, 0, 0, 0);
+  }
   fence_async_smem();
 
-  // per-lane payload of one slice: the whole 512-byte chunks of the item at
-  // this lane (BPDQ / Leech: chunk 2p + h = half h of plane p, lane-rotated;
-  // trellis: the 64-byte packet); plus BPDQ's value table / Leech's parity
-  constexpr int NP = FMT == Q2_LEECH ? 6 : 4;
-  uint4 pl[NP], n1[NP];
+  // Decoder payload of one slice: the rotated words this lane's part needs
+  // (BPDQ / Leech: kPartWords + 1 per plane; trellis: a 5-word window of the
+  // 64-byte symbol packet), at per-lane offsets fixed for the whole kernel;
+  // plus BPDQ's value table / Leech's parity word.
+  constexpr int NPL = FMT == Q2_BPDQ ? 2 : FMT == Q2_LEECH ? 3 : 0;
+  constexpr int NW = FMT == Q2_TRELLIS ? 5 : NPL * (kPartWords + 1);
+  int off[NW];
+  {
+    const int aa = lane >> 2;
+    if (FMT == Q2_TRELLIS) {
+#pragma unroll
+      for (int t = 0; t < 5; ++t) {
+        const int w = (12 - 4 * part + t) & 15;
+        off[t] = (w >> 2) * 512 + (w & 3) * 4;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < NPL; ++q)
+#pragma unroll
+        for (int t = 0; t <= kPartWords; ++t)
+          off[q * (kPartWords + 1) + t] = rot_word_offset(q, (kPartWords * part - 1 + t - aa) & 7);
+    }
+  }
+  uint32_t pl[NW], n1[NW];
   uint2 vt = make_uint2(0, 0), v1 = make_uint2(0, 0);
   uint32_t par = 0, p1 = 0;
-  auto load = [&](int s, uint4 (&d)[NP], uint2& v, uint32_t& pw) {
+  auto load = [&](int s, uint32_t (&d)[NW], uint2& v, uint32_t& pw) {
     const unsigned char* ip = a.bits + ((size_t)s * a.nrb + rb) * Sh::item + lane * 16;
 #pragma unroll
-    for (int k = 0; k < NP; ++k) d[k] = __ldg(reinterpret_cast<const uint4*>(ip + k * 512));
+    for (int t = 0; t < NW; ++t) d[t] = __ldg(reinterpret_cast<const uint32_t*>(ip + off[t]));
     if (FMT == Q2_BPDQ) v = a.vtab[(size_t)s * a.Rpad + row];
     if (FMT == Q2_LEECH) pw = a.parity[(size_t)s * a.Rpad + row];
   };
 #pragma unroll
-  for (int k = 0; k < NP; ++k) pl[k] = n1[k] = make_uint4(0, 0, 0, 0);
+  for (int t = 0; t < NW; ++t) pl[t] = n1[t] = 0;
   if (valid && used > 0) load(sA, pl, vt, par);
   if (valid && used > 1) load(sA + 1, n1, v1, p1);
   pdl_wait();
@@ -394,13 +429,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
   const uint32_t tlane = tmem + ((uint32_t)(rbl * 32) << 16);     // this warp's lane quarter
   bool ok = true;
 
-  if (producer) {
-    // ---- x copies and MMAs (the MMAs and TMA copies are issued by lane 0)
+  if (warp == kMmaWarp) {
+    // ---- MMAs: one handoff per group of kGroup slices, then lane 0 issues
+    // and commits (per slice for its A stage, per group for its B stages)
     const uint32_t idesc = idesc_f16(kRows, a.N);
-    auto produce = [&](int i) {                      // x of slice sA + i into stage i % kStages
-      const int st = i % kStages, s = sA + i;
-      const uint32_t fb = saddr(&full[st]);
-      unsigned char* Bs = B0 + st * bbytes;
+    for (int g = 0; g * kGroup < used; ++g) {
+      ok = handoff(ok);
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) {
+          const int i = g * kGroup + u;
+          if (i < used) {
+            const int sa = i % kStagesA, sb = i % kStagesB;
+            const uint32_t bs = saddr(B0 + sb * bbytes);
+            const uint32_t at = tmem + kAcol0 + (uint32_t)sa * Sh::acols;
+#pragma unroll
+            for (int k = 0; k < Sh::kmma; ++k)
+              mma_f16_ta(tmem, at + (uint32_t)(k * 8), sdesc_sw128(bs + (k >> 2) * atom_bytes + (k & 3) * 32), idesc,
+                         (i > 0 || k > 0) ? 1u : 0u);
+            mma_commit(saddr(&emptyA[sa]));
+          }
+        }
+        mma_commit(saddr(&emptyG[g & 1]));
+      }
+      __syncwarp();
+    }
+  } else if (warp == kHelperWarp) {
+    // ---- stage barriers and x copies (TMA issued by lane 0)
+    auto produce = [&](int i) {                      // x of slice sA + i into B stage i % kStagesB
+      const int sb = i % kStagesB, s = sA + i;
+      const uint32_t fb = saddr(&fullB[sb]);
+      unsigned char* Bs = B0 + sb * bbytes;
       if (a.use_tma) {
         if (lane == 0) {
           mbar_expect_tx(fb, 4u * (uint32_t)atom_bytes);
@@ -422,84 +483,90 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
         if (lane == 0) mbar_arrive(fb);
       }
     };
-    for (int i = 0; i < min(kStages, used); ++i) produce(i);
-    int issued = 0;
-    for (int i = 0; i < used; ++i) {
-      const int st = i % kStages;
-      if (!__all_sync(~0u, mbar_wait(saddr(&full[st]), (uint32_t)(i / kStages) & 1u))) {
+    for (int i = 0; i < min(kStagesB, used); ++i) produce(i);
+    int handed = 0;
+    for (int g = 0; g * kGroup < used; ++g) {
+      bool ready = true;
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) {
+        const int i = g * kGroup + u;
+        if (ready && i < used)
+          ready = mbar_wait(saddr(&fullA[i % kStagesA]), (uint32_t)(i / kStagesA) & 1u) &&
+                  mbar_wait(saddr(&fullB[i % kStagesB]), (uint32_t)(i / kStagesB) & 1u);
+      }
+      if (!__all_sync(~0u, ready)) {
         ok = false;
         if (lane == 0) atomicExch(&q2_tc_error, 3u);
-        break;
       }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t bs = saddr(B0 + st * bbytes);
-        const uint32_t at = tmem + kAcol0 + (uint32_t)st * Sh::acols;
-#pragma unroll
-        for (int k = 0; k < Sh::kmma; ++k)
-          mma_f16_ta(tmem, at + (uint32_t)(k * 8), sdesc_sw128(bs + (k >> 2) * atom_bytes + (k & 3) * 32), idesc,
-                     (i > 0 || k > 0) ? 1u : 0u);
-        mma_commit(saddr(&empty[st]));
-      }
-      __syncwarp();
-      issued = i + 1;
-      // refill the stage of slice i - 1 (its MMAs precede slice i's) with slice i - 1 + kStages
-      const int j = i - 1 + kStages;
-      if (i >= 1 && j < used) {
-        if (!__all_sync(~0u, mbar_wait(saddr(&empty[(i - 1) % kStages]), (uint32_t)((i - 1) / kStages) & 1u))) {
+      tc_fence_before();
+      ok = handoff(ok);
+      if (!ok) break;
+      handed = min(used, (g + 1) * kGroup);
+      // refill the B stages of group g - 1 (its MMAs precede group g's) with the slices kStagesB later
+      const int j0 = (g - 1) * kGroup + kStagesB;
+      if (g >= 1 && j0 < used) {
+        if (!__all_sync(~0u, mbar_wait(saddr(&emptyG[(g - 1) & 1]), (uint32_t)((g - 1) >> 1) & 1u))) {
           ok = false;
           if (lane == 0) atomicExch(&q2_tc_error, 4u);
-          break;
         }
-        produce(j);
+        if (ok)
+          for (int u = 0; u < kGroup && j0 + u < used; ++u) produce(j0 + u);
       }
     }
     // the last commit covers every MMA issued; on an error, also give the
     // copies in flight time to land before the CTA exits
-    if (issued > 0 && !mbar_wait(saddr(&empty[(issued - 1) % kStages]), (uint32_t)((issued - 1) / kStages) & 1u)) {
+    if (handed > 0 &&
+        !mbar_wait(saddr(&emptyA[(handed - 1) % kStagesA]), (uint32_t)((handed - 1) / kStagesA) & 1u)) {
       ok = false;
       if (lane == 0) atomicExch(&q2_tc_error, 5u);
     }
     if (!ok) sleep_us(50);
   } else {
-    // ---- decode into TMEM
+    // ---- decoders: slice i into A stage i % kStagesA
+    const uint32_t sh = 32u - 8u * (uint32_t)(lane & 3);
     for (int i = 0; i < used; ++i) {
-      const int s = sA + i, st = i % kStages;
-      uint4 n2[NP];
+      const int s = sA + i, sa = i % kStagesA;
+      uint32_t n2[NW];
       uint2 v2 = make_uint2(0, 0);
       uint32_t p2 = 0;
 #pragma unroll
-      for (int k = 0; k < NP; ++k) n2[k] = make_uint4(0, 0, 0, 0);
+      for (int t = 0; t < NW; ++t) n2[t] = 0;
       if (valid && i + 2 < used) load(s + 2, n2, v2, p2);
-      // stage st is free once the MMAs of slice i - kStages have completed
-      if (i >= kStages && !__all_sync(~0u, mbar_wait(saddr(&empty[st]), (uint32_t)(i / kStages - 1) & 1u))) {
+      // the stage is free once the MMAs of slice i - kStagesA have completed
+      if (i >= kStagesA &&
+          !__all_sync(~0u, mbar_wait(saddr(&emptyA[sa]), (uint32_t)(i / kStagesA - 1) & 1u))) {
         ok = false;
         if (lane == 0) atomicExch(&q2_tc_error, 6u);
         break;
       }
       tc_fence_after();
-      const uint32_t ta = tlane + kAcol0 + (uint32_t)st * Sh::acols;
+      const uint32_t ta = tlane + kAcol0 + (uint32_t)sa * Sh::acols + (uint32_t)(32 * part);
       if (FMT == Q2_TRELLIS) {
-        const uint32_t W[16] = {pl[0].x, pl[0].y, pl[0].z, pl[0].w, pl[1].x, pl[1].y, pl[1].z, pl[1].w,
-                                pl[2].x, pl[2].y, pl[2].z, pl[2].w, pl[3].x, pl[3].y, pl[3].z, pl[3].w};
-        if (part == 0) trellis_part<0>(W, tab, ta);
-        else trellis_part<1>(W, tab, ta);
+        const uint32_t Lw[5] = {pl[0], pl[1], pl[2], pl[3], pl[4]};
+        trellis_part(Lw, tab, ta);
       } else if (FMT == Q2_BPDQ) {
         const uint32_t tlo = __byte_perm(vt.x, vt.y, 0x6420u);
         const uint32_t thi = __byte_perm(vt.x, vt.y, 0x7531u);
-        const uint32_t R0[8] = {pl[0].x, pl[0].y, pl[0].z, pl[0].w, pl[1].x, pl[1].y, pl[1].z, pl[1].w};
-        const uint32_t R1[8] = {pl[2].x, pl[2].y, pl[2].z, pl[2].w, pl[3].x, pl[3].y, pl[3].z, pl[3].w};
-        if (part == 0) bpdq_part<0>(R0, R1, lane, tlo, thi, ta);
-        else bpdq_part<1>(R0, R1, lane, tlo, thi, ta);
+        uint32_t L0[kPartWords + 1], L1[kPartWords + 1];
+#pragma unroll
+        for (int t = 0; t <= kPartWords; ++t) {
+          L0[t] = pl[t];
+          L1[t] = pl[kPartWords + 1 + t];
+        }
+        bpdq_part(L0, L1, sh, tlo, thi, ta);
       } else {
-        const uint32_t R0[8] = {pl[0].x, pl[0].y, pl[0].z, pl[0].w, pl[1].x, pl[1].y, pl[1].z, pl[1].w};
-        const uint32_t R1[8] = {pl[2].x, pl[2].y, pl[2].z, pl[2].w, pl[3].x, pl[3].y, pl[3].z, pl[3].w};
-        const uint32_t R2[8] = {pl[4].x, pl[4].y, pl[4].z, pl[4].w, pl[5].x, pl[5].y, pl[5].z, pl[5].w};
+        uint32_t L0[kPartWords + 1], L1[kPartWords + 1], L2[kPartWords + 1];
+#pragma unroll
+        for (int t = 0; t <= kPartWords; ++t) {
+          L0[t] = pl[t];
+          L1[t] = pl[kPartWords + 1 + t];
+          L2[t] = pl[2 * (kPartWords + 1) + t];
+        }
+        leech_part(L0, L1, L2, sh, ta);
         if (part == 0) {
-          leech_part<0>(R0, R1, R2, lane, ta);
-          // parity columns (K 256..287, TMEM columns 128..143): A = 1.0 where
-          // the block starting in this slice is odd, once for the hi and
-          // once for the lo part of the block sums
+          // parity columns (K 256..287, TMEM columns 128..143 of the stage):
+          // A = 1.0 where the block starting in this slice is odd, once for
+          // the hi and once for the lo part of the block sums
           uint32_t pv[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
@@ -508,17 +575,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
             pv[q] = lo | hi;
           }
           const uint4 q0 = make_uint4(pv[0], pv[1], pv[2], pv[3]), q1 = make_uint4(pv[4], pv[5], pv[6], pv[7]);
-          tmem_st16(ta + 128u, q0, q1, q0, q1);
-        } else {
-          leech_part<1>(R0, R1, R2, lane, ta);
+          tmem_st16(tlane + kAcol0 + (uint32_t)sa * Sh::acols + 128u, q0, q1, q0, q1);
         }
-        // B side of the parity columns (atom 4): block sums of x for the
-        // blocks starting in this slice, hi part at K 256 + jb, lo part
-        // (sum - hi) at K 272 + jb
+        // B side of the parity columns (atom 4 of B stage i % kStagesB, free:
+        // the MMAs up to slice i - kStagesA, which include those of slice
+        // i - kStagesB, are done):
+        // block sums of x for the blocks starting in this slice, hi part at
+        // K 256 + jb, lo part (sum - hi) at K 272 + jb
         const int bfirst = (s * 256 + 23) / 24;
         const int blast = min(a.nblock - 1, (s * 256 + 256 + 23) / 24 - 1);
         const int nbk = max(0, blast - bfirst + 1);
-        unsigned char* Bp = B0 + st * bbytes + 4 * atom_bytes;
+        unsigned char* Bp = B0 + (i % kStagesB) * bbytes + 4 * atom_bytes;
         for (int e = threadIdx.x; e < a.ntok * 16; e += kDecWarps * 32) {
           const int n = e >> 4, jb = e & 15;
           float xsum = 0.f;
@@ -551,11 +618,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(saddr(&full[st]));
+      if (lane == 0) mbar_arrive(saddr(&fullA[sa]));
 #pragma unroll
-      for (int k = 0; k < NP; ++k) {
-        pl[k] = n1[k];
-        n1[k] = n2[k];
+      for (int t = 0; t < NW; ++t) {
+        pl[t] = n1[t];
+        n1[t] = n2[t];
       }
       vt = v1;
       v1 = v2;
@@ -564,14 +631,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
     }
     // the accumulator is final once the last slice's commit has arrived
     if (ok && warp < 4 && used > 0 &&
-        !__all_sync(~0u, mbar_wait(saddr(&empty[(used - 1) % kStages]), (uint32_t)((used - 1) / kStages) & 1u))) {
+        !__all_sync(~0u, mbar_wait(saddr(&emptyA[(used - 1) % kStagesA]), (uint32_t)((used - 1) / kStagesA) & 1u))) {
       ok = false;
       if (lane == 0) atomicExch(&q2_tc_error, 2u);
     }
   }
   ok = __syncthreads_and(ok);
   tc_fence_after();
-  if (warp < 4 && ok) {
+  if (warp < 4 && ok && used > 0) {
     const int orow = (tile * 4 + warp) * 32 + lane;
     for (int c0 = 0; c0 < a.N; c0 += 16) {
       float v[16];
@@ -672,8 +739,8 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
     }
   }
   a.use_tma = encode_x_map(&a.xmap, x, d.C, ntok, a.N) ? 1 : 0;
-  // table, 1024-byte alignment slack, kStages B buffers, 2 x kStages mbarriers, TMEM slot
-  const int smem = max(kOneCtaSmem, Sh::table + 1024 + kStages * Sh::atoms * a.N * 128 + 2 * kStages * 8 + 16);
+  // table, 1024-byte alignment slack, B buffers, the stage mbarriers, TMEM slot
+  const int smem = max(kOneCtaSmem, Sh::table + 1024 + kStagesB * Sh::atoms * a.N * 128 + (2 * kStagesA + kStagesB + 2) * 8 + 16);
   int st = launch_pdl(k_tc<FMT>, a, a.ntile * a.nsplit, kThreads, smem, stream);
   if (st) return st;
   if (a.nsplit == 1 && FMT == Q2_BPDQ) return Q2_OK;
