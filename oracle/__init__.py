@@ -21,6 +21,9 @@ Modules:
               ("Unfolding the Leech Lattice", introduction and section 7)
   fp16     -- the dense fp16 control
   matvec   -- f64 reference product and the pass criterion
+  rotate   -- the activation rotation x_rot = (H (x) Q)(S x) applied ahead
+              of the GEMV ("Qwen3.8-27B on a 12 GB card", section "What
+              the kernel does per token")
 
 Parity status: every decode function is pinned by closed forms, special
 cases or page-printed values in ``tests/test_oracle_*.py``.  The trellis

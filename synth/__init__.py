@@ -21,6 +21,8 @@ Canonical layouts (the arrays the packers take):
   ``scale``: fp16 ``[R]``.
 * fp16 dense -- ``w``: fp16 ``[R][C]``.
 * activations -- ``x``: fp16 ``[N][C]``.
+* rotation -- ``signs``: uint8 ``[ceil(C/8)]`` column sign bits, ``q``: fp32
+  ``[nq][nq]`` orthogonal, C = nh * nq.
 """
 from __future__ import annotations
 
@@ -272,3 +274,23 @@ def leech(R: int, C: int, seed: int) -> dict:
     scale = rng.uniform(0.005, 0.03, size=R).astype(np.float16)
     tail = rng.normal(0.0, 0.01, size=(R, C % BLOCK)).astype(np.float16)
     return {"R": R, "C": C, "v": v, "shell": shell, "scale": scale, "tail": tail}
+
+
+def rotation(C: int, nh: int, seed: int) -> dict:
+    """Inputs of the activation rotation x_rot = (H (x) Q)(S x).
+
+    Draw order: ``signs`` uint8 [ceil(C/8)] uniform bytes (bit c % 8 of byte
+    c // 8 is the sign of column c, 1 = negate); then an nq x nq matrix of
+    N(0, 1) draws, nq = C / nh, whose QR factor (numpy.linalg.qr, columns
+    sign-fixed by the diagonal of R) is rounded to fp32 as ``q`` (row-major,
+    orthogonal to fp32 rounding).
+    """
+    if C % nh:
+        raise ValueError("C must be a multiple of nh")
+    nq = C // nh
+    rng = _rng(seed, 2)
+    signs = rng.integers(0, 256, size=(C + 7) // 8, dtype=np.uint8)
+    g = rng.normal(0.0, 1.0, size=(nq, nq))
+    qm, rm = np.linalg.qr(g)
+    qm = qm * np.sign(np.diag(rm))[None, :]
+    return {"C": C, "nh": nh, "nq": nq, "signs": signs, "q": qm.astype(np.float32)}
