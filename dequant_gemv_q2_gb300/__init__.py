@@ -61,6 +61,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "q2_decode": [vp, vp, vp],
         "q2_gemv_bpdq_noalloc": [vp, vp, vp, vp],
         "q2_device_errors": [ctypes.POINTER(ctypes.c_uint)],
+        "q2_rotate": [vp, vp, i32, i32, i32, vp, vp, vp],
+        "q2_rotate_split": [i32, ctypes.POINTER(i32), ctypes.POINTER(i32)],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -77,7 +79,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
 EXPORTS = ["q2_pack_fp16", "q2_pack_bpdq", "q2_pack_trellis", "q2_pack_leech", "q2_pack_noweights",
            "q2_bind", "q2_unbind", "q2_workspace_bytes", "q2_set_workspace", "q2_info", "q2_bytes",
            "q2_gemv", "q2_decode_bytes", "q2_decode", "q2_strerror", "q2_gemv_bpdq_noalloc",
-           "q2_device_errors"]
+           "q2_device_errors", "q2_rotate", "q2_rotate_split"]
 
 
 def q2_strerror(status: int) -> str:
@@ -233,3 +235,41 @@ def q2_gemv(fmt: int, packed: Packed, x, y, ntok: int, stream=None) -> int:
     """The C entry point with its own argument order (status returned)."""
     return load().q2_gemv(int(fmt), packed.h, ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()),
                           int(ntok), _stream_ptr(stream))
+
+
+def q2_rotate_split(C: int) -> tuple:
+    """(nh, nq) of the page's examples: nh = 2048 if it divides C, else 1024."""
+    nh, nq = ctypes.c_int(), ctypes.c_int()
+    _check(load().q2_rotate_split(int(C), ctypes.byref(nh), ctypes.byref(nq)), "q2_rotate_split")
+    return nh.value, nq.value
+
+
+def q2_rotate(x, x_rot, ntok: int, C: int, nh: int, signs, q, stream=None) -> int:
+    """The C entry point (status returned): x_rot = (H (x) Q)(S x) per token."""
+    return load().q2_rotate(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(x_rot.data_ptr()), int(ntok), int(C),
+                            int(nh), ctypes.c_void_p(signs.data_ptr()),
+                            ctypes.c_void_p(q.data_ptr()) if q is not None else None, _stream_ptr(stream))
+
+
+class Rotation:
+    """The activation rotation of one input width, x_rot = (H (x) Q)(S x).
+
+    ``signs``: uint8 [ceil(C/8)] column sign bits; ``q``: fp32 [nq][nq]
+    (None when nq == 1).  Both are copied to the device once.
+    """
+
+    def __init__(self, signs: np.ndarray, q, nh: int, C: int, device="cuda"):
+        import torch
+        self.C, self.nh = int(C), int(nh)
+        self.signs = torch.from_numpy(np.ascontiguousarray(signs, dtype=np.uint8)).to(device)
+        self.q = None if q is None else torch.from_numpy(np.ascontiguousarray(q, dtype=np.float32)).to(device)
+
+    def apply(self, x, out=None, stream=None):
+        """Rotate x [ntok][C] (fp16, device) into a new or given fp16 tensor (asynchronous)."""
+        import torch
+        if x.dim() == 1:
+            x = x.view(1, -1)
+        if out is None:
+            out = torch.empty_like(x)
+        _check(q2_rotate(x, out, x.shape[0], self.C, self.nh, self.signs, self.q, stream), "q2_rotate")
+        return out

@@ -195,6 +195,33 @@ int q2_gemv_bpdq_noalloc(const q2_handle* h, const void* x, void* y, q2_stream s
 int q2_decode_bytes(const q2_handle* h, size_t* bytes);
 int q2_decode(const q2_handle* h, void* out_dev, q2_stream stream);
 
+/* ------------------------------------------------------------------ rotation
+ * Activation rotation ahead of the GEMV ("Qwen3.8-27B on a 12 GB card",
+ * section "What the kernel does per token"): weights stored in a rotated
+ * basis need their input rotated at run time, per token,
+ *     x_rot = (H (x) Q)(S x),   C = nh * nq,
+ * with S the column signs, Q an nq x nq orthogonal matrix acting on every
+ * run of nq consecutive columns, and H the orthonormal Sylvester
+ * Walsh-Hadamard transform, H[i][j] = (-1)^popcount(i & j) / sqrt(nh),
+ * acting across the runs: entry (i*nq + a, j*nq + b) of H (x) Q is
+ * H[i][j] * Q[a][b].  Computed in fp32, rounded once to fp16.
+ *   - x, x_rot: device fp16 [ntok][C], distinct buffers; 1 <= ntok <= 64.
+ *   - nh a power of two, C a multiple of nh, nq = C / nh <= 32,
+ *     C <= Q2_ROT_MAX_C; otherwise Q2_ESHAPE.
+ *   - signs: device uint8 [ceil(C/8)]; bit c % 8 of byte c / 8 set means
+ *     column c is negated.
+ *   - q: device fp32 [nq][nq] row-major; may be NULL only when nq == 1
+ *     (Q = [1]).
+ *   - Asynchronous on `stream`, launched like q2_gemv (x is read only after
+ *     the previous kernel on the stream has finished).  One CTA per token.
+ * q2_rotate_split gives the split the page's examples follow: nh = 2048
+ * when 2048 divides C, else 1024 (5120 = 5 x 1024, 6144 = 3 x 2048,
+ * 17408 = 17 x 1024); Q2_ESHAPE if C is not a multiple of it. */
+#define Q2_ROT_MAX_C 49152
+int q2_rotate(const void* x, void* x_rot, int ntok, int C, int nh, const void* signs, const float* q,
+              q2_stream stream);
+int q2_rotate_split(int C, int* nh, int* nq);
+
 /* Device-side error word of the tensor-core (multi-token) kernels, then
  * cleared: 0 in normal operation; nonzero means a bounded wait on the
  * tensor core ran out and the kernel skipped its work (its outputs are not
