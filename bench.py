@@ -225,6 +225,35 @@ def per_format(q2, stream, hbm):
     return out
 
 
+ROT_WIDTHS = [4096, 5120, 12288, 17408]
+
+
+def _rotation(q2, C: int, seed: int):
+    import synth
+    nh, nq = q2.q2_rotate_split(C)
+    inp = synth.rotation(C, nh, seed)
+    return q2.Rotation(inp["signs"], inp["q"] if nq > 1 else None, nh, C), nh, nq
+
+
+def rotations(q2, stream):
+    """Latency of the activation rotation (H (x) Q)(S x) per input width, at
+    1, 16 and 64 tokens: 50 back-to-back rotations per graph replay."""
+    import torch
+    import synth
+    out = {}
+    for C in ROT_WIDTHS:
+        rot, nh, nq = _rotation(q2, C, 900 + C % 1000)
+        rec = {"C": C, "nh": nh, "nq": nq}
+        for ntok in (1, 16, 64):
+            x = torch.from_numpy(synth.activations(ntok, C, 901)).cuda()
+            y = torch.empty_like(x)
+            g = graph_of([lambda: rot.apply(x, y, stream=stream)] * 50, stream)
+            ms = time_graph(g, stream, 20, 3)
+            rec[f"us_ntok{ntok}"] = round(ms * 1e3 / (20 * 50), 3)
+        out[f"rotation_{C}"] = rec
+    return out
+
+
 SHAPES_14B = [("qkv", 7168, 5120), ("o", 5120, 5120), ("gate_up", 34816, 5120), ("down", 5120, 17408)]
 LAYERS_14B = 40
 
@@ -397,7 +426,8 @@ def run_reference(args, ws, rank):
 def profile_case(fmt: str, launches: int = 4, ntok: int = 1):
     """A few launches of one layer-shaped matrix per format, for ncu captures
     (no timing): bpdq 24576x4096 and 4096x12288, trellis 12288x4096, leech
-    17408x5120, fp16 4096x4096, noweights 24576x4096."""
+    17408x5120, fp16 4096x4096, noweights 24576x4096; rotate: the activation
+    rotation at widths 17408 and 4096."""
     import torch
     import dequant_gemv_q2_gb300 as q2
     import synth
@@ -417,6 +447,15 @@ def profile_case(fmt: str, launches: int = 4, ntok: int = 1):
         mats.append((q2.q2_pack_fp16(np.zeros((4096, 4096), dtype=np.float16)), 4096))
     elif fmt == "noweights":
         mats.append((q2.q2_pack_noweights(24576, 4096), 4096))
+    elif fmt == "rotate":
+        for C in (17408, 4096):
+            rot = _rotation(q2, C, 970)[0]
+            x = torch.from_numpy(synth.activations(ntok, C, 7)).cuda()
+            for _ in range(launches):
+                rot.apply(x)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": fmt, "widths": [17408, 4096], "launches_each": launches, "ntok": ntok}))
+        return
     for blob, C in mats:
         pk = q2.Packed(blob, ntok_max=ntok)
         x = torch.from_numpy(synth.activations(ntok, C, 7)).cuda()
@@ -436,7 +475,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the per-format lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--profile-case", default=None,
-                    choices=["bpdq", "trellis", "leech", "fp16", "noweights"],
+                    choices=["bpdq", "trellis", "leech", "fp16", "noweights", "rotate"],
                     help="run a few untimed launches of one format for an ncu capture")
     ap.add_argument("--sweep", action="store_true", help="sweep over the 14B layer stack: formats x tokens")
     ap.add_argument("--sweep-formats", default="fp16,cublas,bpdq,trellis,leech")
@@ -523,9 +562,27 @@ def main():
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws)
     e2e_value = ws * args.ntok * e2e_steps / (e2e_ms / 1e3)
 
-    extras = None
+    extras = rot_line = None
     if not args.no_extras and rank == 0:
         extras = per_format(q2, stream, hbm)
+        extras.update(rotations(q2, stream))
+        # the same stack with every linear's input rotated first (one rotation
+        # per group of projections sharing an input: qkv and gate_up are fused)
+        rots = {C: _rotation(q2, C, 950 + C % 1000)[0] for C in sorted({L["C"] for L in lin})}
+        for L in lin:
+            L["xr"] = torch.empty_like(L["x"])
+        rcalls = []
+        for L in lin:
+            rcalls.append(lambda L=L: rots[L["C"]].apply(L["x"], L["xr"], stream=stream))
+            rcalls.append(lambda L=L: L["pk"].gemv(L["xr"], L["y"]))
+        gr = graph_of(rcalls, stream)
+        rsteps = max(10, args.steps // 4)
+        rms = time_graph(gr, stream, rsteps, 3) / rsteps
+        rot_line = {"workload": "the same stack, each linear's input rotated by q2_rotate first",
+                    "rotations_per_step": len(lin), "ms_per_step": round(rms, 4),
+                    "tok_s": round(args.ntok / (rms * 1e-3), 1),
+                    "rotation_share": round(1.0 - ms_step / rms, 3)}
+        del gr
 
     achieved = step_bytes / (ms_step * 1e-3) / 1e9
     kname = "k_bpdq_b1" if args.ntok == 1 else ("k_bpdq_mt" if args.ntok <= 6 else "k_tc")
@@ -562,6 +619,8 @@ def main():
                                     "sample": "failed: " + cpu.get("error", "")[:200]}
         if extras is not None:
             line["per_format"] = extras
+        if rot_line is not None:
+            line["stack_with_rotation"] = rot_line
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist

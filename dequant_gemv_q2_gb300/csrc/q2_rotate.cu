@@ -198,11 +198,12 @@ __global__ void __launch_bounds__(kRotThreads, 1) k_rotate(RotArgs a) {
 //   1. z = S x of its columns; 2. Q on each of its runs;
 //   3. the Walsh-Hadamard transform over the low log2(J) bits locally;
 //   4. after a cluster barrier, the G-point transform over the high bits:
-//      CTA g takes 1/G of the local positions and, for each,
-//      reads the value at that position in every CTA's shared memory
-//      (distributed shared memory), transforms and writes them back; the
-//      CTAs' position sets are disjoint, so no other ordering is needed;
-//   5. after a second cluster barrier, each CTA writes its columns.
+//      CTA g takes 1/G of the local positions and, for each, reads the value
+//      at that position in every CTA's shared memory (distributed shared
+//      memory), transforms the G values and writes them, normalised and
+//      rounded to fp16, straight to their columns of x_rot;
+//   5. a split cluster barrier (arrive after the peer reads, wait before
+//      exit) keeps every CTA's shared memory alive until its peers are done.
 template <int G>
 __global__ void __launch_bounds__(kRotThreads, 1) k_rotate_cluster(RotArgs a) {
   extern __shared__ __align__(16) unsigned char q2_rot_smem[];
@@ -214,7 +215,6 @@ __global__ void __launch_bounds__(kRotThreads, 1) k_rotate_cluster(RotArgs a) {
   float* u = z + pad(Cl) + 1;                                   // Q z, then the transform, padded
   const size_t col0 = (size_t)(blockIdx.x / G) * a.C + (size_t)g * Cl;
   const __half* xt = a.x + col0;
-  __half* yt = a.y + col0;
   const int gcol = g * Cl;                                      // first column of this CTA in the token
   if (a.q)
     for (int i = threadIdx.x; i < a.nq * a.nq; i += kRotThreads) qs[i] = a.q[i];
@@ -272,10 +272,13 @@ __global__ void __launch_bounds__(kRotThreads, 1) k_rotate_cluster(RotArgs a) {
   // 3. local transform over the low bits of the run index
   wht_runs(u, J, a.nq, a.lognh - (G == 8 ? 3 : G == 4 ? 2 : 1));
   cluster.sync();
-  // 4. G-point transform over the high bits, through distributed shared memory
+  // 4. G-point transform over the high bits, through distributed shared
+  // memory, written straight to x_rot: position pos of chunk k is column
+  // k * Cl + pos of the token
   {
     const int P = Cl / G;
-    float* peer[G];
+    __half* ytok = a.y + (size_t)(blockIdx.x / G) * a.C;
+    const float* peer[G];
 #pragma unroll
     for (int k = 0; k < G; ++k) peer[k] = cluster.map_shared_rank(u, k);
     for (int pos = g * P + threadIdx.x; pos < (g + 1) * P; pos += kRotThreads) {
@@ -293,26 +296,12 @@ __global__ void __launch_bounds__(kRotThreads, 1) k_rotate_cluster(RotArgs a) {
             v[t + h] = s0 - d0;
           }
 #pragma unroll
-      for (int k = 0; k < G; ++k) peer[k][pp] = v[k];
+      for (int k = 0; k < G; ++k) ytok[k * Cl + pos] = __float2half_rn(v[k] * a.inv_sqrt_nh);
     }
   }
-  cluster.sync();
-  // 5. normalise, round to fp16
-  if (a.vec) {
-    uint4* y4 = reinterpret_cast<uint4*>(yt);
-    for (int v = threadIdx.x; v < (Cl >> 3); v += kRotThreads) {
-      uint4 o;
-      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __half2 h = __floats2half2_rn(u[pad(8 * v + 2 * i)] * a.inv_sqrt_nh, u[pad(8 * v + 2 * i + 1)] * a.inv_sqrt_nh);
-        ow[i] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      y4[v] = o;
-    }
-  } else {
-    for (int e = threadIdx.x; e < Cl; e += kRotThreads) yt[e] = __float2half_rn(u[pad(e)] * a.inv_sqrt_nh);
-  }
+  // 5. no CTA leaves while a peer may still read its shared memory
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 template <int G>
