@@ -167,6 +167,18 @@ def test_leech_parity(q2, R, C, seed, ntok):
     _check(y, oleech.decode_f64(d["v"], d["scale"], d["tail"]), x)
 
 
+@pytest.mark.parametrize("ntok", [1, 2, 16, 64])
+def test_leech_width_not_multiple_of_8(q2, ntok):
+    # C % 8 != 0: the tensor-core path cannot describe x rows to TMA (row
+    # stride not a multiple of 16 bytes) and stages the x tiles and the parity
+    # block sums with element loads instead
+    R, C = 70, 24 * 20 + 12
+    d = _leech_with_exceptions(R, C, 3100 + ntok)
+    x = synth.activations(ntok, C, 3101)
+    _, y = _run(q2, q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C), x)
+    _check(y, oleech.decode_f64(d["v"], d["scale"], d["tail"]), x)
+
+
 def test_leech_decode_bit_exact(q2):
     R, C = 70, 24 * 40 + 8
     d = _leech_with_exceptions(R, C, 3010)
