@@ -646,16 +646,27 @@ struct BpdqMtF {
   __device__ void tables(int, const __half* xs, unsigned char* tl) const {
     build_pairs<NT, NP>(xs, a.c.ntok, reinterpret_cast<float*>(q2_smem), reinterpret_cast<float*>(tl + kTailGsum));
   }
+  // Lookup P into accumulator P mod 4, then (s0 + s1) + (s2 + s3): the
+  // order plane_sum uses at one token, so each token's partial (and output)
+  // is bit-identical to the single-token kernel's.
   __device__ void plane(const uint4& c0, const uint4& c1, float2 (&S)[NP]) const {
     const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
     const char* base = reinterpret_cast<const char*>(q2_smem);
+    float2 acc[NP][4];
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[p][k] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int P = 0; P < 32; ++P) {
       const uint32_t sel = (4u + (uint32_t)(P % 3)) | ((uint32_t)(P & 3) << 4) | 0x7700u;
       const uint32_t ad = __byte_perm(w[P >> 2], rot[P / 3], sel);
 #pragma unroll
-      for (int p = 0; p < NP; ++p) S[p] = __fadd2_rn(S[p], *reinterpret_cast<const float2*>(base + p * kPairBytes + ad));
+      for (int p = 0; p < NP; ++p)
+        acc[p][P & 3] = __fadd2_rn(acc[p][P & 3], *reinterpret_cast<const float2*>(base + p * kPairBytes + ad));
     }
+#pragma unroll
+    for (int p = 0; p < NP; ++p) S[p] = __fadd2_rn(__fadd2_rn(acc[p][0], acc[p][1]), __fadd2_rn(acc[p][2], acc[p][3]));
   }
   __device__ void compute(int, int, int, const Item& b, float (&p)[2 * NP]) const {
     float2 S0[NP], S1[NP];
