@@ -854,14 +854,26 @@ extern "C" int q2_mt_bpdq(const q2_handle* h, const void* x, void* y, int ntok, 
   a.bits = h->dev + d.off[SEC_BPDQ_BITS];
   a.c01 = reinterpret_cast<const __half2*>(h->dev + d.off[SEC_BPDQ_C01]);
   a.off = reinterpret_cast<const __half*>(h->dev + d.off[SEC_BPDQ_OFF]);
-  const int np = (ntok + 1) / 2;
+  // Tokens go in pairs through the one-pair kernel, an odd last token
+  // through the single-token kernel: measured faster than two- and
+  // three-pair kernels (their registers allow only 8 warps per SM), and
+  // every token's result is the same bit for bit whichever kernel runs it.
+  // The launches are stream-ordered; each leaves its accumulator words zero
+  // for the next.
   const Geo g = geometry(d);
-  switch (np) {
-    case 1: return launch1(k_bpdq_mt<kWarps, 2, 1>, a, g, kWarps * 32, 1 * kPairBytes, stream);
-    case 2: return launch1(k_bpdq_mt<8, 1, 2>, a, g, 8 * 32, 2 * kPairBytes, stream, kOneCtaSmem);
-    case 3: return launch1(k_bpdq_mt<8, 1, 3>, a, g, 8 * 32, 3 * kPairBytes, stream, kOneCtaSmem);
-    default: return Q2_ENTOK;
+  const __half* xh = static_cast<const __half*>(x);
+  __half* yh = static_cast<__half*>(y);
+  for (int t = 0; t < ntok; t += 2) {
+    int st;
+    if (t + 1 < ntok) {
+      a.c = make_b1(h, xh + (size_t)t * d.C, yh + (size_t)t * d.R, 2);
+      st = launch1(k_bpdq_mt<kWarps, 2, 1>, a, g, kWarps * 32, 1 * kPairBytes, stream);
+    } else {
+      st = q2_b1_bpdq(h, xh + (size_t)t * d.C, yh + (size_t)t * d.R, stream);
+    }
+    if (st) return st;
   }
+  return Q2_OK;
 }
 
 extern "C" int q2_b1_noweights(const q2_handle* h, const void* x, void* y, void* stream) {
