@@ -160,7 +160,7 @@ def _leech_with_exceptions(R, C, seed):
 
 
 @pytest.mark.parametrize("R,C,seed", [(70, 24 * 40 + 8, 3000), (32, 256, 3001), (100, 5120, 3002), (33, 24, 3003)])
-@pytest.mark.parametrize("ntok", [1, 4, 16, 64])
+@pytest.mark.parametrize("ntok", [1, 2, 4, 16, 64])
 def test_leech_parity(q2, R, C, seed, ntok):
     d = _leech_with_exceptions(R, C, seed)
     x = synth.activations(ntok, C, seed)
