@@ -148,3 +148,27 @@ def test_status_codes(q2):
     assert L.q2_gemv(1, h, x, x, 1, None) == -7                              # no workspace
     assert L.q2_strerror(-7) == b"workspace missing or too small"
     L.q2_unbind(h)
+
+
+def test_rotation_split_and_argument_checks(q2):
+    # q2_rotate_split follows the page's examples; q2_rotate validates every
+    # argument before it touches the device (the pointers below are never read)
+    assert q2.q2_rotate_split(5120) == (1024, 5)
+    assert q2.q2_rotate_split(6144) == (2048, 3)
+    assert q2.q2_rotate_split(17408) == (1024, 17)
+    assert q2.q2_rotate_split(4096) == (2048, 2)
+    L = q2.load()
+    a, b = ctypes.c_int(), ctypes.c_int()
+    assert L.q2_rotate_split(1000, ctypes.byref(a), ctypes.byref(b)) == -2          # not a multiple of 1024
+    assert L.q2_rotate_split(4096, None, ctypes.byref(b)) == -1
+    x, y, s, q = (ctypes.c_void_p(1 << k) for k in (21, 22, 23, 24))
+    assert L.q2_rotate(None, y, 1, 4096, 2048, s, q, None) == -1                    # null x
+    assert L.q2_rotate(x, y, 1, 4096, 2048, None, q, None) == -1                    # null signs
+    assert L.q2_rotate(x, y, 0, 4096, 2048, s, q, None) == -5                       # ntok
+    assert L.q2_rotate(x, y, 65, 4096, 2048, s, q, None) == -5
+    assert L.q2_rotate(x, y, 1, 4096, 1000, s, q, None) == -2                       # nh not a power of two
+    assert L.q2_rotate(x, y, 1, 4097, 1024, s, q, None) == -2                       # C % nh
+    assert L.q2_rotate(x, y, 1, 64 * 33, 64, s, q, None) == -2                      # nq = 33 > 32
+    assert L.q2_rotate(x, y, 1, 2048 * 32, 2048, s, q, None) == -2                  # C over the maximum
+    assert L.q2_rotate(x, y, 1, 4096, 1024, s, None, None) == -1                    # nq = 4 needs Q
+    assert L.q2_rotate(x, x, 1, 4096, 4096, s, None, None) == -1                    # in place
