@@ -116,13 +116,22 @@ def _barrier(ws):
 
 
 def _max_over_ranks(v: float, ws: int) -> float:
+    """The largest of every rank's v (a timing: the job ends with its slowest rank)."""
     if ws == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _job_value(ws: int, ntok: int, steps: int, ms: float) -> float:
+    """Whole-job tokens per second: every replica processes ntok tokens per
+    step, so all ranks together do ws * ntok * steps tokens in the slowest
+    rank's ms."""
+    return ws * ntok * steps / (ms / 1e3)
 
 
 def build_stack(q2, ntok: int, config: int = 1):
@@ -531,7 +540,7 @@ def main():
     clocks = clk.stop()
     ms = _max_over_ranks(ms, ws)
     ms_step = ms / args.steps
-    value = ws * args.ntok * args.steps / (ms / 1e3)
+    value = _job_value(ws, args.ntok, args.steps, ms)
 
     # end to end through the C ABI: pinned host x in, host y out, every step
     xs_host = [L["x"].cpu().pin_memory() for L in lin]
@@ -560,7 +569,7 @@ def main():
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws)
-    e2e_value = ws * args.ntok * e2e_steps / (e2e_ms / 1e3)
+    e2e_value = _job_value(ws, args.ntok, e2e_steps, e2e_ms)
 
     extras = rot_line = None
     if not args.no_extras and rank == 0:
