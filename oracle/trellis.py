@@ -4,7 +4,7 @@ in and emits V weights, so the rate is T/V bits per weight; in a bitshift
 trellis the state is the last L bits of the stream, so position i is decoded
 from one L-bit window, with no dependence between steps.
 
-This build's configuration: L = 16, T = 4, V = 2 (the page's V2T4 layout,
+The configuration implemented: L = 16, T = 4, V = 2 (the page's V2T4 layout,
 2 bits per weight).  The codebook is a shared table of 4096 x 2 fp16 values
 indexed by ((s * 0x9E37) & 0xFFFF) >> 4; bit 0 of the state sets the sign of
 both emitted weights (1 = negative); the stream restarts every 256 columns.
