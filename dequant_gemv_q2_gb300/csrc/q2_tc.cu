@@ -20,9 +20,9 @@
 // access: any memory access by the issuing thread waits for its queue of
 // MMAs to drain and leaves the tensor core idle (about 350 cycles per
 // access on GB300), so the MMA lane touches no memory at all.
-// At the end the decoder warps of the first 32-row quarter group read the
-// accumulator (each its 32 TMEM lanes) and write fp32 partial sums for the
-// split-K reduction kernel, or y directly.
+// At the end decoder warps 0..3 (one per TMEM lane quarter) read the
+// accumulator, each its 32 lanes = 32 rows, and write fp32 partial sums for
+// the split-K reduction kernel, or y directly.
 //
 // TMEM columns (all 512 are allocated; one CTA per SM): D at 0 .. N - 1,
 // A of stage st at kAcol0 + st * (4 x K chunks); A column j of a lane holds

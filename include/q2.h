@@ -145,12 +145,15 @@ int q2_bytes(const q2_handle* h, int ntok, size_t* weight_bytes_read_per_call);
  * [ntok][C]; y: device fp16 [ntok][R]; both 16-byte aligned; 1 <= ntok <= 64.
  * Asynchronous and ordered on `stream`; never synchronises.  Needs the
  * workspace of q2_workspace_bytes(h, ntok) bound first (0 bytes for fp16).
- * The packed formats at 1..6 tokens (BPDQ) or 1 token (trellis, Leech) run
- * as one launch that reduces its split-K partial sums itself, through the
+ * The packed formats at 1 token, and BPDQ at 2..6 tokens, run on CUDA cores
+ * in launches that reduce their split-K partial sums themselves, through the
  * workspace's fixed-point accumulator words (integer sums: the result does
- * not depend on the order in which slices arrive); the tensor-core path
- * (7..64 tokens, or 2..64 for trellis and Leech) adds a second, in-order
- * reduction launch.  The fixed-point scale 2^F is chosen per matrix from its
+ * not depend on the order in which slices arrive).  BPDQ at 3..6 tokens runs
+ * its tokens in pairs plus a single-token launch, stream-ordered; every
+ * token's BPDQ result at 1..6 tokens is bit-identical whatever the batch.
+ * Leech at 2 tokens runs two single-token launches when C and R are
+ * multiples of 8.  The tensor-core path (7..64 tokens, or 2..64 for trellis
+ * and the other Leech cases) adds a second, in-order reduction launch.  The fixed-point scale 2^F is chosen per matrix from its
  * largest weight magnitude so that no fp16 x can overflow it; each slice's
  * partial then carries an absolute rounding error of at most 2^-(F+1),
  * about 1e-8 for weights of magnitude 0.05.  Launches use programmatic dependent launch: weights are
