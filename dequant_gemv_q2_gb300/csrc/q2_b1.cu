@@ -177,27 +177,6 @@ __device__ __forceinline__ float plane_sum(uint32_t lane4, const uint4& c0, cons
   return (s[0] + s[1]) + (s[2] + s[3]);
 }
 
-// ------------------------------------------- fixed-point accumulation
-// Accumulator word: bits 56..63 count the slices added so far; bits 0..55
-// hold the sum of (q + 2^47) over those slices, q = round(partial * 2^F) in
-// [-(2^47 - 1), 2^47 - 1].  At most Q2_MAX_SPLIT (255) biased terms of at
-// most 2^48 each sum below 2^56, so the value never carries into the count.
-constexpr unsigned long long kBias = 1ull << 47;
-constexpr unsigned long long kCountOne = 1ull << 56;
-constexpr unsigned long long kValueMask = kCountOne - 1;
-
-__device__ __forceinline__ unsigned long long fx_term(float p, float fscale) {
-  long long q = __float2ll_rn(p * fscale);
-  q = max(min(q, (long long)kBias - 1), -(long long)kBias + 1);   // NaN/inf partials stay in range
-  return kCountOne + (unsigned long long)(q + (long long)kBias);
-}
-
-// The value of a complete accumulator word (all nslice terms added).
-__device__ __forceinline__ float fx_value(unsigned long long w, int nslice, float finv) {
-  const long long v = (long long)(w & kValueMask) - (long long)nslice * (long long)kBias;
-  return (float)v * finv;
-}
-
 // Atomics a lane has issued for one item (NT tokens), settled one item later
 // so the atomic's round trip overlaps the next item's work.
 template <int NT>

@@ -148,6 +148,29 @@ struct Reduce {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// ------------------------------------------- fixed-point accumulation
+// Accumulator word: bits 56..63 count the slices added so far; bits 0..55
+// hold the sum of (q + 2^47) over those slices, q = round(partial * 2^F) in
+// [-(2^47 - 1), 2^47 - 1].  At most Q2_MAX_SPLIT (255) biased terms of at
+// most 2^48 each sum below 2^56, so the value never carries into the count.
+// The batch-1 kernels add one term per 256-column slice, the tensor-core
+// kernel one per K split.
+constexpr unsigned long long kBias = 1ull << 47;
+constexpr unsigned long long kCountOne = 1ull << 56;
+constexpr unsigned long long kValueMask = kCountOne - 1;
+
+__device__ __forceinline__ unsigned long long fx_term(float p, float fscale) {
+  long long q = __float2ll_rn(p * fscale);
+  q = max(min(q, (long long)kBias - 1), -(long long)kBias + 1);   // NaN/inf partials stay in range
+  return kCountOne + (unsigned long long)(q + (long long)kBias);
+}
+
+// The value of a complete accumulator word (all nslice terms added).
+__device__ __forceinline__ float fx_value(unsigned long long w, int nslice, float finv) {
+  const long long v = (long long)(w & kValueMask) - (long long)nslice * (long long)kBias;
+  return (float)v * finv;
+}
+
 // Launch with programmatic stream serialization allowed (PDL): the kernel
 // may start while the previous kernel on the stream drains; it must call
 // pdl_wait() before reading anything that kernel writes.

@@ -45,6 +45,8 @@
 // rest of its work; the helper warp waits for the outstanding copies and
 // MMAs before the CTA frees its TMEM columns.
 #include <cuda.h>
+#include <cmath>
+#include <algorithm>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
@@ -211,6 +213,12 @@ struct TcArgs {
   float* partial;              // [ntok][nsplit][Rpad]
   int R, C, Rpad, nrb, S, ntok, N, nsplit, ntile, nblock;
   int use_tma;                 // 0: x rows not 16-byte aligned, staged with element loads
+  // BPDQ with a K split: the splits' partials are added inside the launch as
+  // fixed-point terms to accumulator words [ntok][Rpad] (the batch-1 scheme:
+  // the add that completes the count writes y and zeroes the word)
+  int fused;
+  unsigned long long* acc;
+  float fscale, finv;
 };
 
 constexpr uint32_t kHashHi = 0x9E37u << 16;     // trellis: (s*0x9E37 mod 2^16) in bits 16..31
@@ -643,6 +651,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
     for (int c0 = 0; c0 < a.N; c0 += 16) {
       float v[16];
       tmem_ld16(tlane + (uint32_t)c0, v);
+      if (FMT == Q2_BPDQ && a.fused) {
+        // 16 tokens' atomics in flight, then the completion checks
+        if (orow < a.Rpad) {
+          unsigned long long add[16], old[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (c0 + i < a.ntok) {
+              add[i] = fx_term(v[i], a.fscale);
+              old[i] = atomicAdd(a.acc + (size_t)(c0 + i) * a.Rpad + orow, add[i]);
+            }
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (c0 + i < a.ntok) {
+              const unsigned long long w = old[i] + add[i];
+              if ((int)(w >> 56) == a.nsplit) {
+                if (orow < a.R) a.y[(size_t)(c0 + i) * a.R + orow] = __float2half_rn(fx_value(w, a.nsplit, a.finv));
+                a.acc[(size_t)(c0 + i) * a.Rpad + orow] = 0ull;
+              }
+            }
+        }
+        continue;
+      }
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int t = c0 + i;
@@ -739,11 +769,23 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
     }
   }
   a.use_tma = encode_x_map(&a.xmap, x, d.C, ntok, a.N) ? 1 : 0;
+  // BPDQ with a K split reduces inside the launch when its accumulator words
+  // fit the workspace's reserve; the scale 2^F keeps a split's partial (at
+  // most its slices times the per-slice bound) below 2^46
+  a.fused = (FMT == Q2_BPDQ && a.nsplit > 1 && (size_t)ntok * d.Rpad <= (size_t)Q2_MAX_ACC_TOK * Q2_MAX_ROWS) ? 1 : 0;
+  if (a.fused) {
+    int e = 0;
+    if (h->pbound > 0.0) std::frexp(h->pbound * (double)((a.S + a.nsplit - 1) / a.nsplit), &e);
+    const int F = std::max(-100, std::min(100, 46 - e));
+    a.acc = static_cast<unsigned long long*>(h->ws);
+    a.fscale = std::ldexp(1.0f, F);
+    a.finv = std::ldexp(1.0f, -F);
+  }
   // table, 1024-byte alignment slack, B buffers, the stage mbarriers, TMEM slot
   const int smem = max(kOneCtaSmem, Sh::table + 1024 + kStagesB * Sh::atoms * a.N * 128 + (2 * kStagesA + kStagesB + 2) * 8 + 16);
   int st = launch_pdl(k_tc<FMT>, a, a.ntile * a.nsplit, kThreads, smem, stream);
   if (st) return st;
-  if (a.nsplit == 1 && FMT == Q2_BPDQ) return Q2_OK;
+  if (FMT == Q2_BPDQ && (a.nsplit == 1 || a.fused)) return Q2_OK;
   return q2_launch_reduce_n(h, x, y, ntok, a.nsplit, stream);
 }
 
