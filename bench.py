@@ -602,7 +602,10 @@ def main():
 
     achieved = step_bytes / (ms_step * 1e-3) / 1e9
     kname = "k_bpdq_b1" if args.ntok == 1 else ("k_bpdq_mt" if args.ntok <= 6 else "k_tc")
-    launches_per_gemv = 1 if args.ntok <= 6 else 2
+    # launches of one BPDQ GEMV: one at 1 token; token pairs plus a single
+    # token at 2..6; one tensor-core launch from 7 (the split-K reduction runs
+    # inside it for every shape of this stack)
+    launches_per_gemv = 1 if args.ntok == 1 else (args.ntok + 1) // 2 if args.ntok <= 6 else 1
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
