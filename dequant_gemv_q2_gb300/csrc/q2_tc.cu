@@ -21,8 +21,11 @@
 // MMAs to drain and leaves the tensor core idle (about 350 cycles per
 // access on GB300), so the MMA lane touches no memory at all.
 // At the end decoder warps 0..3 (one per TMEM lane quarter) read the
-// accumulator, each its 32 lanes = 32 rows, and write fp32 partial sums for
-// the split-K reduction kernel, or y directly.
+// accumulator, each its 32 lanes = 32 rows, and write y directly (one K
+// split), add it as fixed-point terms to the rows' accumulator words (BPDQ
+// with a K split; the completing add writes y), or write fp32 partial sums
+// for the split-K reduction kernel (trellis and Leech, whose epilogue needs
+// the row scale, tail and exceptions).
 //
 // TMEM columns (all 512 are allocated; one CTA per SM): D at 0 .. N - 1,
 // A of stage st at kAcol0 + st * (4 x K chunks); A column j of a lane holds
