@@ -126,8 +126,10 @@ void q2_unbind(q2_handle* h);
  * together with an arrival count, in one atomic, and the addition that
  * completes the count writes y and resets the word.  These words must be
  * zero when the workspace is first used (allocate it zero-filled); every
- * completed call leaves them at zero again.  The tensor-core path keeps
- * fp32 partial sums (nslice x ntok x Rpad floats) at byte offset
+ * completed call leaves them at zero again.  The tensor-core path adds BPDQ's
+ * K-split partials to the same words (one term per split) when ntok x Rpad
+ * <= 6 x 524288; otherwise, and for trellis and Leech, it keeps fp32
+ * partial sums (nslice x ntok x Rpad floats) at byte offset
  * 6 x 524288 x 8 (24 MiB), past any handle's accumulators, so one
  * workspace may serve many handles whose calls are ordered on one stream;
  * calls that overlap on the GPU must use different workspaces.  Limits:
@@ -153,10 +155,13 @@ int q2_bytes(const q2_handle* h, int ntok, size_t* weight_bytes_read_per_call);
  * token's BPDQ result at 1..6 tokens is bit-identical whatever the batch.
  * Leech at 2 tokens runs two single-token launches when C and R are
  * multiples of 8.  The tensor-core path (7..64 tokens, or 2..64 for trellis
- * and the other Leech cases) adds a second, in-order reduction launch.  The fixed-point scale 2^F is chosen per matrix from its
- * largest weight magnitude so that no fp16 x can overflow it; each slice's
- * partial then carries an absolute rounding error of at most 2^-(F+1),
- * about 1e-8 for weights of magnitude 0.05.  Launches use programmatic dependent launch: weights are
+ * and the other Leech cases) reduces BPDQ's K splits the same way inside its
+ * launch; trellis and Leech add a second, in-order reduction launch.  The
+ * fixed-point scale 2^F is chosen per matrix (and, on the tensor-core path,
+ * per K split) from its largest weight magnitude so that no fp16 x can
+ * overflow it; each term then carries an absolute rounding error of at most
+ * 2^-(F+1), about 1e-8 per 256-column slice for weights of magnitude
+ * 0.05.  Launches use programmatic dependent launch: weights are
  * fetched before the previous kernel on the stream has finished; x, y and
  * the workspace are touched only after it has.  Returns Q2_ECUDA if a
  * launch fails. */
