@@ -481,6 +481,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--ntok", type=int, default=1)
     ap.add_argument("--impl", default="q2", choices=["q2", "reference"])
+    ap.add_argument("--lookahead", type=int, default=0,
+                    help="q2_gemv_chain lookahead: GEMVs ahead whose weights each launch prefetches into L2")
     ap.add_argument("--no-extras", action="store_true", help="skip the per-format lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--profile-case", default=None,
@@ -540,8 +542,10 @@ def main():
         L["pk"].set_workspace(wsbuf)
         del L["blob"]
     step_bytes = sum(L["pk"].bytes_read(args.ntok) for L in lin)
-    calls = [lambda L=L: L["pk"].gemv(L["x"], L["y"]) for L in lin]
-    g = graph_of(calls, stream)
+    # the step is one q2_gemv_chain call: the 144 GEMVs in order, each launch
+    # prefetching the weights of the next `lookahead` into L2
+    chain = q2.Chain([(L["pk"], L["x"], L["y"]) for L in lin], args.ntok, args.lookahead)
+    g = graph_of([chain.run], stream)
 
     clk = Clocks(torch.cuda.current_device())
     clk.start()
@@ -614,7 +618,8 @@ def main():
             "data": "synthetic (seeded BPDQ weights and N(0,1) fp16 activations of the Qwen3-8B shapes)",
             "config": {"workload": "BPDQ Qwen3-8B-shaped decode stack: 36 layers x (qkv 4096->6144, o 4096->4096, "
                                    "gate_up 4096->24576, down 12288->4096), linears only",
-                       "ntok": args.ntok, "launches_per_step": len(lin) * launches_per_gemv,
+                       "ntok": args.ntok, "lookahead": args.lookahead,
+                       "launches_per_step": len(lin) * launches_per_gemv,
                        "bytes_per_step": step_bytes,
                        "l2": "weights 1.9 GB > L2, no flush", "parallelism": "replicas" if ws > 1 else "single"},
             "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,

@@ -59,6 +59,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "q2_gemv": [i32, vp, vp, vp, i32, vp],
         "q2_decode_bytes": [vp, psz],
         "q2_decode": [vp, vp, vp],
+        "q2_gemv_chain": [i32, vp, vp, vp, vp, i32, i32, vp],
         "q2_gemv_bpdq_noalloc": [vp, vp, vp, vp],
         "q2_device_errors": [ctypes.POINTER(ctypes.c_uint)],
         "q2_rotate": [vp, vp, i32, i32, i32, vp, vp, vp],
@@ -78,7 +79,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
 
 EXPORTS = ["q2_pack_fp16", "q2_pack_bpdq", "q2_pack_trellis", "q2_pack_leech", "q2_pack_noweights",
            "q2_bind", "q2_unbind", "q2_workspace_bytes", "q2_set_workspace", "q2_info", "q2_bytes",
-           "q2_gemv", "q2_decode_bytes", "q2_decode", "q2_strerror", "q2_gemv_bpdq_noalloc",
+           "q2_gemv", "q2_gemv_chain", "q2_decode_bytes", "q2_decode", "q2_strerror", "q2_gemv_bpdq_noalloc",
            "q2_device_errors", "q2_rotate", "q2_rotate_split"]
 
 
@@ -235,6 +236,29 @@ def q2_gemv(fmt: int, packed: Packed, x, y, ntok: int, stream=None) -> int:
     """The C entry point with its own argument order (status returned)."""
     return load().q2_gemv(int(fmt), packed.h, ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()),
                           int(ntok), _stream_ptr(stream))
+
+
+class Chain:
+    """A decode step's chain of GEMVs run through q2_gemv_chain.
+
+    ``links`` is a list of (Packed, x, y) with device fp16 tensors x [ntok][C]
+    and y [ntok][R]; the pointer arrays are built once, so ``run`` only makes
+    the one C call (and may be captured in a CUDA graph).
+    """
+
+    def __init__(self, links, ntok: int, lookahead: int = 2):
+        n = len(links)
+        self.links = list(links)            # keeps the tensors alive
+        self.ntok, self.lookahead = int(ntok), int(lookahead)
+        self._fmt = (ctypes.c_int * n)(*[p.fmt for p, _, _ in links])
+        self._h = (ctypes.c_void_p * n)(*[p.h.value for p, _, _ in links])
+        self._x = (ctypes.c_void_p * n)(*[x.data_ptr() for _, x, _ in links])
+        self._y = (ctypes.c_void_p * n)(*[y.data_ptr() for _, _, y in links])
+
+    def run(self, stream=None) -> None:
+        st = load().q2_gemv_chain(len(self.links), self._fmt, self._h, self._x, self._y, self.ntok, self.lookahead,
+                                  _stream_ptr(stream))
+        _check(st, "q2_gemv_chain")
 
 
 def q2_rotate_split(C: int) -> tuple:

@@ -53,6 +53,7 @@ struct B1 {
   float fscale, finv;           // 2^F and 2^-F of the fixed-point partials
   int R, C, Rpad, nrb, nslice, ntok;
   int aligned;                  // 1: slice-aligned CTA ranges, 0: equal contiguous ranges
+  q2_pf pf;                     // weights of later launches to fetch into L2 (zero lengths: none)
 };
 
 // Shared memory of the single-token table kernels: a small tail at the
@@ -240,6 +241,21 @@ __device__ __forceinline__ void b1_range(const B1& c, int& i0, int& i1) {
   }
 }
 
+// This CTA's 1/grid share of each range in c.pf, fetched into L2 by one
+// thread with bulk prefetches: the weights of the launches that follow
+// stream from HBM while this launch and its successors run their
+// latency-bound prologues and reductions.
+__device__ __forceinline__ void prefetch_next(const q2_pf& pf) {
+  const unsigned long long G = gridDim.x, b = blockIdx.x;
+#pragma unroll
+  for (int r = 0; r < Q2_PF_SLOTS; ++r) {
+    const unsigned long long n16 = pf.len[r] >> 4;        // whole 16-byte units
+    if (!n16) continue;
+    const unsigned long long u0 = n16 * b / G, u1 = n16 * (b + 1) / G;
+    if (u1 > u0) prefetch_l2(pf.ptr[r] + u0 * 16, (size_t)(u1 - u0) * 16);
+  }
+}
+
 // ------------------------------------------------------- pipelined items
 // run_b1 drives every split-K kernel.  The CTA's item range (b1_range) is
 // cut into groups: one slice per group for the table kernels (F::kGroup ==
@@ -274,6 +290,7 @@ __device__ __forceinline__ void run_b1(F& f, const B1& c, unsigned char* tail) {
     for (int d = 0; d < AHEAD; ++d)
       if (it0 + d * W < j1) f.load(it0 + d * W, slice_of(it0 + d * W), lane, buf[d]);
     if (!waited) {
+      if (threadIdx.x == 0) prefetch_next(c.pf);
       pdl_wait();
       pdl_trigger();
       waited = true;
@@ -308,6 +325,7 @@ __device__ __forceinline__ void run_b1(F& f, const B1& c, unsigned char* tail) {
     j0 = j1;
   }
   if (!waited) {
+    if (threadIdx.x == 0) prefetch_next(c.pf);
     pdl_wait();
     pdl_trigger();
   }
@@ -515,6 +533,230 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks) k_noweights_b1(BpdqArgs a)
   if ((uint32_t)__cvta_generic_to_shared(q2_smem) + kTailFixed > kTabAddr) return;   // layout needs a low window base
   NoWeightsF<W * 32> f{a};
   run_b1<W, 1>(f, a.c, tail1());
+}
+
+// ------------------------------------------------ BPDQ, one token (lean)
+// The single-token BPDQ GEMV and its no-weights control.  Same work unit,
+// tables and reduction as run_b1, but written for the fewest instructions
+// per item, because at one token the item loop is bound by issue and
+// shared-memory throughput rather than by HBM (measured on GB300: a
+// 24576x4096 GEMV whose weights are all in L2 is no faster than one
+// reading them from HBM):
+//   - the CTA's item range comes from the host in the parameter block
+//     (the slice-aligned split of run_b1's b1_range, computed once per
+//     launch), so no warp spends its prologue on integer divisions;
+//   - each warp walks its items with pointers advanced by a constant
+//     stride instead of recomputing 64-bit addresses per item;
+//   - the lookups of plane 0 and plane 1 at the same rotated position are
+//     added as one packed fp32 pair, into four pair accumulators (lookup P
+//     into accumulator P mod 4, then (s0 + s1) + (s2 + s3)): per plane the
+//     same operations in the same order as plane_sum, so the result is
+//     bit-identical to run_b1's and to the token-pair kernel's;
+//   - x is read straight from global memory by the table build (16 tasks
+//     share each 16-byte load), without a staging pass.
+constexpr int kLeanMaxGrid = 192;
+#ifndef Q2_LEAN_W
+#define Q2_LEAN_W 24
+#endif
+#ifndef Q2_LEAN_MB
+#define Q2_LEAN_MB 1
+#endif
+constexpr int kLeanW = Q2_LEAN_W;        // warps per CTA
+constexpr int kLeanMinBlocks = Q2_LEAN_MB;
+
+struct LeanArgs {
+  const __half* x;              // [C]
+  __half* y;                    // [R]
+  unsigned long long* acc;      // [Rpad] accumulator words (zero between calls)
+  const uint4* bits;            // item-major planes (see q2_layout.h)
+  const uint32_t* c01;          // [nslice][Rpad] c0 | c1 << 16 (fp16)
+  const unsigned short* off;    // [nslice][Rpad] fp16
+  float fscale, finv;
+  int R, C, Rpad, nrb, nslice;
+  q2_pf pf;
+  uint32_t pfq, pfr;            // slot 0 of pf in 16-byte units over grid x W warps: quotient, remainder
+  uint32_t start[kLeanMaxGrid + 1];   // CTA b owns items [start[b], start[b+1])
+};
+
+struct LeanItem {
+  uint4 w[4];            // plane 0: w[0], w[1]; plane 1: w[2], w[3]
+  uint32_t c01;
+  unsigned short off;
+};
+
+// Lookup P of both planes into pair accumulator P mod 4, then the rest.
+template <int P>
+__device__ __forceinline__ void pair_steps(uint32_t lane4, const uint32_t (&w0)[8], const uint32_t (&w1)[8],
+                                           float2 (&s)[4]) {
+  if constexpr (P < 32) {
+    s[P & 3] = __fadd2_rn(s[P & 3], make_float2(tl<P>(lane4, w0[P >> 2]), tl<P>(lane4, w1[P >> 2])));
+    pair_steps<P + 1>(lane4, w0, w1, s);
+  }
+}
+
+// (sum of plane 0's 32 lookups, sum of plane 1's)
+__device__ __forceinline__ float2 planes_sum(uint32_t lane4, const uint4& a0, const uint4& a1, const uint4& b0,
+                                             const uint4& b1) {
+  const uint32_t w0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+  const uint32_t w1[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+  float2 s[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  pair_steps<0>(lane4, w0, w1, s);
+  return __fadd2_rn(__fadd2_rn(s[0], s[1]), __fadd2_rn(s[2], s[3]));
+}
+
+template <bool kWeights>
+__device__ __forceinline__ void lean_load(const LeanArgs& a, const uint4* wp, size_t ci, int it, int lane,
+                                          LeanItem& b) {
+  if constexpr (kWeights) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) b.w[k] = ldg_stream(wp + k * 32);
+    b.c01 = __ldg(a.c01 + ci);
+    b.off = __ldg(a.off + ci);
+  } else {
+    // the no-weights control: "weights" derived from the item and lane
+    const uint32_t h = (uint32_t)it * 0x9E3779B9u ^ ((uint32_t)lane * 0x85EBCA6Bu);
+    b.w[0] = make_uint4(h, h ^ 0x5bd1e995u, h * 3u, h * 5u);
+    b.w[1] = make_uint4(h * 7u, h ^ 0x27d4eb2fu, h * 11u, h * 13u);
+    b.w[2] = b.w[1];
+    b.w[3] = b.w[0];
+    b.c01 = 0x211F251Fu;      // fp16 (0.02, 0.01)
+    b.off = 0x211Fu;          // fp16 0.01
+  }
+}
+
+__device__ __forceinline__ float lean_partial(uint32_t lane4, const LeanItem& b, float gs) {
+  const float2 S = planes_sum(lane4, b.w[0], b.w[1], b.w[2], b.w[3]);
+  const float2 cf = __half22float2(*reinterpret_cast<const __half2*>(&b.c01));
+  const float of = __half2float(__ushort_as_half(b.off));
+  return fmaf(cf.x, S.x, fmaf(cf.y, S.y, of * gs));
+}
+
+// The weights of a later GEMV (c.pf slot 0), fetched into L2 a piece per
+// item: warp w of CTA b owns 1/(grid*W) of the range and issues it in as
+// many pieces as it has items, one after each item's own loads, so the
+// extra HBM traffic is spread over the GEMV instead of queueing ahead of
+// its loads in one burst (a burst at launch start made every GEMV of a
+// stack slower on GB300).  Other slots, and warps without items, issue
+// their share at once.
+struct PacedPf {
+  const unsigned char* cur;
+  uint32_t left, piece;
+  __device__ __forceinline__ void step(int lane) {
+    if (left) {
+      const uint32_t n = left < piece ? left : piece;
+      if (lane == 0) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cur), "r"(n) : "memory");
+      cur += n;
+      left -= n;
+    }
+  }
+};
+
+// Warp k = b*W + w of the grid gets 16-byte units [k*q + min(k, r), ...) of
+// slot 0, q and r being the quotient and remainder of its units over all
+// warps (computed on the host).
+__device__ __forceinline__ PacedPf paced_share(const q2_pf& pf, uint32_t q, uint32_t r, int warp, int W, int nitems) {
+  PacedPf p;
+  const uint32_t k = blockIdx.x * (uint32_t)W + (uint32_t)warp;
+  const uint32_t u0 = k * q + min(k, r), n = q + (k < r ? 1u : 0u);
+  p.cur = pf.ptr[0] + (size_t)u0 * 16;
+  p.left = n * 16;
+  const uint32_t m = nitems > 0 ? (uint32_t)nitems : 1u;
+  p.piece = p.left ? min(65536u, ((p.left + m - 1) / m + 15) / 16 * 16) : 0u;
+  return p;
+}
+
+struct LeanPending {
+  unsigned long long old, add;
+  unsigned long long* p;
+  int row;               // -1: nothing pending
+};
+
+__device__ __forceinline__ void lean_settle(LeanPending& pd, const LeanArgs& a) {
+  if (pd.row < 0) return;
+  const unsigned long long w = pd.old + pd.add;
+  if ((int)(w >> 56) == a.nslice) {                   // this lane completed the row
+    if (pd.row < a.R) a.y[pd.row] = __float2half_rn(fx_value(w, a.nslice, a.finv));
+    *pd.p = 0ull;
+  }
+  pd.row = -1;
+}
+
+template <int W, bool kWeights, bool kPaced>
+__global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_constant__ LeanArgs a) {
+  if ((uint32_t)__cvta_generic_to_shared(q2_smem) + kTailFixed > kTabAddr) return;   // layout needs a low window base
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t lane4 = (uint32_t)lane * 4u;
+  const int i0 = (int)a.start[blockIdx.x], i1 = (int)a.start[blockIdx.x + 1];
+  float* gsum = reinterpret_cast<float*>(q2_smem + kTailGsum);
+  LeanPending pd;
+  pd.row = -1;
+  bool waited = false;
+  PacedPf pp;
+  pp.left = 0;
+  if constexpr (kPaced) pp = paced_share(a.pf, a.pfq, a.pfr, warp, W, (i1 - i0 - warp + W - 1) / W);
+  int g = i0 / a.nrb;
+  for (int j0 = i0; j0 < i1; ++g) {
+    const int j1 = min(i1, (g + 1) * a.nrb);
+    int it = j0 + warp;
+    const int rb = it - g * a.nrb;
+    const uint4* wp = a.bits + (size_t)it * (Q2_ITEM_BYTES_BPDQ / 16) + lane;
+    size_t ci = (size_t)g * a.Rpad + (size_t)rb * 32 + lane;
+    unsigned long long* ap = a.acc + (size_t)rb * 32 + lane;
+    int row = rb * 32 + lane;
+    LeanItem b0, b1;
+    if (it < j1) lean_load<kWeights>(a, wp, ci, it, lane, b0);
+    if (!waited) {
+      if (threadIdx.x == 0) {                           // slots past the first: at once
+        q2_pf rest = a.pf;
+        rest.len[0] = 0;
+        prefetch_next(rest);
+      }
+      if (kPaced && it >= j1) pp.step(lane);            // no items: the whole share now
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    } else {
+      __syncthreads();                                  // the previous slice's table is no longer read
+    }
+    q2::build_table<W * 32>(a.x + (size_t)g * Q2_SLICE, a.C - g * Q2_SLICE, tab1(), gsum);
+    __syncthreads();
+    const float gs = *gsum;
+    constexpr int kStrideW = W * (Q2_ITEM_BYTES_BPDQ / 16);
+    // two items per trip so the two buffers are named statically
+    for (; it < j1; it += 2 * W) {
+      const bool m1 = it + W < j1;
+      if (m1) lean_load<kWeights>(a, wp + kStrideW, ci + W * 32, it + W, lane, b1);
+      if constexpr (kPaced) pp.step(lane);
+      float p = lean_partial(lane4, b0, gs);
+      lean_settle(pd, a);
+      pd.add = fx_term(p, a.fscale);
+      pd.old = atomicAdd(ap, pd.add);
+      pd.p = ap;
+      pd.row = row;
+      if (!m1) break;
+      const bool m2 = it + 2 * W < j1;
+      if (m2) lean_load<kWeights>(a, wp + 2 * kStrideW, ci + 2 * W * 32, it + 2 * W, lane, b0);
+      if constexpr (kPaced) pp.step(lane);
+      p = lean_partial(lane4, b1, gs);
+      lean_settle(pd, a);
+      pd.add = fx_term(p, a.fscale);
+      pd.old = atomicAdd(ap + W * 32, pd.add);
+      pd.p = ap + W * 32;
+      pd.row = row + W * 32;
+      wp += 2 * kStrideW;
+      ci += 2 * W * 32;
+      ap += 2 * W * 32;
+      row += 2 * W * 32;
+    }
+    j0 = j1;
+  }
+  if (!waited) {
+    if (threadIdx.x == 0) prefetch_next(a.pf);
+    pdl_wait();
+    pdl_trigger();
+  }
+  pp.left = 0;
+  lean_settle(pd, a);
 }
 
 // ------------------------------------------------- BPDQ, 2 to 6 tokens
@@ -778,9 +1020,11 @@ Geo geometry(const q2_blob_header& d) {
 // workspace at most Q2_MAX_ROWS rows per token.
 bool b1_shape_ok(const q2_blob_header& d) { return d.nslice >= 1 && d.nslice <= Q2_MAX_SPLIT && d.Rpad <= Q2_MAX_ROWS; }
 
-B1 make_b1(const q2_handle* h, const void* x, void* y, int ntok) {
+B1 make_b1(const q2_handle* h, const void* x, void* y, int ntok, const q2_pf* pf = nullptr) {
   const q2_blob_header& d = h->hdr;
   B1 c;
+  if (pf) c.pf = *pf;
+  else c.pf = q2_pf{};
   c.aligned = (d.fmt == Q2_BPDQ || d.fmt == Q2_NOWEIGHTS) ? 1 : 0;
   c.x = static_cast<const __half*>(x);
   c.y = static_cast<__half*>(y);
@@ -807,24 +1051,63 @@ int launch1(void (*kernel)(A), const A& args, const Geo& g, int threads, int tab
   return launch_pdl(kernel, args, g.grid, threads, smem, stream);
 }
 
+// The lean single-token kernel's arguments: the pointers and scalars of
+// make_b1, and each CTA's slice-aligned item range (b1_range, aligned mode).
+LeanArgs make_lean(const q2_handle* h, const void* x, void* y, const q2_pf* pf, int grid) {
+  const q2_blob_header& d = h->hdr;
+  const B1 c = make_b1(h, x, y, 1, pf);
+  LeanArgs a;
+  a.x = c.x;
+  a.y = c.y;
+  a.acc = c.acc;
+  a.bits = reinterpret_cast<const uint4*>(h->dev + d.off[SEC_BPDQ_BITS]);
+  a.c01 = reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_BPDQ_C01]);
+  a.off = reinterpret_cast<const unsigned short*>(h->dev + d.off[SEC_BPDQ_OFF]);
+  a.fscale = c.fscale;
+  a.finv = c.finv;
+  a.R = c.R;
+  a.C = c.C;
+  a.Rpad = c.Rpad;
+  a.nrb = c.nrb;
+  a.nslice = c.nslice;
+  a.pf = c.pf;
+  const unsigned long long units = a.pf.len[0] >> 4, parts = (unsigned long long)grid * kLeanW;
+  a.pfq = (uint32_t)(units / parts);
+  a.pfr = (uint32_t)(units % parts);
+  const int ns = c.nslice, nrb = c.nrb, G = grid;
+  for (int b = 0; b < G; ++b) {
+    int i0;
+    if (ns <= G) {
+      const int g = b * ns / G;
+      const int first = (g * G + ns - 1) / ns, last = ((g + 1) * G + ns - 1) / ns;
+      i0 = g * nrb + (b - first) * nrb / (last - first);
+    } else {
+      i0 = b * ns / G * nrb;
+    }
+    a.start[b] = (uint32_t)i0;
+  }
+  a.start[G] = (uint32_t)(ns * nrb);
+  return a;
+}
+
+int lean_grid(const q2_blob_header& d) { return std::min(geometry(d).grid, kLeanMaxGrid); }
+
 }  // namespace
 }  // namespace q2
 
 using namespace q2;
 
-extern "C" int q2_b1_bpdq(const q2_handle* h, const void* x, void* y, void* stream) {
+extern "C" int q2_b1_bpdq(const q2_handle* h, const void* x, void* y, void* stream, const q2_pf* pf) {
   const q2_blob_header& d = h->hdr;
   if (!b1_shape_ok(d)) return Q2_ESHAPE;
-  BpdqArgs a;
-  a.c = make_b1(h, x, y, 1);
-  a.bits = h->dev + d.off[SEC_BPDQ_BITS];
-  a.c01 = reinterpret_cast<const __half2*>(h->dev + d.off[SEC_BPDQ_C01]);
-  a.off = reinterpret_cast<const __half*>(h->dev + d.off[SEC_BPDQ_OFF]);
-  return launch1(k_bpdq_b1<kWarps, kBpdqAhead>, a, geometry(d), kWarps * 32, kTabSmem, stream);
+  const int G = lean_grid(d);
+  const LeanArgs a = make_lean(h, x, y, pf, G);
+  if (a.pf.len[0]) return launch_pdl(k_bpdq1<kLeanW, true, true>, a, G, kLeanW * 32, kTabSmem, stream);
+  return launch_pdl(k_bpdq1<kLeanW, true, false>, a, G, kLeanW * 32, kTabSmem, stream);
 }
 
 // BPDQ at 2..6 tokens on CUDA cores (x is [ntok][C]; partials [ntok][nslice][Rpad]).
-extern "C" int q2_mt_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
+extern "C" int q2_mt_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream, const q2_pf* pf) {
   const q2_blob_header& d = h->hdr;
   if (ntok < 2 || ntok > kMtMaxTok) return Q2_ENTOK;
   if (!b1_shape_ok(d)) return Q2_ESHAPE;
@@ -845,28 +1128,29 @@ extern "C" int q2_mt_bpdq(const q2_handle* h, const void* x, void* y, int ntok, 
   for (int t = 0; t < ntok; t += 2) {
     int st;
     if (t + 1 < ntok) {
-      a.c = make_b1(h, xh + (size_t)t * d.C, yh + (size_t)t * d.R, 2);
+      a.c = make_b1(h, xh + (size_t)t * d.C, yh + (size_t)t * d.R, 2, t == 0 ? pf : nullptr);
       st = launch1(k_bpdq_mt<kWarps, 2, 1>, a, g, kWarps * 32, 1 * kPairBytes, stream);
     } else {
-      st = q2_b1_bpdq(h, xh + (size_t)t * d.C, yh + (size_t)t * d.R, stream);
+      st = q2_b1_bpdq(h, xh + (size_t)t * d.C, yh + (size_t)t * d.R, stream, t == 0 ? pf : nullptr);
     }
     if (st) return st;
   }
   return Q2_OK;
 }
 
-extern "C" int q2_b1_noweights(const q2_handle* h, const void* x, void* y, void* stream) {
+extern "C" int q2_b1_noweights(const q2_handle* h, const void* x, void* y, void* stream, const q2_pf* pf) {
   if (!b1_shape_ok(h->hdr)) return Q2_ESHAPE;
-  BpdqArgs a = {};
-  a.c = make_b1(h, x, y, 1);
-  return launch1(k_noweights_b1<kWarps>, a, geometry(h->hdr), kWarps * 32, kTabSmem, stream);
+  const int G = lean_grid(h->hdr);
+  const LeanArgs a = make_lean(h, x, y, pf, G);
+  if (a.pf.len[0]) return launch_pdl(k_bpdq1<kLeanW, false, true>, a, G, kLeanW * 32, kTabSmem, stream);
+  return launch_pdl(k_bpdq1<kLeanW, false, false>, a, G, kLeanW * 32, kTabSmem, stream);
 }
 
-extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* stream) {
+extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* stream, const q2_pf* pf) {
   const q2_blob_header& d = h->hdr;
   if (!b1_shape_ok(d)) return Q2_ESHAPE;
   LeechArgs a;
-  a.c = make_b1(h, x, y, 1);
+  a.c = make_b1(h, x, y, 1, pf);
   a.planes = h->dev + d.off[SEC_LEECH_PLANES];
   a.parity = reinterpret_cast<const uint16_t*>(h->dev + d.off[SEC_LEECH_PARITY]);
   a.scale = reinterpret_cast<const __half*>(h->dev + d.off[SEC_LEECH_SCALE]);
@@ -880,11 +1164,11 @@ extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* str
   return launch1(k_leech_b1<kWarps, kLeechAhead>, a, geometry(d), kWarps * 32, kTabSmem, stream);
 }
 
-extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* stream) {
+extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* stream, const q2_pf* pf) {
   const q2_blob_header& d = h->hdr;
   if (!b1_shape_ok(d)) return Q2_ESHAPE;
   TrellisArgs a;
-  a.c = make_b1(h, x, y, 1);
+  a.c = make_b1(h, x, y, 1, pf);
   a.stream = h->dev + d.off[SEC_TRL_STREAM];
   a.table = reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_TRL_TABLE]);
   a.scale = reinterpret_cast<const __half*>(h->dev + d.off[SEC_TRL_SCALE]);
@@ -955,5 +1239,5 @@ extern "C" int q2_gemv_bpdq_noalloc(const q2_handle* h, const void* x, void* y, 
   q2_handle view = *h;
   view.ws = scratch;
   view.ws_bytes = Q2_NOALLOC_SCRATCH_BYTES;
-  return q2_b1_bpdq(&view, x, y, static_cast<void*>(stream));
+  return q2_b1_bpdq(&view, x, y, static_cast<void*>(stream), nullptr);
 }

@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreads) k_fp16_mt(DenseArgs a) {
 
 using namespace q2;
 
-extern "C" int q2_launch_fp16(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
+extern "C" int q2_launch_fp16(const q2_handle* h, const void* x, void* y, int ntok, void* stream, const q2_pf*) {
   const q2_blob_header& d = h->hdr;
   DenseArgs a;
   a.w = reinterpret_cast<const __half*>(h->dev + d.off[SEC_FP16_W]);

@@ -461,7 +461,8 @@ int q2_decode_bytes(const q2_handle* h, size_t* bytes) {
   return Q2_OK;
 }
 
-int q2_gemv(q2_fmt fmt, const q2_handle* h, const void* x, void* y, int ntok, q2_stream stream) {
+static int gemv_impl(q2_fmt fmt, const q2_handle* h, const void* x, void* y, int ntok, q2_stream stream,
+                     const q2_pf* pf) {
   if (!h || !x || !y) return Q2_EINVAL;
   if ((int)fmt != h->hdr.fmt) return Q2_EFMT;
   if (ntok < 1 || ntok > Q2_MAX_NTOK) return Q2_ENTOK;
@@ -473,13 +474,60 @@ int q2_gemv(q2_fmt fmt, const q2_handle* h, const void* x, void* y, int ntok, q2
   if (h->hdr.Rpad > Q2_MAX_ROWS || h->hdr.nslice > Q2_MAX_SPLIT) return Q2_ESHAPE;
   void* s = static_cast<void*>(stream);
   switch (h->hdr.fmt) {
-    case Q2_FP16: return q2_launch_fp16(h, x, y, ntok, s);
-    case Q2_BPDQ: return q2_launch_bpdq(h, x, y, ntok, s);
-    case Q2_TRELLIS: return q2_launch_trellis(h, x, y, ntok, s);
-    case Q2_LEECH: return q2_launch_leech(h, x, y, ntok, s);
-    case Q2_NOWEIGHTS: return q2_launch_noweights(h, x, y, ntok, s);
+    case Q2_FP16: return q2_launch_fp16(h, x, y, ntok, s, pf);
+    case Q2_BPDQ: return q2_launch_bpdq(h, x, y, ntok, s, pf);
+    case Q2_TRELLIS: return q2_launch_trellis(h, x, y, ntok, s, pf);
+    case Q2_LEECH: return q2_launch_leech(h, x, y, ntok, s, pf);
+    case Q2_NOWEIGHTS: return q2_launch_noweights(h, x, y, ntok, s, pf);
     default: return Q2_EFMT;
   }
+}
+
+int q2_gemv(q2_fmt fmt, const q2_handle* h, const void* x, void* y, int ntok, q2_stream stream) {
+  return gemv_impl(fmt, h, x, y, ntok, stream, nullptr);
+}
+
+// The device bytes a GEMV of h reads at ntok tokens on the CUDA-core path,
+// as one range from its first weight section to the end of the last one it
+// reads (the holes between sections are alignment padding, under 256 bytes
+// each).  Zero length for the no-weights control.
+static void weight_range(const q2_handle* h, int ntok, const unsigned char** p, unsigned long long* n) {
+  const q2_blob_header& d = h->hdr;
+  int last = -1;
+  switch (d.fmt) {
+    case Q2_FP16: last = SEC_FP16_W; break;
+    case Q2_BPDQ: last = ntok <= Q2_MAX_ACC_TOK ? SEC_BPDQ_OFF : -1; break;
+    case Q2_TRELLIS: last = ntok == 1 ? SEC_TRL_SCALE : -1; break;
+    case Q2_LEECH: last = ntok == 1 ? SEC_LEECH_EXCCOL : -1; break;
+    default: last = -1;
+  }
+  *p = h->dev + d.off[0];
+  *n = 0;
+  for (int s = last; s >= 0; --s)
+    if (d.len[s]) {                       // the last non-empty section ends the range
+      *n = (d.off[s] + d.len[s] - d.off[0]) / 16 * 16;
+      break;
+    }
+}
+
+int q2_gemv_chain(int n, const q2_fmt* fmt, q2_handle* const* h, const void* const* x, void* const* y, int ntok,
+                  int lookahead, q2_stream stream) {
+  if (n < 0 || (n > 0 && (!fmt || !h || !x || !y))) return Q2_EINVAL;
+  if (lookahead < 0 || lookahead > Q2_PF_SLOTS) return Q2_EINVAL;
+  for (int i = 0; i < n; ++i) {               // refuse the whole chain before launching any of it
+    if (!h[i] || !x[i] || !y[i]) return Q2_EINVAL;
+    if ((int)fmt[i] != h[i]->hdr.fmt) return Q2_EFMT;
+  }
+  for (int i = 0; i < n; ++i) {
+    // launch 0 fetches GEMVs 1..lookahead, launch i > 0 only GEMV i + lookahead
+    // (the ones in between were fetched by the launches before it)
+    q2_pf pf = {};
+    for (int k = (i == 0 ? 1 : lookahead), slot = 0; k <= lookahead && i + k < n; ++k, ++slot)
+      weight_range(h[i + k], ntok, &pf.ptr[slot], &pf.len[slot]);
+    const int st = gemv_impl(fmt[i], h[i], x[i], y[i], ntok, stream, lookahead ? &pf : nullptr);
+    if (st) return st;
+  }
+  return Q2_OK;
 }
 
 int q2_decode(const q2_handle* h, void* out_dev, q2_stream stream) {

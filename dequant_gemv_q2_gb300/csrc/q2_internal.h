@@ -13,16 +13,26 @@ struct q2_handle {
 
 static inline int q2_nrb(const q2_blob_header& h) { return h.Rpad / Q2_ROWS; }
 
+// Device byte ranges a launch prefetches into L2 for the launches after it
+// (q2_gemv_chain); each CTA issues its 1/grid share of every range.  Ranges
+// start 16-byte aligned; a zero length is an unused slot.
+#define Q2_PF_SLOTS 4
+struct q2_pf {
+  const unsigned char* ptr[Q2_PF_SLOTS];
+  unsigned long long len[Q2_PF_SLOTS];
+};
+
 
 #ifdef __cplusplus
 extern "C" {
 #endif
 // Launchers (CUDA side).  Each returns a q2 status.
-int q2_launch_fp16(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
-int q2_launch_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
-int q2_launch_trellis(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
-int q2_launch_leech(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
-int q2_launch_noweights(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
+// pf: ranges to prefetch into L2 (batch-1 launches only), or NULL.
+int q2_launch_fp16(const q2_handle* h, const void* x, void* y, int ntok, void* stream, const q2_pf* pf);
+int q2_launch_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream, const q2_pf* pf);
+int q2_launch_trellis(const q2_handle* h, const void* x, void* y, int ntok, void* stream, const q2_pf* pf);
+int q2_launch_leech(const q2_handle* h, const void* x, void* y, int ntok, void* stream, const q2_pf* pf);
+int q2_launch_noweights(const q2_handle* h, const void* x, void* y, int ntok, void* stream, const q2_pf* pf);
 int q2_launch_decode(const q2_handle* h, void* out, void* stream);
 #ifdef __cplusplus
 }

@@ -167,6 +167,31 @@ int q2_bytes(const q2_handle* h, int ntok, size_t* weight_bytes_read_per_call);
  * launch fails. */
 int q2_gemv(q2_fmt fmt, const q2_handle* h, const void* x, void* y, int ntok, q2_stream stream);
 
+/* A decode step's chain of GEMVs: for i = 0..n-1, y[i] = W_i x[i] with W_i
+ * the packed matrix of h[i] (format fmt[i]), all at ntok tokens, launched in
+ * order on `stream` exactly as n q2_gemv calls would be (each launch reads
+ * x[i] only after the launch before it has finished, so x[i+1] may be
+ * computed from y[i] by the caller's own kernels in between, or be y[i]).
+ * The difference is the weight stream: on the CUDA-core paths (BPDQ at
+ * 1..6 tokens, trellis and Leech at 1 token) launch i also fetches the
+ * weights of GEMV i + lookahead (launch 0: GEMVs 1..lookahead; lookahead
+ * 0..4) from HBM into L2, each of its CTAs a 1/grid share, so that every
+ * GEMV's weights are requested once, `lookahead` launches before its own,
+ * and those bytes arrive while the
+ * launches before them run their latency-bound parts (the wait for the
+ * previous launch, staging x, building the slice tables, the split-K
+ * atomics).  This is the cross-matmul prefetch of "Qwen3-8B -- 2-bit BPDQ
+ * (packed)", Kernels (at up to 8 tokens a second stream loads each weight
+ * matrix into L2 two matmuls ahead of its use, paced by a progress flag);
+ * here the launch order itself paces it, so nothing waits on a flag.
+ * Results are bit-identical to the same q2_gemv calls.  Every handle needs
+ * its workspace as for q2_gemv (handles may share one workspace: the calls
+ * are ordered).  All handles and pointers are checked before anything is
+ * launched; a launch failure returns its status with the launches before
+ * it already enqueued.  lookahead == 0 is exactly n q2_gemv calls. */
+int q2_gemv_chain(int n, const q2_fmt* fmt, q2_handle* const* h, const void* const* x, void* const* y, int ntok,
+                  int lookahead, q2_stream stream);
+
 /* Allocation-free y = W x for a BPDQ handle at one token (no counterpart on
  * the source pages; an addition of this library).  For callers that cannot
  * allocate device memory when they run the GEMV: code running under CUDA

@@ -147,6 +147,18 @@ def test_status_codes(q2):
     assert L.q2_gemv(1, h, ctypes.c_void_p((1 << 21) + 2), x, 1, None) == -3  # alignment
     assert L.q2_gemv(1, h, x, x, 1, None) == -7                              # no workspace
     assert L.q2_strerror(-7) == b"workspace missing or too small"
+    # the chain checks every link before it launches anything
+    fmts = (ctypes.c_int * 2)(1, 1)
+    hs = (ctypes.c_void_p * 2)(h.value, h.value)
+    xs = (ctypes.c_void_p * 2)(1 << 21, 1 << 21)
+    assert L.q2_gemv_chain(0, None, None, None, None, 1, 2, None) == 0                 # empty chain
+    assert L.q2_gemv_chain(2, fmts, hs, xs, xs, 1, 5, None) == -1                      # lookahead > 4
+    assert L.q2_gemv_chain(2, fmts, hs, xs, xs, 1, -1, None) == -1
+    assert L.q2_gemv_chain(2, fmts, None, xs, xs, 1, 2, None) == -1
+    fmts[1] = 2
+    assert L.q2_gemv_chain(2, fmts, hs, xs, xs, 1, 2, None) == -4                      # fmt of link 1
+    fmts[1] = 1
+    assert L.q2_gemv_chain(2, fmts, hs, xs, xs, 1, 2, None) == -7                      # no workspace
     L.q2_unbind(h)
 
 
