@@ -1,10 +1,12 @@
 """Benchmark: one decode step of a synthetic Qwen3-8B-shaped BPDQ stack.
 
 A step is every linear of 36 layers (qkv 4096->6144, o 4096->4096, gate_up
-4096->24576, down 12288->4096) at ntok tokens: 144 q2_gemv launches through
-the C ABI, captured once in a CUDA graph and replayed.  Weights (1.90 GB
-packed) and activations are resident in HBM; the weights are larger than L2,
-so no flush is needed between steps.  Prints one JSON line.
+4096->24576, down 12288->4096) at ntok tokens: 144 GEMVs through the C ABI
+(one q2_gemv_chain call), captured once in a CUDA graph and replayed.  The
+weights (1.90 GB packed) are resident in HBM and larger than L2, so no flush
+is needed between steps; the activations are one input and one output
+buffer per projection, shared by the layers as an engine's activation
+buffers are.  Prints one JSON line.
 
 Besides the headline, the line carries per-format GEMV timings at the other
 configurations (trellis 12288x4096 and 4096x12288, Leech 17408x5120 and
@@ -13,6 +15,17 @@ each cycling enough distinct copies of its matrix to exceed L2 several times.
 
 --impl reference times the CPU oracle (decode + f64 matvec) on a bounded
 sample of the same workload and reports the same metric.
+
+The JSON line ends with the other configurations, compact (lists are
+[us or ms, GB/s or tok/s, fraction of the measured HBM bandwidth]):
+  "stack8b":  the 8B stack at 1, 4 and 16 tokens  [ms/step, tok/s, frac]
+  "sweep14b": the 14B stack (40 layers, 4 distinct layer copies cycled) per
+              format at 1, 16 and 64 tokens        [ms/step, tok/s, frac]
+  "fmt":      single GEMVs at batch 1 per format and shape, each cycling
+              copies of its matrix over >= 4x L2   [us, GB/s, frac]
+  "rot":      activation rotation us at 1 and 64 tokens, and the 8B stack
+              with every input rotated first
+so that they survive a tail of the output.
 """
 from __future__ import annotations
 
@@ -34,13 +47,13 @@ HIDDEN, QKV, INTER, LAYERS = 4096, 6144, 12288, 36
 SHAPES_8B = [("qkv", QKV, HIDDEN), ("o", HIDDEN, HIDDEN), ("gate_up", 2 * INTER, HIDDEN), ("down", HIDDEN, INTER)]
 L2_BYTES = 126 * 1024 * 1024
 
-# DRAM traffic of the dominant kernel from the ncu capture summarised in
-# profiles/bpdq_b1_qwen3_8b_stack.md: (dram__bytes_read.sum +
-# dram__bytes_write.sum) / algorithmic bytes on a 24576x4096 launch.  The
-# stack's traffic per launch is that ratio times the stack's algorithmic
-# bytes per launch (traffic scales with the items processed).  Must be reset
-# to None whenever the kernel changes.
-NCU_TRAFFIC_RATIO = {"k_bpdq_b1": 27751936 / 27525120}
+# DRAM traffic of the dominant kernel per launch, as a ratio to its
+# algorithmic bytes, from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum) of a 24576x4096 launch of the kernel as it is now;
+# the stack's traffic per launch is that ratio times the stack's algorithmic
+# bytes per launch (traffic scales with the items processed).  A kernel with
+# no entry has no capture of its current code, and reports null.
+NCU_TRAFFIC_RATIO = {}
 
 
 def _peaks():
@@ -135,9 +148,16 @@ def _job_value(ws: int, ntok: int, steps: int, ms: float) -> float:
 
 
 def build_stack(q2, ntok: int, config: int = 1):
-    """36 layers x 4 BPDQ linears, distinct seeded weights and activations."""
+    """36 layers x 4 BPDQ linears with distinct seeded weights.  The inputs
+    are one seeded activation per projection (qkv, o, gate_up, down), shared
+    by the 36 layers as an inference engine's activation buffers are: every
+    layer's projection reads the same buffer, which therefore stays in L2
+    (as the output of the kernel before it would be) while the weights
+    stream from HBM."""
     import torch
     import synth
+    xs = {name: torch.from_numpy(synth.activations(ntok, C, 1000 * config + 900 + j)).cuda()
+          for j, (name, R, C) in enumerate(SHAPES_8B)}
     lin = []
     for layer in range(LAYERS):
         for j, (name, R, C) in enumerate(SHAPES_8B):
@@ -145,8 +165,7 @@ def build_stack(q2, ntok: int, config: int = 1):
             d = synth.bpdq(R, C, seed)
             blob = q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"])
             del d
-            x = torch.from_numpy(synth.activations(ntok, C, seed)).cuda()
-            lin.append({"name": name, "R": R, "C": C, "blob": blob, "x": x})
+            lin.append({"name": name, "R": R, "C": C, "blob": blob, "x": xs[name]})
     return lin
 
 
@@ -184,18 +203,19 @@ def time_graph(g, stream, steps: int, warmup: int, ws: int = 1):
 
 
 def per_format(q2, stream, hbm):
-    """GEMV us, GB/s and fraction of the byte bound per format (batch 1)."""
+    """Batch-1 GEMV per format and shape: {label: [us, GB/s, frac of HBM]}
+    (the no-weights control: [us]); each label cycles enough distinct copies
+    of its matrix to read >= 4x L2 per pass, with one input vector."""
     import torch
     import synth
     out = {}
 
-    def cycle(name, blob, R, C, fmt_label, fill=None):
+    def cycle(name, blob, R, C, fill=None):
         pk0 = q2.Packed(blob, ntok_max=1)
         if fill is not None:
             fill(pk0)
         nb = pk0.bytes_read(1)
-        copies = max(4, int(np.ceil(4 * L2_BYTES / max(nb, 1))))
-        copies = min(copies, 64)
+        copies = 64 if nb == 0 else max(4, int(np.ceil(4 * L2_BYTES / nb)))
         pks = [pk0] + [q2.Packed(blob, ntok_max=1, workspace=pk0.ws) for _ in range(copies - 1)]
         if fill is not None:
             for p in pks[1:]:
@@ -207,30 +227,30 @@ def per_format(q2, stream, hbm):
         ms = time_graph(g, stream, reps, 3)
         us = ms * 1e3 / (reps * copies)
         gbs = nb / (us * 1e-6) / 1e9
-        out[name] = {"format": fmt_label, "R": R, "C": C, "us_per_gemv": round(us, 3),
-                     "bytes_per_gemv": nb, "bpw_read": round(8 * nb / (R * C), 4),
-                     "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4), "copies": copies}
+        out[name] = [round(us, 2), round(gbs), round(gbs / hbm, 3)] if nb else [round(us, 2)]
         del pks, g
 
     for R, C in [(12288, 4096), (4096, 12288)]:
         d = synth.trellis(R, C, 2000 + (R > C))
-        cycle(f"trellis_{R}x{C}", q2.q2_pack_trellis(d["stream"], d["table"], d["scale"]), R, C, "trellis")
+        cycle(f"trl_{R}x{C}", q2.q2_pack_trellis(d["stream"], d["table"], d["scale"]), R, C)
+    pool = synth._sample_shell(np.random.default_rng(3000), np.random.default_rng(3001).integers(2, 7, 200000))
     for R, C in [(17408, 5120), (5120, 17408)]:
-        d = synth.leech(R, C, 3000 + (R > C))
-        cycle(f"leech_{R}x{C}", q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C), R, C, "leech")
+        d = _leech_pool_matrix(R, C, 3000 + (R > C), pool)
+        cycle(f"leech_{R}x{C}", q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C), R, C)
+    d = synth.bpdq(1024, 1024, 0)
+    cycle("bpdq_1024x1024", q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]), 1024, 1024)
     for name, R, C in SHAPES_8B:
         blob = q2.q2_pack_fp16(np.zeros((R, C), dtype=np.float16))
         g = torch.Generator(device="cuda").manual_seed(R + C)
-
         off = int(np.frombuffer(blob[56:64].tobytes(), dtype="<u8")[0])   # weight section offset
 
         def fill(p, R=R, C=C, g=g, off=off):
             w = torch.randn((R, C), generator=g, device="cuda", dtype=torch.float32).mul_(0.02).half()
             p.dev[off:off + R * C * 2].copy_(w.view(-1).view(torch.uint8))
-        cycle(f"fp16_{name}_{R}x{C}", blob, R, C, "fp16", fill)
+        cycle(f"fp16_{name}", blob, R, C, fill)
         d = synth.bpdq(R, C, 1000 + R + C)
-        cycle(f"bpdq_{name}_{R}x{C}", q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]), R, C, "bpdq")
-        cycle(f"noweights_{name}_{R}x{C}", q2.q2_pack_noweights(R, C), R, C, "noweights")
+        cycle(f"bpdq_{name}", q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]), R, C)
+        cycle(f"nw_{name}", q2.q2_pack_noweights(R, C), R, C)
     return out
 
 
@@ -245,21 +265,21 @@ def _rotation(q2, C: int, seed: int):
 
 
 def rotations(q2, stream):
-    """Latency of the activation rotation (H (x) Q)(S x) per input width, at
-    1, 16 and 64 tokens: 50 back-to-back rotations per graph replay."""
+    """Latency of the activation rotation (H (x) Q)(S x) per input width, us
+    at 1 and 64 tokens: 50 back-to-back rotations per graph replay."""
     import torch
     import synth
     out = {}
     for C in ROT_WIDTHS:
         rot, nh, nq = _rotation(q2, C, 900 + C % 1000)
-        rec = {"C": C, "nh": nh, "nq": nq}
-        for ntok in (1, 16, 64):
+        rec = []
+        for ntok in (1, 64):
             x = torch.from_numpy(synth.activations(ntok, C, 901)).cuda()
             y = torch.empty_like(x)
             g = graph_of([lambda: rot.apply(x, y, stream=stream)] * 50, stream)
             ms = time_graph(g, stream, 20, 3)
-            rec[f"us_ntok{ntok}"] = round(ms * 1e3 / (20 * 50), 3)
-        out[f"rotation_{C}"] = rec
+            rec.append(round(ms * 1e3 / (20 * 50), 2))
+        out[str(C)] = rec
     return out
 
 
@@ -281,22 +301,18 @@ def _leech_pool_matrix(R: int, C: int, seed: int, pool: np.ndarray) -> dict:
     return {"v": v, "scale": scale, "tail": tail}
 
 
-def sweep(args):
-    """Config 4: Qwen3-14B-shaped stack (40 layers x qkv/o/gate_up/down) in each
-    format, ntok in {1,2,4,8,16,32,64}; `distinct` layer copies are cycled
-    through the 40 layers (their footprint is several times L2)."""
+def sweep14b(q2, stream, formats, ntoks, distinct: int, steps: int, hbm: float) -> dict:
+    """Config 4: the Qwen3-14B-shaped stack (40 layers x qkv/o/gate_up/down)
+    per format at each token count; `distinct` layer copies are cycled
+    through the 40 layers (their footprint is several times L2).  Returns
+    {fmt: {ntok: [ms/step, tok/s, frac of HBM]}}; "cublas" is torch.matmul
+    on dense fp16 weights, "fp16" this library's dense control."""
     import torch
-    import dequant_gemv_q2_gb300 as q2
     import synth
-    q2.load()
-    torch.cuda.set_device(0)
-    stream = torch.cuda.Stream()
-    ntoks = [int(t) for t in args.sweep_ntok.split(",")]
-    distinct = args.sweep_distinct
     pool = None
     results = {}
-    for fmt in args.sweep_formats.split(","):
-        mats = []                                   # per distinct layer: 4 Packed
+    for fmt in formats:
+        mats = []                                   # per distinct layer: 4 Packed (or cuBLAS weights)
         for layer in range(distinct):
             row = []
             for j, (name, R, C) in enumerate(SHAPES_14B):
@@ -323,26 +339,23 @@ def sweep(args):
                 else:
                     if pool is None:
                         pool = synth._sample_shell(np.random.default_rng(4242),
-                                                   np.random.default_rng(4243).integers(2, 7, size=2_000_000))
+                                                   np.random.default_rng(4243).integers(2, 7, size=400_000))
                     d = _leech_pool_matrix(R, C, seed, pool)
                     pk = q2.Packed(q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C), ntok_max=max(ntoks),
                                    workspace=torch.zeros(16, dtype=torch.uint8, device="cuda"))
                 row.append(pk)
             mats.append(row)
-        if fmt != "cublas" and fmt != "fp16":
+        if fmt not in ("cublas", "fp16"):
             need = max(p.workspace_bytes(max(ntoks)) for row in mats for p in row)
             wsbuf = torch.zeros(need, dtype=torch.uint8, device="cuda")
             for row in mats:
                 for p in row:
                     p.set_workspace(wsbuf)
-        layer_bytes = 0
-        if fmt == "cublas":
-            layer_bytes = sum(R * C * 2 for _, R, C in SHAPES_14B)
         results[fmt] = {}
         for nt in ntoks:
             xs = {C: torch.from_numpy(synth.activations(nt, C, 9)).cuda() for _, _, C in SHAPES_14B}
             ys = {R: torch.empty((nt, R), dtype=torch.float16, device="cuda") for _, R, _ in SHAPES_14B}
-            calls = []
+            links, calls = [], []
             for layer in range(LAYERS_14B):
                 for j, (name, R, C) in enumerate(SHAPES_14B):
                     item = mats[layer % distinct][j]
@@ -350,86 +363,187 @@ def sweep(args):
                         w = item[1]
                         calls.append(lambda w=w, x=xs[C], y=ys[R]: torch.matmul(x, w.t(), out=y))
                     else:
-                        calls.append(lambda p=item, x=xs[C], y=ys[R]: p.gemv(x, y))
+                        links.append((item, xs[C], ys[R]))
+            if links:
+                chain = q2.Chain(links, nt, 0)
+                calls = [chain.run]
             g = graph_of(calls, stream)
-            ms = time_graph(g, stream, args.sweep_steps, 3)
-            step_ms = ms / args.sweep_steps
+            ms = time_graph(g, stream, steps, 3)
+            step_ms = ms / steps
             if fmt == "cublas":
-                step_bytes = layer_bytes * LAYERS_14B
+                step_bytes = LAYERS_14B * sum(R * C * 2 for _, R, C in SHAPES_14B)
             else:
                 step_bytes = sum(mats[l % distinct][j].bytes_read(nt) for l in range(LAYERS_14B) for j in range(4))
             gbs = step_bytes / (step_ms * 1e-3) / 1e9
-            results[fmt][nt] = {"ms_per_step": round(step_ms, 4), "tok_s": round(nt / (step_ms * 1e-3), 1),
-                                "gbs": round(gbs, 1), "bytes_per_step": step_bytes}
-            del g, calls
+            results[fmt][str(nt)] = [round(step_ms, 3), round(nt / (step_ms * 1e-3)), round(gbs / hbm, 3)]
+            del g, calls, links
         del mats
         torch.cuda.empty_cache()
+    return results
+
+
+def sweep(args):
+    """--sweep: config 4 over the formats and token counts given on the command line."""
+    import torch
+    import dequant_gemv_q2_gb300 as q2
+    q2.load()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    hbm, _ = _peaks()
+    res = sweep14b(q2, stream, args.sweep_formats.split(","), [int(t) for t in args.sweep_ntok.split(",")],
+                   args.sweep_distinct, args.sweep_steps, hbm)
     print(json.dumps({"sweep": "Qwen3-14B-shaped stack, 40 layers x (qkv 5120->7168, o 5120->5120, "
-                               "gate_up 5120->34816, down 17408->5120), linears only",
-                      "distinct_layer_copies": distinct, "results": results}), flush=True)
+                               "gate_up 5120->34816, down 17408->5120), linears only; [ms/step, tok/s, frac]",
+                      "distinct_layer_copies": args.sweep_distinct, "results": res}), flush=True)
 
 
-def cpu_oracle_sample(seconds_target: float = 15.0) -> dict:
-    """Oracle (decode + f64 matvec) on o-projection-shaped BPDQ matrices;
-    returns seconds per weight and what was sampled.  Run in a subprocess
-    with single-threaded numpy/BLAS."""
-    code = r"""
-import json, os, sys, time
-sys.path.insert(0, %r)
-import numpy as np
-import synth
-from oracle import bpdq, matvec
-t0 = time.perf_counter(); n = 0; k = 0
-while True:
-    d = synth.bpdq(4096, 4096, 5000 + k)
-    x = synth.activations(1, 4096, 5000 + k)
-    t1 = time.perf_counter()
-    w = bpdq.decode_f64(d["plane0"], d["plane1"], d["coef"])
-    y = matvec.gemv(w, x)
-    n += w.size; k += 1
-    if time.perf_counter() - t0 > %f: break
-el = time.perf_counter() - t0
-print(json.dumps({"sec_per_weight": el / n, "matrices": k, "weights": n, "seconds": el}))
-""" % (ROOT, seconds_target)
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
-    if r.returncode != 0:
-        return {"error": r.stderr[-500:]}
-    return json.loads(r.stdout.strip().splitlines()[-1])
+# Oracle cases timed on the host cores: configs 0, 2 and 3 per GEMV, and the
+# four 8B projections (config 1: one layer, times 36 for the step).
+CPU_CASES = [("bpdq_1024x1024", "bpdq", 1024, 1024),
+             ("trellis_12288x4096", "trellis", 12288, 4096), ("trellis_4096x12288", "trellis", 4096, 12288),
+             ("leech_17408x5120", "leech", 17408, 5120), ("leech_5120x17408", "leech", 5120, 17408)] + \
+            [(f"bpdq_{n}", "bpdq", R, C) for n, R, C in SHAPES_8B]
+
+_CPU_CASE_CACHE = {}
+_CPU_BARRIER = None
 
 
-def stack_weights() -> int:
-    return LAYERS * sum(R * C for _, R, C in SHAPES_8B)
+def _cpu_case_inputs(fmt: str, R: int, C: int, seed: int):
+    import synth
+    if fmt == "bpdq":
+        d = synth.bpdq(R, C, seed)
+    elif fmt == "trellis":
+        d = synth.trellis(R, C, seed)
+    else:
+        pool = synth._sample_shell(np.random.default_rng(seed), np.random.default_rng(seed + 1).integers(2, 7, 50000))
+        d = _leech_pool_matrix(R, C, seed, pool)
+    return d, synth.activations(1, C, seed)
+
+
+def _cpu_rows(fmt: str, d: dict, r0: int, r1: int) -> dict:
+    """The canonical arrays of rows [r0, r1) (rows are independent)."""
+    if fmt == "bpdq":
+        return {"plane0": d["plane0"][r0:r1], "plane1": d["plane1"][r0:r1], "coef": d["coef"][:, r0:r1]}
+    if fmt == "trellis":
+        return {"stream": d["stream"][r0:r1], "table": d["table"], "scale": d["scale"][r0:r1]}
+    return {"v": d["v"][r0:r1], "scale": d["scale"][r0:r1], "tail": d["tail"][r0:r1]}
+
+
+def _cpu_case_run(fmt: str, d, x):
+    """One oracle GEMV: exact f64 decode of the canonical weights, then the
+    f64 matvec."""
+    from oracle import bpdq, leech, matvec, trellis
+    if fmt == "bpdq":
+        w = bpdq.decode_f64(d["plane0"], d["plane1"], d["coef"])
+    elif fmt == "trellis":
+        w = trellis.decode_f64(d["stream"], d["table"], d["scale"])
+    else:
+        w = leech.decode_f64(d["v"], d["scale"], d["tail"])
+    return matvec.gemv(w, x)
+
+
+def _cpu_init(barrier):
+    global _CPU_BARRIER
+    _CPU_BARRIER = barrier
+
+
+def _cpu_worker(task):
+    """Time the oracle on rows [k*R/n, (k+1)*R/n) of a case in this
+    single-threaded process; the inputs are generated once per process and
+    not timed.  With a barrier, every process starts its timed part together."""
+    fmt, R, C, seed, k, n = task
+    key = (fmt, R, C, seed)
+    if key not in _CPU_CASE_CACHE:
+        _CPU_CASE_CACHE.clear()
+        _CPU_CASE_CACHE[key] = _cpu_case_inputs(fmt, R, C, seed)
+    d, x = _CPU_CASE_CACHE[key]
+    part = _cpu_rows(fmt, d, k * R // n, (k + 1) * R // n)
+    if _CPU_BARRIER is not None:
+        _CPU_BARRIER.wait(timeout=900)
+    t0 = time.perf_counter()
+    _cpu_case_run(fmt, part, x)
+    return time.perf_counter() - t0
+
+
+def _cpu_model() -> str:
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part", "hardware")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_oracle_baseline() -> dict:
+    """The oracle timed on the host cores, per case (us per GEMV): one
+    process on one core (single-threaded BLAS), then the same GEMV split by
+    rows over one process per core, all starting together (the GEMV's time
+    is the slowest process's).  Spawned processes, before any GPU work."""
+    import multiprocessing as mp
+    ncores = os.cpu_count() or 1
+    os.environ.update({"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"})
+    ctx = mp.get_context("spawn")
+    out = {"cores": ncores, "cpu": _cpu_model(), "per_gemv_us": {}}
+    with ctx.Pool(1) as p1:
+        for label, fmt, R, C in CPU_CASES:
+            t = p1.map(_cpu_worker, [(fmt, R, C, 7000, 0, 1)])[0]
+            out["per_gemv_us"][label] = [round(t * 1e6, 1)]
+    bar = ctx.Barrier(ncores)
+    with ctx.Pool(ncores, initializer=_cpu_init, initargs=(bar,)) as pn:
+        for label, fmt, R, C in CPU_CASES:
+            ts = pn.map(_cpu_worker, [(fmt, R, C, 7000, k, ncores) for k in range(ncores)], chunksize=1)
+            out["per_gemv_us"][label].append(round(max(ts) * 1e6, 1))
+    return out
 
 
 def run_reference(args, ws, rank):
-    """CPU oracle arm: each step is a bounded sample (one 4096x4096 BPDQ GEMV)."""
+    """CPU oracle arm.  Each step is a bounded sample of the stack: one
+    o-projection-shaped (4096x4096) oracle GEMV split by rows over every host
+    core (one single-threaded process per core); tok/s is scaled from the
+    weights the step covers to the stack's weights."""
     if rank != 0:
         return
-    import synth
-    from oracle import bpdq, matvec
-    d = synth.bpdq(4096, 4096, 5000)
-    x = synth.activations(args.ntok, 4096, 5000)
-    for _ in range(args.warmup):
-        matvec.gemv(bpdq.decode_f64(d["plane0"], d["plane1"], d["coef"]), x)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        matvec.gemv(bpdq.decode_f64(d["plane0"], d["plane1"], d["coef"]), x)
-    el = time.perf_counter() - t0
-    sec_per_w = el / (args.steps * 4096 * 4096)
-    step_s = sec_per_w * stack_weights()
-    v = args.ntok / step_s
+    import multiprocessing as mp
+    ncores = os.cpu_count() or 1
+    os.environ.update({"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"})
+    tasks = [("bpdq", HIDDEN, HIDDEN, 5000, k, ncores) for k in range(ncores)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(ncores, initializer=_cpu_init, initargs=(ctx.Barrier(ncores),)) as pool:
+        for _ in range(max(1, args.warmup)):
+            pool.map(_cpu_worker, tasks, chunksize=1)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            pool.map(_cpu_worker, tasks, chunksize=1)
+        el = time.perf_counter() - t0
+    step_s = el / args.steps
+    frac = HIDDEN * HIDDEN / stack_weights()             # share of a stack step per timed step
+    v = args.ntok * frac / step_s
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "BPDQ Qwen3-8B-shaped decode stack (36 layers x qkv/o/gate_up/down), linears only",
+        "config": {"workload": "BPDQ Qwen3-8B-shaped decode stack: 36 layers x (qkv 4096->6144, o 4096->4096, "
+                               "gate_up 4096->24576, down 12288->4096), linears only",
                    "ntok": args.ntok, "parallelism": "replicas"},
-        "cpu_baseline": {"value": v, "unit": "tok/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{args.steps} oracle GEMVs of one 4096x4096 BPDQ matrix (decode + f64 matvec), "
-                                   f"scaled to the stack's {stack_weights()} weights"},
+        "cpu_baseline": {"value": v, "unit": "tok/s", "cores": ncores, "kind": "oracle", "cpu": _cpu_model(),
+                         "sample": f"each step: one oracle GEMV of a 4096x4096 BPDQ matrix (exact f64 decode + "
+                                   f"f64 matvec) split by rows over {ncores} single-threaded processes; tok/s = "
+                                   f"ntok x {frac:.5f} of a stack step per step time"},
         "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
+
+
+def stack_weights() -> int:
+    return LAYERS * sum(R * C for _, R, C in SHAPES_8B)
 
 
 def profile_case(fmt: str, launches: int = 4, ntok: int = 1):
@@ -508,11 +622,14 @@ def main():
         run_reference(args, ws, rank)
         return
 
-    # the oracle baseline runs in a subprocess started before any GPU work
+    # the oracle baseline runs in spawned processes before any GPU work
     cpu = None
     ws_env = int(os.environ.get("WORLD_SIZE", "1"))
     if int(os.environ.get("RANK", "0")) == 0 and ws_env == 1 and not args.no_cpu:
-        cpu = cpu_oracle_sample()
+        try:
+            cpu = cpu_oracle_baseline()
+        except Exception as e:                      # a failed baseline must not cost the GPU line
+            cpu = {"error": repr(e)[:200]}
 
     import torch
     import dequant_gemv_q2_gb300 as q2
@@ -522,30 +639,45 @@ def main():
     stream = torch.cuda.Stream()
 
     lin = build_stack(q2, args.ntok)
-    # every linear's x and y are views of one input and one output buffer, so
-    # the end-to-end leg moves a step's inputs and outputs with one copy each
-    xbuf = torch.empty(sum(L["x"].numel() for L in lin), dtype=torch.float16, device="cuda")
-    ybuf = torch.empty(sum(args.ntok * L["R"] for L in lin), dtype=torch.float16, device="cuda")
-    xo = yo = 0
-    need = 0
+    names = [n for n, _, _ in SHAPES_8B]
+    shape = {n: (R, C) for n, R, C in SHAPES_8B}
     for L in lin:
-        n = L["x"].numel()
-        xbuf[xo:xo + n].copy_(L["x"].reshape(-1))
-        L["x"] = xbuf[xo:xo + n].view(args.ntok, L["C"])
-        xo += n
         L["pk"] = q2.Packed(L["blob"], ntok_max=args.ntok, workspace=torch.zeros(16, dtype=torch.uint8, device="cuda"))
-        need = max(need, L["pk"].workspace_bytes(args.ntok))
-        L["y"] = ybuf[yo:yo + args.ntok * L["R"]].view(args.ntok, L["R"])
-        yo += args.ntok * L["R"]
-    wsbuf = torch.zeros(need, dtype=torch.uint8, device="cuda")
-    for L in lin:
-        L["pk"].set_workspace(wsbuf)
         del L["blob"]
+    x0 = {n: next(L["x"] for L in lin if L["name"] == n) for n in names}
+
+    def stack_graph(nt: int, xsrc=None):
+        """The step at nt tokens as one q2_gemv_chain call in a CUDA graph: one
+        input and one output buffer per projection, shared by the layers (the
+        four inputs are views of one buffer and the four outputs of another,
+        so the end-to-end leg moves a step's inputs and outputs with one copy
+        each)."""
+        xbuf = torch.empty(sum(nt * shape[n][1] for n in names), dtype=torch.float16, device="cuda")
+        ybuf = torch.empty(sum(nt * shape[n][0] for n in names), dtype=torch.float16, device="cuda")
+        xv, yv, xo, yo = {}, {}, 0, 0
+        for j, n in enumerate(names):
+            R, C = shape[n]
+            xv[n] = xbuf[xo:xo + nt * C].view(nt, C)
+            xv[n].copy_(xsrc[n] if xsrc is not None else
+                        torch.from_numpy(__import__("synth").activations(nt, C, 1900 + j)).cuda())
+            yv[n] = ybuf[yo:yo + nt * R].view(nt, R)
+            xo += nt * C
+            yo += nt * R
+        need = max(L["pk"].workspace_bytes(nt) for L in lin)
+        wsbuf = torch.zeros(need, dtype=torch.uint8, device="cuda")
+        for L in lin:
+            L["pk"].set_workspace(wsbuf)
+        chain = q2.Chain([(L["pk"], xv[L["name"]], yv[L["name"]]) for L in lin], nt, args.lookahead)
+        return graph_of([chain.run], stream), xbuf, ybuf, wsbuf, xv, yv
+
+    def launches_per_gemv(nt: int) -> int:
+        # one launch at 1 token; token pairs plus a single token at 2..6; one
+        # tensor-core launch from 7 (the split-K reduction runs inside it for
+        # every shape of this stack)
+        return 1 if nt == 1 else (nt + 1) // 2 if nt <= 6 else 1
+
+    g, xbuf, ybuf, wsbuf, xv, yv = stack_graph(args.ntok, x0)
     step_bytes = sum(L["pk"].bytes_read(args.ntok) for L in lin)
-    # the step is one q2_gemv_chain call: the 144 GEMVs in order, each launch
-    # prefetching the weights of the next `lookahead` into L2
-    chain = q2.Chain([(L["pk"], L["x"], L["y"]) for L in lin], args.ntok, args.lookahead)
-    g = graph_of([chain.run], stream)
 
     clk = Clocks(torch.cuda.current_device())
     clk.start()
@@ -556,8 +688,8 @@ def main():
     ms_step = ms / args.steps
     value = _job_value(ws, args.ntok, args.steps, ms)
 
-    # end to end through the C ABI: every step copies all 144 inputs from
-    # pinned host memory (one copy) and reads all outputs back (one copy)
+    # end to end through the C ABI: every step copies the step's inputs from
+    # pinned host memory (one copy) and reads its outputs back (one copy)
     xs_host = xbuf.cpu().pin_memory()
     ys_host = torch.empty_like(ybuf, device="cpu").pin_memory()
     h2d = xs_host.numel() * 2
@@ -582,34 +714,45 @@ def main():
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws)
     e2e_value = _job_value(ws, args.ntok, e2e_steps, e2e_ms)
 
-    extras = rot_line = None
+    extras = {}
     if not args.no_extras and rank == 0:
-        extras = per_format(q2, stream, hbm)
-        extras.update(rotations(q2, stream))
-        # the same stack with every linear's input rotated first (one rotation
-        # per group of projections sharing an input: qkv and gate_up are fused)
-        rots = {C: _rotation(q2, C, 950 + C % 1000)[0] for C in sorted({L["C"] for L in lin})}
-        for L in lin:
-            L["xr"] = torch.empty_like(L["x"])
+        # the same 8B stack at the other token counts of its configuration
+        st8 = {}
+        for nt in (1, 4, 16):
+            if nt == args.ntok:
+                st8[str(nt)] = [round(ms_step, 4), round(value), round(step_bytes / (ms_step * 1e-3) / 1e9 / hbm, 3)]
+                continue
+            g2 = stack_graph(nt)[0]
+            k = 40
+            m2 = time_graph(g2, stream, k, 3) / k
+            b2 = sum(L["pk"].bytes_read(nt) for L in lin)
+            st8[str(nt)] = [round(m2, 4), round(nt / (m2 * 1e-3)), round(b2 / (m2 * 1e-3) / 1e9 / hbm, 3)]
+            del g2
+        extras["stack8b"] = st8
+        # the same stack with every linear's input rotated first
+        rots = {C: _rotation(q2, C, 950 + C % 1000)[0] for C in sorted({C for _, C in shape.values()})}
+        g, xbuf, ybuf, wsbuf, xv, yv = stack_graph(args.ntok, x0)
+        xr = {n: torch.empty_like(xv[n]) for n in names}
         rcalls = []
         for L in lin:
-            rcalls.append(lambda L=L: rots[L["C"]].apply(L["x"], L["xr"], stream=stream))
-            rcalls.append(lambda L=L: L["pk"].gemv(L["xr"], L["y"]))
+            n = L["name"]
+            rcalls.append(lambda n=n: rots[shape[n][1]].apply(xv[n], xr[n], stream=stream))
+            rcalls.append(lambda L=L, n=n: L["pk"].gemv(xr[n], yv[n]))
         gr = graph_of(rcalls, stream)
-        rsteps = max(10, args.steps // 4)
+        rsteps = 40
         rms = time_graph(gr, stream, rsteps, 3) / rsteps
-        rot_line = {"workload": "the same stack, each linear's input rotated by q2_rotate first",
-                    "rotations_per_step": len(lin), "ms_per_step": round(rms, 4),
-                    "tok_s": round(args.ntok / (rms * 1e-3), 1),
-                    "rotation_share": round(1.0 - ms_step / rms, 3)}
-        del gr
+        del gr, rcalls
+        rot = rotations(q2, stream)
+        rot["stack_ms"] = round(rms, 4)
+        del lin, g, xbuf, ybuf, wsbuf, xv, yv
+        torch.cuda.empty_cache()
+        extras["sweep14b"] = sweep14b(q2, stream, ["bpdq", "trellis", "leech", "cublas"], [1, 16, 64], 4, 10, hbm)
+        extras["sweep14b"]["fp16"] = sweep14b(q2, stream, ["fp16"], [1], 4, 10, hbm)["fp16"]
+        extras["fmt"] = per_format(q2, stream, hbm)
+        extras["rot"] = rot
 
     achieved = step_bytes / (ms_step * 1e-3) / 1e9
-    kname = "k_bpdq_b1" if args.ntok == 1 else ("k_bpdq_mt" if args.ntok <= 6 else "k_tc")
-    # launches of one BPDQ GEMV: one at 1 token; token pairs plus a single
-    # token at 2..6; one tensor-core launch from 7 (the split-K reduction runs
-    # inside it for every shape of this stack)
-    launches_per_gemv = 1 if args.ntok == 1 else (args.ntok + 1) // 2 if args.ntok <= 6 else 1
+    kname = "k_bpdq1" if args.ntok == 1 else ("k_bpdq_mt" if args.ntok <= 6 else "k_tc")
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
@@ -619,33 +762,38 @@ def main():
             "config": {"workload": "BPDQ Qwen3-8B-shaped decode stack: 36 layers x (qkv 4096->6144, o 4096->4096, "
                                    "gate_up 4096->24576, down 12288->4096), linears only",
                        "ntok": args.ntok, "lookahead": args.lookahead,
-                       "launches_per_step": len(lin) * launches_per_gemv,
+                       "launches_per_step": len(SHAPES_8B) * LAYERS * launches_per_gemv(args.ntok),
                        "bytes_per_step": step_bytes,
-                       "l2": "weights 1.9 GB > L2, no flush", "parallelism": "replicas" if ws > 1 else "single"},
+                       "l2": "weights 1.9 GB > L2, no flush; activations: one buffer per projection, shared by "
+                             "the layers (L2-resident)", "parallelism": "replicas" if ws > 1 else "single"},
             "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                         "traffic": (round(NCU_TRAFFIC_RATIO[kname] * step_bytes / len(lin))
+                         "traffic": (round(NCU_TRAFFIC_RATIO[kname] * step_bytes / (len(SHAPES_8B) * LAYERS))
                                      if NCU_TRAFFIC_RATIO.get(kname) else None),
                          "traffic_unit": "bytes per launch"},
-            "gpu_launches": len(lin) * launches_per_gemv * args.steps,
+            "gpu_launches": len(SHAPES_8B) * LAYERS * launches_per_gemv(args.ntok) * args.steps,
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "us_per_gemv_avg": round(ms_step * 1e3 / len(lin), 3),
+            "us_per_gemv_avg": round(ms_step * 1e3 / (len(SHAPES_8B) * LAYERS), 3),
         }
-        if cpu is not None and "sec_per_weight" in cpu:
-            step_s = cpu["sec_per_weight"] * stack_weights()
-            line["cpu_baseline"] = {"value": args.ntok / step_s, "unit": "tok/s", "cores": 1, "kind": "oracle",
-                                    "sample": f"{cpu['matrices']} oracle GEMVs of 4096x4096 BPDQ matrices "
-                                              f"(decode + f64 matvec, {cpu['seconds']:.1f} s), scaled to the "
-                                              f"stack's {stack_weights()} weights"}
+        if cpu is not None and "per_gemv_us" in cpu:
+            us = cpu["per_gemv_us"]
+            layer1 = sum(us[f"bpdq_{n}"][0] for n in names)
+            layern = sum(us[f"bpdq_{n}"][-1] for n in names)
+            line["cpu_baseline"] = {
+                "value": args.ntok / (LAYERS * layer1 * 1e-6), "unit": "tok/s", "cores": 1, "kind": "oracle",
+                "sample": "one oracle GEMV (exact f64 decode + f64 matvec) of each 8B projection shape, timed, "
+                          "x 36 layers (extrapolated to the stack step)",
+                "all_cores": {"cores": cpu["cores"], "value": args.ntok / (LAYERS * layern * 1e-6),
+                              "how": "each GEMV split by rows over one single-threaded process per core, started "
+                                     "together; its time is the slowest process's"},
+                "cpu": cpu["cpu"],
+                "us": us}
         elif cpu is not None:
             line["cpu_baseline"] = {"value": None, "unit": "tok/s", "cores": 1, "kind": "oracle",
-                                    "sample": "failed: " + cpu.get("error", "")[:200]}
-        if extras is not None:
-            line["per_format"] = extras
-        if rot_line is not None:
-            line["stack_with_rotation"] = rot_line
-        print(json.dumps(line), flush=True)
+                                    "sample": "failed: " + str(cpu.get("error", ""))[:200]}
+        line.update(extras)                         # compact, and last: they survive a tail of the output
+        print(json.dumps(line, separators=(",", ":")), flush=True)
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

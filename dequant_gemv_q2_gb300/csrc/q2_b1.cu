@@ -555,6 +555,11 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks) k_noweights_b1(BpdqArgs a)
 //   - x is read straight from global memory by the table build (16 tasks
 //     share each 16-byte load), without a staging pass.
 constexpr int kLeanMaxGrid = 192;
+// Launch shape (build-time tunables): 24 warps in one CTA per SM, 80
+// registers.  Measured on the Qwen3-8B stack (us per step): 16 warps 698,
+// 20 warps 689, 24 warps 659, 28 warps 740, 32 warps 781 (spills); two CTAs
+// per SM, so that the next GEMV's CTAs are resident early: 8 warps 921,
+// 12 warps 808, 16 warps 898 (fewer registers, less in flight).
 #ifndef Q2_LEAN_W
 #define Q2_LEAN_W 24
 #endif
