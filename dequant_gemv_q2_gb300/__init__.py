@@ -178,7 +178,8 @@ class Packed:
         _check(L.q2_info(h, ctypes.byref(f), ctypes.byref(R), ctypes.byref(C)), "q2_info")
         self.fmt, self.R, self.C = f.value, R.value, C.value
         self.ws = None
-        need = self.workspace_bytes(ntok_max)
+        # the workspace of every call up to ntok_max tokens (the paths differ by token count)
+        need = max(self.workspace_bytes(t) for t in range(1, int(ntok_max) + 1))
         if workspace is not None:
             self.set_workspace(workspace)
         elif need:

@@ -197,15 +197,19 @@ __device__ __forceinline__ void acc_issue(Pending<NT>& pd, const B1& c, int row,
   pd.row = row;
 }
 
+// nfm: bit t set when token t's x holds an inf or NaN; its outputs are NaN.
 template <int NT, class F>
-__device__ __forceinline__ void acc_settle(Pending<NT>& pd, const B1& c, const F& f) {
+__device__ __forceinline__ void acc_settle(Pending<NT>& pd, const B1& c, const F& f, uint32_t nfm) {
   if (pd.row < 0) return;
 #pragma unroll
   for (int t = 0; t < NT; ++t)
     if (t < c.ntok) {
       const unsigned long long w = pd.old[t] + pd.add[t];
       if ((int)(w >> 56) == c.nslice) {                // this lane completed the row
-        if (pd.row < c.R) f.finish(t, pd.row, fx_value(w, c.nslice, c.finv));
+        if (pd.row < c.R) {
+          if ((nfm >> t) & 1u) c.y[(size_t)t * c.R + pd.row] = __ushort_as_half((unsigned short)0x7E00u);
+          else f.finish(t, pd.row, fx_value(w, c.nslice, c.finv));
+        }
         c.acc[(size_t)t * c.Rpad + pd.row] = 0ull;
       }
     }
@@ -276,7 +280,8 @@ __device__ __forceinline__ void run_b1(F& f, const B1& c, unsigned char* tail) {
   __half* xs = reinterpret_cast<__half*>(tail + kTailX);
   const int stage_n = max(1, kStageMax / c.ntok);
   int sg0 = 0, sgn = 0;                          // staged slices [sg0, sg0 + sgn)
-  bool waited = false;
+  bool waited = false, scanned = false;
+  uint32_t nfm = 0;                              // tokens whose x holds an inf or NaN
   Pending<F::kTok> pd;
   for (int j0 = i0; j0 < i1;) {
     const int gA = j0 / c.nrb;
@@ -304,8 +309,18 @@ __device__ __forceinline__ void run_b1(F& f, const B1& c, unsigned char* tail) {
       f.stage_extra(sg0, sgn, tail);
       __syncthreads();
     }
+    uint32_t bad = 0;
+    if (!scanned)
+      for (int t = 0; t < c.ntok; ++t) bad |= (uint32_t)x_nonfinite<W * 32>(c.x + (size_t)t * c.C, c.C) << t;
     f.tables(gA, xs + (size_t)(gA - sg0) * c.ntok * Q2_SLICE, tail);
-    __syncthreads();
+    if (!scanned) {
+      // one barrier in the common case; per-token ones only when some x is bad
+      if (__syncthreads_or(bad != 0))
+        for (int t = 0; t < c.ntok; ++t) nfm |= (uint32_t)__syncthreads_or((bad >> t) & 1u) << t;
+      scanned = true;
+    } else {
+      __syncthreads();
+    }
     // the AHEAD + 1 buffers are indexed statically: AHEAD + 1 items per trip
     for (int base = it0; base < j1; base += (AHEAD + 1) * W) {
 #pragma unroll
@@ -317,7 +332,7 @@ __device__ __forceinline__ void run_b1(F& f, const B1& c, unsigned char* tail) {
           const int g = slice_of(it);
           float p[F::kTok];
           f.compute(it, g, lane, buf[u], p);
-          acc_settle(pd, c, f);
+          acc_settle(pd, c, f, nfm);
           acc_issue(pd, c, (it - g * c.nrb) * 32 + lane, p);
         }
       }
@@ -329,7 +344,7 @@ __device__ __forceinline__ void run_b1(F& f, const B1& c, unsigned char* tail) {
     pdl_wait();
     pdl_trigger();
   }
-  acc_settle(pd, c, f);
+  acc_settle(pd, c, f, nfm);
 }
 
 __device__ __forceinline__ void ld_item(const unsigned char* base, int item_bytes, int it, int lane, uint4* w,
@@ -676,11 +691,13 @@ struct LeanPending {
   int row;               // -1: nothing pending
 };
 
-__device__ __forceinline__ void lean_settle(LeanPending& pd, const LeanArgs& a) {
+// nonfinite: x holds an inf or NaN, so every output is NaN (x_nonfinite).
+__device__ __forceinline__ void lean_settle(LeanPending& pd, const LeanArgs& a, bool nonfinite) {
   if (pd.row < 0) return;
   const unsigned long long w = pd.old + pd.add;
   if ((int)(w >> 56) == a.nslice) {                   // this lane completed the row
-    if (pd.row < a.R) a.y[pd.row] = __float2half_rn(fx_value(w, a.nslice, a.finv));
+    if (pd.row < a.R)
+      a.y[pd.row] = nonfinite ? __ushort_as_half((unsigned short)0x7E00u) : __float2half_rn(fx_value(w, a.nslice, a.finv));
     *pd.p = 0ull;
   }
   pd.row = -1;
@@ -695,7 +712,7 @@ __global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_c
   float* gsum = reinterpret_cast<float*>(q2_smem + kTailGsum);
   LeanPending pd;
   pd.row = -1;
-  bool waited = false;
+  bool waited = false, nonfinite = false;
   PacedPf pp;
   pp.left = 0;
   if constexpr (kPaced) pp = paced_share(a.pf, a.pfq, a.pfr, warp, W, (i1 - i0 - warp + W - 1) / W);
@@ -723,8 +740,11 @@ __global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_c
     } else {
       __syncthreads();                                  // the previous slice's table is no longer read
     }
+    const bool scan = g * a.nrb <= i0;                  // the first slice: check all of x as well
+    const bool bad = scan && x_nonfinite<W * 32>(a.x, a.C);
     q2::build_table<W * 32>(a.x + (size_t)g * Q2_SLICE, a.C - g * Q2_SLICE, tab1(), gsum);
-    __syncthreads();
+    if (scan) nonfinite = __syncthreads_or(bad);
+    else __syncthreads();
     const float gs = *gsum;
     constexpr int kStrideW = W * (Q2_ITEM_BYTES_BPDQ / 16);
     // two items per trip so the two buffers are named statically
@@ -733,7 +753,7 @@ __global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_c
       if (m1) lean_load<kWeights>(a, wp + kStrideW, ci + W * 32, it + W, lane, b1);
       if constexpr (kPaced) pp.step(lane);
       float p = lean_partial(lane4, b0, gs);
-      lean_settle(pd, a);
+      lean_settle(pd, a, nonfinite);
       pd.add = fx_term(p, a.fscale);
       pd.old = atomicAdd(ap, pd.add);
       pd.p = ap;
@@ -743,7 +763,7 @@ __global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_c
       if (m2) lean_load<kWeights>(a, wp + 2 * kStrideW, ci + 2 * W * 32, it + 2 * W, lane, b0);
       if constexpr (kPaced) pp.step(lane);
       p = lean_partial(lane4, b1, gs);
-      lean_settle(pd, a);
+      lean_settle(pd, a, nonfinite);
       pd.add = fx_term(p, a.fscale);
       pd.old = atomicAdd(ap + W * 32, pd.add);
       pd.p = ap + W * 32;
@@ -761,7 +781,7 @@ __global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_c
     pdl_trigger();
   }
   pp.left = 0;
-  lean_settle(pd, a);
+  lean_settle(pd, a, nonfinite);
 }
 
 // ------------------------------------------------- BPDQ, 2 to 6 tokens

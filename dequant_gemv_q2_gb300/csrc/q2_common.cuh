@@ -134,6 +134,34 @@ __device__ __forceinline__ void build_table(const __half* __restrict__ xg, int n
   }
 }
 
+// ------------------------------------------------- non-finite inputs
+// The fixed-point split-K sums cannot carry an inf or NaN: a non-finite
+// slice partial is clamped into range.  But one inf or NaN anywhere in a
+// token's x makes every output of that token non-finite in IEEE arithmetic
+// (every row has a weight in that column, and 0 x inf is NaN), so each CTA
+// checks the whole x of its tokens itself and its completing lanes write
+// NaN for those tokens.  An fp16 value is non-finite when its exponent bits
+// are all ones.  Strided over the CTA's NT threads; x rows of C halves.
+__device__ __forceinline__ bool half2_nonfinite(uint32_t v) {
+  return ((v & 0x7C00u) == 0x7C00u) | ((v & 0x7C000000u) == 0x7C000000u);
+}
+
+template <int NT>
+__device__ __forceinline__ bool x_nonfinite(const __half* __restrict__ x, int C) {
+  bool bad = false;
+  if ((C & 7) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    for (int i = threadIdx.x; i < C / 8; i += NT) {
+      const uint4 v = __ldg(xv + i);
+      bad |= half2_nonfinite(v.x) | half2_nonfinite(v.y) | half2_nonfinite(v.z) | half2_nonfinite(v.w);
+    }
+  } else {
+    const unsigned short* xs = reinterpret_cast<const unsigned short*>(x);
+    for (int i = threadIdx.x; i < C; i += NT) bad |= (__ldg(xs + i) & 0x7C00u) == 0x7C00u;
+  }
+  return bad;
+}
+
 // ---------------------------------------------------- split-K reduction
 // Each (slice, 32-row block) item writes fp32 partials for its rows with
 // plain stores.  A second kernel (q2_reduce.cu), chained by programmatic
@@ -164,6 +192,15 @@ __device__ __forceinline__ unsigned long long fx_term(float p, float fscale) {
   q = max(min(q, (long long)kBias - 1), -(long long)kBias + 1);   // NaN/inf partials stay in range
   return kCountOne + (unsigned long long)(q + (long long)kBias);
 }
+
+// The tensor-core kernel's fused reduction adds at most kFusedMaxSplit
+// terms per word, whose finite sum stays below 15 * 3 * 2^46 < 2^52; an
+// inf or NaN split partial adds kPoison instead, so the completed word's
+// value reaches 2^52 exactly when some term was non-finite, and 15 poison
+// terms stay below 2^56 (no carry into the count).  The fp32 partials of
+// every other multi-token path carry infs and NaNs themselves.
+constexpr int kFusedMaxSplit = 15;
+constexpr unsigned long long kPoison = 1ull << 52;
 
 // The value of a complete accumulator word (all nslice terms added).
 __device__ __forceinline__ float fx_value(unsigned long long w, int nslice, float finv) {

@@ -388,6 +388,8 @@ int q2_bind(const void* blob_host, const void* blob_dev, q2_handle** h) {
 
 void q2_unbind(q2_handle* h) { delete h; }
 
+extern "C" size_t q2_tc_workspace_bytes(const q2_handle* h, int ntok);   // q2_tc.cu
+
 int q2_workspace_bytes(const q2_handle* h, int ntok, size_t* bytes) {
   if (!h || !bytes) return Q2_EINVAL;
   if (ntok < 1 || ntok > Q2_MAX_NTOK) return Q2_ENTOK;
@@ -396,11 +398,12 @@ int q2_workspace_bytes(const q2_handle* h, int ntok, size_t* bytes) {
     return Q2_OK;
   }
   const int fmt = h->hdr.fmt;
-  const bool cuda_core = ntok == 1 || (fmt == Q2_BPDQ && ntok <= Q2_MAX_ACC_TOK);
+  const bool cuda_core = ntok == 1 || (fmt == Q2_BPDQ && ntok <= Q2_MAX_ACC_TOK) ||
+                         (fmt == Q2_LEECH && ntok == 2 && h->hdr.C % 8 == 0 && h->hdr.R % 8 == 0);
   if (cuda_core)
     *bytes = (size_t)ntok * h->hdr.Rpad * 8;                 // accumulators
   else
-    *bytes = Q2_WS_PARTIAL_OFFSET + (size_t)h->hdr.nslice * ntok * h->hdr.Rpad * 4;
+    *bytes = q2_tc_workspace_bytes(h, ntok);                  // the tensor-core launch's plan
   return Q2_OK;
 }
 

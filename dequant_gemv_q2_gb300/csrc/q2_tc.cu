@@ -649,6 +649,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
   }
   ok = __syncthreads_and(ok);
   tc_fence_after();
+  if (FMT == Q2_BPDQ && a.fused && !ok && warp < 4 && used > 0) {
+    // A bounded wait ran out: the accumulator is not valid, but the other
+    // splits have added (or will add) their terms to these rows' words.
+    // Add a poison term for every token so the counts still complete: the
+    // completing lane writes NaN and resets the word, so the workspace is
+    // left at zero for the next call, as after a normal one.
+    const int orow = (tile * 4 + warp) * 32 + lane;
+    if (orow < a.Rpad)
+      for (int t = 0; t < a.ntok; ++t) {
+        const unsigned long long w = atomicAdd(a.acc + (size_t)t * a.Rpad + orow, kCountOne + kPoison) + kCountOne + kPoison;
+        if ((int)(w >> 56) == a.nsplit) {
+          if (orow < a.R) a.y[(size_t)t * a.R + orow] = __ushort_as_half((unsigned short)0x7E00u);
+          a.acc[(size_t)t * a.Rpad + orow] = 0ull;
+        }
+      }
+  }
   if (warp < 4 && ok && used > 0) {
     const int orow = (tile * 4 + warp) * 32 + lane;
     for (int c0 = 0; c0 < a.N; c0 += 16) {
@@ -661,7 +677,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             if (c0 + i < a.ntok) {
-              add[i] = fx_term(v[i], a.fscale);
+              // a non-finite partial adds the poison term instead (the
+              // split count is at most kFusedMaxSplit, see the launcher)
+              add[i] = isfinite(v[i]) ? fx_term(v[i], a.fscale) : kCountOne + kPoison;
               old[i] = atomicAdd(a.acc + (size_t)(c0 + i) * a.Rpad + orow, add[i]);
             }
 #pragma unroll
@@ -669,7 +687,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
             if (c0 + i < a.ntok) {
               const unsigned long long w = old[i] + add[i];
               if ((int)(w >> 56) == a.nsplit) {
-                if (orow < a.R) a.y[(size_t)(c0 + i) * a.R + orow] = __float2half_rn(fx_value(w, a.nsplit, a.finv));
+                if (orow < a.R)
+                  a.y[(size_t)(c0 + i) * a.R + orow] = (w & kValueMask) >= kPoison
+                                                           ? __ushort_as_half((unsigned short)0x7E00u)
+                                                           : __float2half_rn(fx_value(w, a.nsplit, a.finv));
                 a.acc[(size_t)(c0 + i) * a.Rpad + orow] = 0ull;
               }
             }
@@ -727,6 +748,30 @@ bool encode_x_map(CUtensorMap* map, const void* x, int C, int ntok, int N) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The K split of the tensor-core launch and whether BPDQ reduces it inside
+// the launch.  One CTA per SM at a time, so the makespan is (waves of CTAs)
+// x (slices per CTA + about one slice of prologue and epilogue).  BPDQ with
+// a K split of at most kFusedMaxSplit reduces inside the launch when its
+// accumulator words fit the workspace's reserve (the scale 2^F keeps a
+// split's partial, at most its slices times the per-slice bound, below
+// 2^46); everything else keeps fp32 partials for the reduce kernel.
+void tc_plan(const q2_blob_header& d, int ntok, int* nsplit, int* fused) {
+  const int sms = dev_info().sms;
+  const int ntile = (d.Rpad + kRows - 1) / kRows, S = d.nslice;
+  long best = -1;
+  for (int ns = 1; ns <= S; ++ns) {
+    const long ctas = (long)ntile * ns;
+    const long waves = (ctas + sms - 1) / sms;
+    const long cost = waves * ((S + ns - 1) / ns + 1);
+    if (best < 0 || cost < best) {
+      best = cost;
+      *nsplit = ns;
+    }
+  }
+  *fused = (d.fmt == Q2_BPDQ && *nsplit > 1 && *nsplit <= kFusedMaxSplit &&
+            (size_t)ntok * d.Rpad <= (size_t)Q2_MAX_ACC_TOK * Q2_MAX_ROWS) ? 1 : 0;
+}
+
 // Packed formats at 2..64 tokens on the tensor cores (tokens padded to a
 // multiple of 16).  Split-K partials (and every trellis / Leech result, whose
 // epilogue needs the row scale, exceptions and tail) go through the reduce
@@ -758,24 +803,8 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
   a.ntok = ntok;
   a.N = (ntok + 15) / 16 * 16;
   a.ntile = (d.Rpad + kRows - 1) / kRows;
-  const int sms = dev_info().sms;
-  // K split: one CTA per SM at a time, so the makespan is (waves of CTAs) x
-  // (slices per CTA + about one slice of prologue and epilogue)
-  long best = -1;
-  for (int ns = 1; ns <= a.S; ++ns) {
-    const long ctas = (long)a.ntile * ns;
-    const long waves = (ctas + sms - 1) / sms;
-    const long cost = waves * ((a.S + ns - 1) / ns + 1);
-    if (best < 0 || cost < best) {
-      best = cost;
-      a.nsplit = ns;
-    }
-  }
+  tc_plan(d, ntok, &a.nsplit, &a.fused);
   a.use_tma = encode_x_map(&a.xmap, x, d.C, ntok, a.N) ? 1 : 0;
-  // BPDQ with a K split reduces inside the launch when its accumulator words
-  // fit the workspace's reserve; the scale 2^F keeps a split's partial (at
-  // most its slices times the per-slice bound) below 2^46
-  a.fused = (FMT == Q2_BPDQ && a.nsplit > 1 && (size_t)ntok * d.Rpad <= (size_t)Q2_MAX_ACC_TOK * Q2_MAX_ROWS) ? 1 : 0;
   if (a.fused) {
     int e = 0;
     if (h->pbound > 0.0) std::frexp(h->pbound * (double)((a.S + a.nsplit - 1) / a.nsplit), &e);
@@ -794,6 +823,18 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
 
 }  // namespace
 }  // namespace q2
+
+// Workspace bytes of a tensor-core launch on the current device: none for
+// BPDQ without a K split (it writes y), the accumulator words when BPDQ's
+// split is reduced inside the launch, else the fp32 partials past the
+// accumulator reserve.
+extern "C" size_t q2_tc_workspace_bytes(const q2_handle* h, int ntok) {
+  int nsplit = 1, fused = 0;
+  q2::tc_plan(h->hdr, ntok, &nsplit, &fused);
+  if (h->hdr.fmt == Q2_BPDQ && nsplit == 1) return 0;
+  if (fused) return (size_t)ntok * h->hdr.Rpad * 8;
+  return Q2_WS_PARTIAL_OFFSET + (size_t)nsplit * ntok * h->hdr.Rpad * 4;
+}
 
 extern "C" int q2_tc_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
   return q2::launch_tc<Q2_BPDQ>(h, x, y, ntok, stream);

@@ -126,14 +126,21 @@ void q2_unbind(q2_handle* h);
  * together with an arrival count, in one atomic, and the addition that
  * completes the count writes y and resets the word.  These words must be
  * zero when the workspace is first used (allocate it zero-filled); every
- * completed call leaves them at zero again.  The tensor-core path adds BPDQ's
- * K-split partials to the same words (one term per split) when ntok x Rpad
+ * completed call leaves them at zero again (a call whose x holds an inf or
+ * NaN, or whose tensor-core launch hit a bounded-wait timeout, too: its
+ * outputs are NaN).  The tensor-core path writes y directly when it does
+ * not split K (BPDQ; no workspace), adds BPDQ's K-split partials to the same
+ * words (one term per split) when the split is at most 15 and ntok x Rpad
  * <= 6 x 524288; otherwise, and for trellis and Leech, it keeps fp32
- * partial sums (nslice x ntok x Rpad floats) at byte offset
+ * partial sums (nsplit x ntok x Rpad floats) at byte offset
  * 6 x 524288 x 8 (24 MiB), past any handle's accumulators, so one
  * workspace may serve many handles whose calls are ordered on one stream;
  * calls that overlap on the GPU must use different workspaces.  Limits:
- * R <= 524288 rows; on the CUDA-core paths C <= 255 x 256 columns. */
+ * R <= 524288 rows; on the CUDA-core paths C <= 255 x 256 columns.
+ * The size depends on the path a token count takes (and, for the
+ * tensor-core path, on the K split chosen for the current device's SM
+ * count), so it is not monotone in ntok: a workspace for every call up to
+ * N tokens is the largest q2_workspace_bytes over ntok = 1..N. */
 int q2_workspace_bytes(const q2_handle* h, int ntok, size_t* bytes);
 int q2_set_workspace(q2_handle* h, void* ws_dev, size_t ws_bytes);
 
