@@ -191,25 +191,22 @@ __device__ __forceinline__ void acc_issue(Pending<NT>& pd, const B1& c, int row,
 #pragma unroll
   for (int t = 0; t < NT; ++t)
     if (t < c.ntok) {
-      pd.add[t] = fx_term(p[t], c.fscale);
-      pd.old[t] = atomicAdd(c.acc + (size_t)t * c.Rpad + row, pd.add[t]);
+      unsigned long long* word = c.acc + (size_t)t * c.Rpad + row;
+      pd.add[t] = fx_prepare(word, p[t], c.fscale);
+      pd.old[t] = atomicAdd(word, pd.add[t]);
     }
   pd.row = row;
 }
 
-// nfm: bit t set when token t's x holds an inf or NaN; its outputs are NaN.
 template <int NT, class F>
-__device__ __forceinline__ void acc_settle(Pending<NT>& pd, const B1& c, const F& f, uint32_t nfm) {
+__device__ __forceinline__ void acc_settle(Pending<NT>& pd, const B1& c, const F& f) {
   if (pd.row < 0) return;
 #pragma unroll
   for (int t = 0; t < NT; ++t)
     if (t < c.ntok) {
       const unsigned long long w = pd.old[t] + pd.add[t];
       if ((int)(w >> 56) == c.nslice) {                // this lane completed the row
-        if (pd.row < c.R) {
-          if ((nfm >> t) & 1u) c.y[(size_t)t * c.R + pd.row] = __ushort_as_half((unsigned short)0x7E00u);
-          else f.finish(t, pd.row, fx_value(w, c.nslice, c.finv));
-        }
+        if (pd.row < c.R) f.finish(t, pd.row, fx_value(w, c.nslice, c.finv));   // NaN stays NaN
         c.acc[(size_t)t * c.Rpad + pd.row] = 0ull;
       }
     }
@@ -280,8 +277,7 @@ __device__ __forceinline__ void run_b1(F& f, const B1& c, unsigned char* tail) {
   __half* xs = reinterpret_cast<__half*>(tail + kTailX);
   const int stage_n = max(1, kStageMax / c.ntok);
   int sg0 = 0, sgn = 0;                          // staged slices [sg0, sg0 + sgn)
-  bool waited = false, scanned = false;
-  uint32_t nfm = 0;                              // tokens whose x holds an inf or NaN
+  bool waited = false;
   Pending<F::kTok> pd;
   for (int j0 = i0; j0 < i1;) {
     const int gA = j0 / c.nrb;
@@ -309,18 +305,8 @@ __device__ __forceinline__ void run_b1(F& f, const B1& c, unsigned char* tail) {
       f.stage_extra(sg0, sgn, tail);
       __syncthreads();
     }
-    uint32_t bad = 0;
-    if (!scanned)
-      for (int t = 0; t < c.ntok; ++t) bad |= (uint32_t)x_nonfinite<W * 32>(c.x + (size_t)t * c.C, c.C) << t;
     f.tables(gA, xs + (size_t)(gA - sg0) * c.ntok * Q2_SLICE, tail);
-    if (!scanned) {
-      // one barrier in the common case; per-token ones only when some x is bad
-      if (__syncthreads_or(bad != 0))
-        for (int t = 0; t < c.ntok; ++t) nfm |= (uint32_t)__syncthreads_or((bad >> t) & 1u) << t;
-      scanned = true;
-    } else {
-      __syncthreads();
-    }
+    __syncthreads();
     // the AHEAD + 1 buffers are indexed statically: AHEAD + 1 items per trip
     for (int base = it0; base < j1; base += (AHEAD + 1) * W) {
 #pragma unroll
@@ -332,7 +318,7 @@ __device__ __forceinline__ void run_b1(F& f, const B1& c, unsigned char* tail) {
           const int g = slice_of(it);
           float p[F::kTok];
           f.compute(it, g, lane, buf[u], p);
-          acc_settle(pd, c, f, nfm);
+          acc_settle(pd, c, f);
           acc_issue(pd, c, (it - g * c.nrb) * 32 + lane, p);
         }
       }
@@ -344,7 +330,7 @@ __device__ __forceinline__ void run_b1(F& f, const B1& c, unsigned char* tail) {
     pdl_wait();
     pdl_trigger();
   }
-  acc_settle(pd, c, f, nfm);
+  acc_settle(pd, c, f);
 }
 
 __device__ __forceinline__ void ld_item(const unsigned char* base, int item_bytes, int it, int lane, uint4* w,
@@ -492,7 +478,11 @@ struct LeechF {
     const float* xb = reinterpret_cast<const float*>(q2_smem + kTailXb) + (g - sg0) * 12;
     float pacc = 0.f;
     for (int j = 0; j < nbk; ++j) pacc += ((b.pw >> j) & 1u) ? xb[j] : 0.f;
-    p[0] = fmaf(2.f, P0, fmaf(4.f, P1, fmaf(-8.f, P2, pacc)));
+    // + 0 x (sum of the slice's x): the subset sums skip zero weights, but in
+    // IEEE arithmetic 0 x inf is NaN, so an inf or NaN anywhere in the slice
+    // must still make the partial non-finite
+    const float gs = *reinterpret_cast<const float*>(q2_smem + kTailGsum);
+    p[0] = fmaf(0.f, gs, fmaf(2.f, P0, fmaf(4.f, P1, fmaf(-8.f, P2, pacc))));
   }
   __device__ void finish(int tok, int row, float v) const {
     const __half* xt = a.c.x + (size_t)tok * a.c.C;
@@ -691,13 +681,11 @@ struct LeanPending {
   int row;               // -1: nothing pending
 };
 
-// nonfinite: x holds an inf or NaN, so every output is NaN (x_nonfinite).
-__device__ __forceinline__ void lean_settle(LeanPending& pd, const LeanArgs& a, bool nonfinite) {
+__device__ __forceinline__ void lean_settle(LeanPending& pd, const LeanArgs& a) {
   if (pd.row < 0) return;
   const unsigned long long w = pd.old + pd.add;
   if ((int)(w >> 56) == a.nslice) {                   // this lane completed the row
-    if (pd.row < a.R)
-      a.y[pd.row] = nonfinite ? __ushort_as_half((unsigned short)0x7E00u) : __float2half_rn(fx_value(w, a.nslice, a.finv));
+    if (pd.row < a.R) a.y[pd.row] = __float2half_rn(fx_value(w, a.nslice, a.finv));
     *pd.p = 0ull;
   }
   pd.row = -1;
@@ -712,7 +700,7 @@ __global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_c
   float* gsum = reinterpret_cast<float*>(q2_smem + kTailGsum);
   LeanPending pd;
   pd.row = -1;
-  bool waited = false, nonfinite = false;
+  bool waited = false;
   PacedPf pp;
   pp.left = 0;
   if constexpr (kPaced) pp = paced_share(a.pf, a.pfq, a.pfr, warp, W, (i1 - i0 - warp + W - 1) / W);
@@ -740,11 +728,8 @@ __global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_c
     } else {
       __syncthreads();                                  // the previous slice's table is no longer read
     }
-    const bool scan = g * a.nrb <= i0;                  // the first slice: check all of x as well
-    const bool bad = scan && x_nonfinite<W * 32>(a.x, a.C);
     q2::build_table<W * 32>(a.x + (size_t)g * Q2_SLICE, a.C - g * Q2_SLICE, tab1(), gsum);
-    if (scan) nonfinite = __syncthreads_or(bad);
-    else __syncthreads();
+    __syncthreads();
     const float gs = *gsum;
     constexpr int kStrideW = W * (Q2_ITEM_BYTES_BPDQ / 16);
     // two items per trip so the two buffers are named statically
@@ -753,8 +738,8 @@ __global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_c
       if (m1) lean_load<kWeights>(a, wp + kStrideW, ci + W * 32, it + W, lane, b1);
       if constexpr (kPaced) pp.step(lane);
       float p = lean_partial(lane4, b0, gs);
-      lean_settle(pd, a, nonfinite);
-      pd.add = fx_term(p, a.fscale);
+      lean_settle(pd, a);
+      pd.add = fx_prepare(ap, p, a.fscale);
       pd.old = atomicAdd(ap, pd.add);
       pd.p = ap;
       pd.row = row;
@@ -763,8 +748,8 @@ __global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_c
       if (m2) lean_load<kWeights>(a, wp + 2 * kStrideW, ci + 2 * W * 32, it + 2 * W, lane, b0);
       if constexpr (kPaced) pp.step(lane);
       p = lean_partial(lane4, b1, gs);
-      lean_settle(pd, a, nonfinite);
-      pd.add = fx_term(p, a.fscale);
+      lean_settle(pd, a);
+      pd.add = fx_prepare(ap + W * 32, p, a.fscale);
       pd.old = atomicAdd(ap + W * 32, pd.add);
       pd.p = ap + W * 32;
       pd.row = row + W * 32;
@@ -781,7 +766,7 @@ __global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_c
     pdl_trigger();
   }
   pp.left = 0;
-  lean_settle(pd, a, nonfinite);
+  lean_settle(pd, a);
 }
 
 // ------------------------------------------------- BPDQ, 2 to 6 tokens
@@ -941,12 +926,24 @@ __global__ void __launch_bounds__(W * 32, 1) k_bpdq_mt(BpdqArgs a) {
 }
 
 // ---------------------------------------------------------------- trellis
-// Lane = row, item = (segment, 32 rows).  The 16 KiB table and all of x sit
-// in shared memory for the whole kernel (one group spanning every segment).
+// Lane = row, item = (segment, 32 rows).  The codebook and all of x sit in
+// shared memory for the whole kernel (one group spanning every segment).
 // Step k of a segment reads the 16-bit state at bit offset 4*(127 - k) of
 // the lane's 512-bit packet (a funnel shift of two words), hashes it, loads
 // one fp16 pair, flips both signs by state bit 0 and accumulates two fp32
 // FMAs.  The epilogue multiplies by the row scale.
+//
+// The codebook row of a step is effectively random per lane, so 32 lanes
+// loading one word each from a single 16 KiB table land about 3.5 to a bank
+// at worst (the expected maximum of 32 uniform draws over 32 banks), and the
+// warp's load replays that often.  The table is therefore stored K times,
+// interleaved: copy c of entry i is word i*K + c, so copy c lives in banks
+// c, c + K, c + 2K, ..., and lane l reads copy l % K.  A warp's 32 loads then
+// split into K independent groups of 32/K lanes over 32/K banks each: the
+// expected worst bank load is 2.1 at K = 8 (four lanes over four banks), 2.5
+// at K = 4, against 3.5 at K = 1.  The byte address of entry i is
+// i * 4K + 4c: a shift and a masked OR of the hashed state, as cheap as the
+// single table's.
 struct TrellisArgs {
   B1 c;
   const unsigned char* stream;
@@ -955,9 +952,11 @@ struct TrellisArgs {
 };
 
 constexpr uint32_t kHashHi = 0x9E37u << 16;   // (s*0x9E37 mod 2^16) lands in bits 16..31
-constexpr int kTrlTail = 4096 * 4;           // x (C/2 words) follows the table; then the tail
 
-template <int NT>
+template <int K>
+constexpr int trl_table_bytes() { return 4096 * 4 * K; }
+
+template <int NT, int K>
 struct TrellisF {
   struct Item {
     uint4 w[4];
@@ -965,9 +964,11 @@ struct TrellisF {
   static constexpr bool kStaged = false;
   static constexpr int kGroup = 1 << 30;   // one group: x and the table stay for every segment
   static constexpr int kTok = 1;
+  static constexpr int kLog4K = K == 8 ? 5 : K == 4 ? 4 : 2;   // log2(4K)
   const TrellisArgs& a;
-  const uint32_t* tab;
+  const unsigned char* tab;   // K interleaved copies of the codebook
   uint32_t* xs;
+  uint32_t c4;                // 4 * (this lane's copy)
   __device__ void load(int it, int, int lane, Item& b) const { ld_item(a.stream, Q2_ITEM_BYTES_TRL, it, lane, b.w, 4); }
   __device__ void stage_extra(int, int, unsigned char*) {}
   __device__ void tables(int, const __half*, unsigned char*) const {
@@ -989,7 +990,9 @@ struct TrellisF {
         const int n = 127 - k;
         const uint32_t f = __funnelshift_r(W[n >> 3], W[((n >> 3) + 1) & 15], 4 * (n & 7));
         const uint32_t h = f * kHashHi;
-        uint32_t e = tab[h >> 20];
+        // byte address of copy c4/4 of entry h >> 20: (h >> 20) * 4K + c4
+        const uint32_t off = ((h >> (20 - kLog4K)) & (0xFFFu << kLog4K)) | c4;
+        uint32_t e = *reinterpret_cast<const uint32_t*>(tab + off);
         e ^= (f & 1u) ? 0x80008000u : 0u;
         if (kk & 1) {
           acc1 = fma_h(lo16(e), lo16(xx[kk]), acc1);
@@ -1009,13 +1012,22 @@ struct TrellisF {
 
 constexpr int kTrellisAhead = 1;
 
-template <int W, int AHEAD>
+template <int W, int AHEAD, int K>
 __global__ void __launch_bounds__(W * 32, kMinBlocks) k_trellis_b1(TrellisArgs a) {
-  uint32_t* tab = reinterpret_cast<uint32_t*>(q2_smem);                 // 16 KiB
-  uint32_t* xs = reinterpret_cast<uint32_t*>(q2_smem + kTrlTail);       // x as half2, C/2 words
-  for (int i = threadIdx.x; i < 4096; i += W * 32) tab[i] = a.table[i];
-  TrellisF<W * 32> f{a, tab, xs};
-  unsigned char* tail = q2_smem + kTrlTail + ((a.c.C * 2 + 15) / 16) * 16;
+  uint32_t* tab = reinterpret_cast<uint32_t*>(q2_smem);                                  // K copies
+  uint32_t* xs = reinterpret_cast<uint32_t*>(q2_smem + trl_table_bytes<K>());           // x as half2, C/2 words
+  // K copies of each entry, written as K consecutive words (16-byte stores for K >= 4)
+  for (int i = threadIdx.x; i < 4096; i += W * 32) {
+    const uint32_t v = __ldg(a.table + i);
+    if constexpr (K >= 4) {
+#pragma unroll
+      for (int c = 0; c < K; c += 4) *reinterpret_cast<uint4*>(tab + i * K + c) = make_uint4(v, v, v, v);
+    } else {
+      tab[i] = v;
+    }
+  }
+  TrellisF<W * 32, K> f{a, reinterpret_cast<const unsigned char*>(tab), xs, (uint32_t)((threadIdx.x & 31) % K) * 4u};
+  unsigned char* tail = q2_smem + trl_table_bytes<K>() + ((a.c.C * 2 + 15) / 16) * 16;
   run_b1<W, AHEAD>(f, a.c, tail);                  // one group over all segments
 }
 
@@ -1028,6 +1040,7 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks) k_trellis_b1(TrellisArgs a
 // token-pair tables) need more than half and run one per SM with the whole
 // register file.
 constexpr int kOneCtaSmem = 116 * 1024;
+constexpr int kMaxDynSmem = 227 * 1024;   // opt-in dynamic shared memory per CTA
 constexpr int kTwoCtaSmem = kMinBlocks == 2 ? 80 * 1024 : kOneCtaSmem;
 
 struct Geo {
@@ -1054,10 +1067,10 @@ B1 make_b1(const q2_handle* h, const void* x, void* y, int ntok, const q2_pf* pf
   c.x = static_cast<const __half*>(x);
   c.y = static_cast<__half*>(y);
   c.acc = static_cast<unsigned long long*>(h->ws);
-  // fixed-point scale 2^F with |partial| * 2^F < 2^46 for every fp16 x
+  // fixed-point scale 2^F with |partial| * 2^F < 2^45 for every fp16 x
   int e = 0;
   if (h->pbound > 0.0) std::frexp(h->pbound, &e);    // pbound < 2^e
-  const int F = std::max(-100, std::min(100, 46 - e));
+  const int F = std::max(-100, std::min(100, 45 - e));
   c.fscale = std::ldexp(1.0f, F);
   c.finv = std::ldexp(1.0f, -F);
   c.R = d.R;
@@ -1197,8 +1210,17 @@ extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* s
   a.stream = h->dev + d.off[SEC_TRL_STREAM];
   a.table = reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_TRL_TABLE]);
   a.scale = reinterpret_cast<const __half*>(h->dev + d.off[SEC_TRL_SCALE]);
-  return launch1(k_trellis_b1<kWarps, kTrellisAhead>, a, geometry(d), kWarps * 32,
-                 kTrlTail + (d.C * 2 + 15) / 16 * 16, stream);
+  // as many codebook copies as fit beside x and the tail in one CTA's shared memory
+  const int xbytes = (d.C * 2 + 15) / 16 * 16;
+  auto fits = [&](int tb) { return tb + xbytes + kTailFixed <= kMaxDynSmem; };
+  if (fits(trl_table_bytes<8>()))
+    return launch1(k_trellis_b1<kWarps, kTrellisAhead, 8>, a, geometry(d), kWarps * 32, trl_table_bytes<8>() + xbytes,
+                   stream);
+  if (fits(trl_table_bytes<4>()))
+    return launch1(k_trellis_b1<kWarps, kTrellisAhead, 4>, a, geometry(d), kWarps * 32, trl_table_bytes<4>() + xbytes,
+                   stream);
+  return launch1(k_trellis_b1<kWarps, kTrellisAhead, 1>, a, geometry(d), kWarps * 32, trl_table_bytes<1>() + xbytes,
+                 stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -134,34 +134,6 @@ __device__ __forceinline__ void build_table(const __half* __restrict__ xg, int n
   }
 }
 
-// ------------------------------------------------- non-finite inputs
-// The fixed-point split-K sums cannot carry an inf or NaN: a non-finite
-// slice partial is clamped into range.  But one inf or NaN anywhere in a
-// token's x makes every output of that token non-finite in IEEE arithmetic
-// (every row has a weight in that column, and 0 x inf is NaN), so each CTA
-// checks the whole x of its tokens itself and its completing lanes write
-// NaN for those tokens.  An fp16 value is non-finite when its exponent bits
-// are all ones.  Strided over the CTA's NT threads; x rows of C halves.
-__device__ __forceinline__ bool half2_nonfinite(uint32_t v) {
-  return ((v & 0x7C00u) == 0x7C00u) | ((v & 0x7C000000u) == 0x7C000000u);
-}
-
-template <int NT>
-__device__ __forceinline__ bool x_nonfinite(const __half* __restrict__ x, int C) {
-  bool bad = false;
-  if ((C & 7) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
-    const uint4* xv = reinterpret_cast<const uint4*>(x);
-    for (int i = threadIdx.x; i < C / 8; i += NT) {
-      const uint4 v = __ldg(xv + i);
-      bad |= half2_nonfinite(v.x) | half2_nonfinite(v.y) | half2_nonfinite(v.z) | half2_nonfinite(v.w);
-    }
-  } else {
-    const unsigned short* xs = reinterpret_cast<const unsigned short*>(x);
-    for (int i = threadIdx.x; i < C; i += NT) bad |= (__ldg(xs + i) & 0x7C00u) == 0x7C00u;
-  }
-  return bad;
-}
-
 // ---------------------------------------------------- split-K reduction
 // Each (slice, 32-row block) item writes fp32 partials for its rows with
 // plain stores.  A second kernel (q2_reduce.cu), chained by programmatic
@@ -177,34 +149,47 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ------------------------------------------- fixed-point accumulation
-// Accumulator word: bits 56..63 count the slices added so far; bits 0..55
-// hold the sum of (q + 2^47) over those slices, q = round(partial * 2^F) in
-// [-(2^47 - 1), 2^47 - 1].  At most Q2_MAX_SPLIT (255) biased terms of at
-// most 2^48 each sum below 2^56, so the value never carries into the count.
-// The batch-1 kernels add one term per 256-column slice, the tensor-core
-// kernel one per K split.
-constexpr unsigned long long kBias = 1ull << 47;
+// Accumulator word: bits 56..63 count the terms added so far; bit 55 is a
+// sticky flag set by any non-finite term; bits 0..54 hold the sum of
+// (q + 2^46) over the finite terms, q = round(partial * 2^F), where the
+// launcher picks F so that |partial| * 2^F < 2^45 for every fp16 x (the
+// clamp below only ever bites on absurd inputs).  At most Q2_MAX_SPLIT
+// (255) terms of less than 2^47 each sum below 255 * 2^47 < 2^55: the value
+// never reaches the flag or the count.  The batch-1 kernels add one term
+// per 256-column slice, the tensor-core kernel one per K split.
+//
+// One inf or NaN in x makes the IEEE result non-finite, but an integer sum
+// cannot carry it.  A lane whose partial is not finite therefore sets the
+// flag with an atomic OR and then adds its count with an atomic add, both
+// on the same word: later atomics on a word see earlier ones, so whichever
+// lane completes the count finds the flag in its add's result and writes
+// NaN (IEEE would give inf or NaN: non-finite either way).
+constexpr unsigned long long kBias = 1ull << 46;
 constexpr unsigned long long kCountOne = 1ull << 56;
-constexpr unsigned long long kValueMask = kCountOne - 1;
+constexpr unsigned long long kNonFinite = 1ull << 55;
+constexpr unsigned long long kValueMask = kNonFinite - 1;
 
 __device__ __forceinline__ unsigned long long fx_term(float p, float fscale) {
   long long q = __float2ll_rn(p * fscale);
-  q = max(min(q, (long long)kBias - 1), -(long long)kBias + 1);   // NaN/inf partials stay in range
+  q = max(min(q, (long long)kBias - 1), -(long long)kBias + 1);
   return kCountOne + (unsigned long long)(q + (long long)kBias);
 }
 
-// The tensor-core kernel's fused reduction adds at most kFusedMaxSplit
-// terms per word, whose finite sum stays below 15 * 3 * 2^46 < 2^52; an
-// inf or NaN split partial adds kPoison instead, so the completed word's
-// value reaches 2^52 exactly when some term was non-finite, and 15 poison
-// terms stay below 2^56 (no carry into the count).  The fp32 partials of
-// every other multi-token path carry infs and NaNs themselves.
-constexpr int kFusedMaxSplit = 15;
-constexpr unsigned long long kPoison = 1ull << 52;
+// The term to add for partial p to *word.  A non-finite p sets the flag on
+// the word first (the OR is ordered before the caller's add on the same
+// word) and adds only the count.  The caller adds the returned term with
+// atomicAdd and may look at the result later (its round trip overlaps work).
+__device__ __forceinline__ unsigned long long fx_prepare(unsigned long long* word, float p, float fscale) {
+  if (isfinite(p)) return fx_term(p, fscale);
+  atomicOr(word, kNonFinite);
+  return kCountOne;
+}
 
-// The value of a complete accumulator word (all nslice terms added).
-__device__ __forceinline__ float fx_value(unsigned long long w, int nslice, float finv) {
-  const long long v = (long long)(w & kValueMask) - (long long)nslice * (long long)kBias;
+// The value of a completed word (all n terms added): NaN when a term was not
+// finite, else the fixed-point sum scaled back by finv = 2^-F.
+__device__ __forceinline__ float fx_value(unsigned long long w, int n, float finv) {
+  if (w & kNonFinite) return __int_as_float(0x7fc00000);
+  const long long v = (long long)(w & kValueMask) - (long long)n * (long long)kBias;
   return (float)v * finv;
 }
 

@@ -658,7 +658,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
     const int orow = (tile * 4 + warp) * 32 + lane;
     if (orow < a.Rpad)
       for (int t = 0; t < a.ntok; ++t) {
-        const unsigned long long w = atomicAdd(a.acc + (size_t)t * a.Rpad + orow, kCountOne + kPoison) + kCountOne + kPoison;
+        unsigned long long* word = a.acc + (size_t)t * a.Rpad + orow;
+        atomicOr(word, kNonFinite);
+        const unsigned long long w = atomicAdd(word, kCountOne) + kCountOne;
         if ((int)(w >> 56) == a.nsplit) {
           if (orow < a.R) a.y[(size_t)t * a.R + orow] = __ushort_as_half((unsigned short)0x7E00u);
           a.acc[(size_t)t * a.Rpad + orow] = 0ull;
@@ -677,20 +679,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             if (c0 + i < a.ntok) {
-              // a non-finite partial adds the poison term instead (the
-              // split count is at most kFusedMaxSplit, see the launcher)
-              add[i] = isfinite(v[i]) ? fx_term(v[i], a.fscale) : kCountOne + kPoison;
-              old[i] = atomicAdd(a.acc + (size_t)(c0 + i) * a.Rpad + orow, add[i]);
+              unsigned long long* word = a.acc + (size_t)(c0 + i) * a.Rpad + orow;
+              add[i] = fx_prepare(word, v[i], a.fscale);
+              old[i] = atomicAdd(word, add[i]);
             }
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             if (c0 + i < a.ntok) {
               const unsigned long long w = old[i] + add[i];
               if ((int)(w >> 56) == a.nsplit) {
-                if (orow < a.R)
-                  a.y[(size_t)(c0 + i) * a.R + orow] = (w & kValueMask) >= kPoison
-                                                           ? __ushort_as_half((unsigned short)0x7E00u)
-                                                           : __float2half_rn(fx_value(w, a.nsplit, a.finv));
+                if (orow < a.R) a.y[(size_t)(c0 + i) * a.R + orow] = __float2half_rn(fx_value(w, a.nsplit, a.finv));
                 a.acc[(size_t)(c0 + i) * a.Rpad + orow] = 0ull;
               }
             }
@@ -751,10 +749,10 @@ bool encode_x_map(CUtensorMap* map, const void* x, int C, int ntok, int N) {
 // The K split of the tensor-core launch and whether BPDQ reduces it inside
 // the launch.  One CTA per SM at a time, so the makespan is (waves of CTAs)
 // x (slices per CTA + about one slice of prologue and epilogue).  BPDQ with
-// a K split of at most kFusedMaxSplit reduces inside the launch when its
-// accumulator words fit the workspace's reserve (the scale 2^F keeps a
-// split's partial, at most its slices times the per-slice bound, below
-// 2^46); everything else keeps fp32 partials for the reduce kernel.
+// a K split reduces inside the launch when its accumulator words fit the
+// workspace's reserve (the scale 2^F keeps a split's partial, at most its
+// slices times the per-slice bound, below 2^45); everything else keeps fp32
+// partials for the reduce kernel.
 void tc_plan(const q2_blob_header& d, int ntok, int* nsplit, int* fused) {
   const int sms = dev_info().sms;
   const int ntile = (d.Rpad + kRows - 1) / kRows, S = d.nslice;
@@ -768,7 +766,7 @@ void tc_plan(const q2_blob_header& d, int ntok, int* nsplit, int* fused) {
       *nsplit = ns;
     }
   }
-  *fused = (d.fmt == Q2_BPDQ && *nsplit > 1 && *nsplit <= kFusedMaxSplit &&
+  *fused = (d.fmt == Q2_BPDQ && *nsplit > 1 &&
             (size_t)ntok * d.Rpad <= (size_t)Q2_MAX_ACC_TOK * Q2_MAX_ROWS) ? 1 : 0;
 }
 
@@ -808,7 +806,7 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
   if (a.fused) {
     int e = 0;
     if (h->pbound > 0.0) std::frexp(h->pbound * (double)((a.S + a.nsplit - 1) / a.nsplit), &e);
-    const int F = std::max(-100, std::min(100, 46 - e));
+    const int F = std::max(-100, std::min(100, 45 - e));
     a.acc = static_cast<unsigned long long*>(h->ws);
     a.fscale = std::ldexp(1.0f, F);
     a.finv = std::ldexp(1.0f, -F);

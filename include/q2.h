@@ -167,8 +167,10 @@ int q2_bytes(const q2_handle* h, int ntok, size_t* weight_bytes_read_per_call);
  * fixed-point scale 2^F is chosen per matrix (and, on the tensor-core path,
  * per K split) from its largest weight magnitude so that no fp16 x can
  * overflow it; each term then carries an absolute rounding error of at most
- * 2^-(F+1), about 1e-8 per 256-column slice for weights of magnitude
- * 0.05.  Launches use programmatic dependent launch: weights are
+ * 2^-(F+1), about 2e-8 per 256-column slice for weights of magnitude
+ * 0.05.  An inf or NaN in a token's x makes that token's outputs NaN (the
+ * IEEE result is non-finite for every row; the fixed-point sums carry a
+ * sticky flag for it).  Launches use programmatic dependent launch: weights are
  * fetched before the previous kernel on the stream has finished; x, y and
  * the workspace are touched only after it has.  Returns Q2_ECUDA if a
  * launch fails. */
