@@ -234,19 +234,28 @@ def per_format(q2, stream, hbm):
         d = synth.trellis(R, C, 2000 + (R > C))
         cycle(f"trl_{R}x{C}", q2.q2_pack_trellis(d["stream"], d["table"], d["scale"]), R, C)
     pool = synth._sample_shell(np.random.default_rng(3000), np.random.default_rng(3001).integers(2, 7, 200000))
+
+    def fp16_fill(R, C, seed):
+        blob = q2.q2_pack_fp16(np.zeros((R, C), dtype=np.float16))
+        g = torch.Generator(device="cuda").manual_seed(seed)
+        off = int(np.frombuffer(blob[56:64].tobytes(), dtype="<u8")[0])   # weight section offset
+
+        def fill(p):
+            w = torch.randn((R, C), generator=g, device="cuda", dtype=torch.float32).mul_(0.02).half()
+            p.dev[off:off + R * C * 2].copy_(w.view(-1).view(torch.uint8))
+        return blob, fill
+
     for R, C in [(17408, 5120), (5120, 17408)]:
         d = _leech_pool_matrix(R, C, 3000 + (R > C), pool)
-        cycle(f"leech_{R}x{C}", q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C), R, C)
+        # the two in-memory layouts (bits per weight read is the design axis) and the fp16 control
+        cycle(f"leech_{R}x{C}", q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C, q2.LEECH_PLANES3), R, C)
+        cycle(f"leech4_{R}x{C}", q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C, q2.LEECH_OFFSET4), R, C)
+        blob, fill = fp16_fill(R, C, R + C)
+        cycle(f"fp16_{R}x{C}", blob, R, C, fill)
     d = synth.bpdq(1024, 1024, 0)
     cycle("bpdq_1024x1024", q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]), 1024, 1024)
     for name, R, C in SHAPES_8B:
-        blob = q2.q2_pack_fp16(np.zeros((R, C), dtype=np.float16))
-        g = torch.Generator(device="cuda").manual_seed(R + C)
-        off = int(np.frombuffer(blob[56:64].tobytes(), dtype="<u8")[0])   # weight section offset
-
-        def fill(p, R=R, C=C, g=g, off=off):
-            w = torch.randn((R, C), generator=g, device="cuda", dtype=torch.float32).mul_(0.02).half()
-            p.dev[off:off + R * C * 2].copy_(w.view(-1).view(torch.uint8))
+        blob, fill = fp16_fill(R, C, R + C)
         cycle(f"fp16_{name}", blob, R, C, fill)
         d = synth.bpdq(R, C, 1000 + R + C)
         cycle(f"bpdq_{name}", q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]), R, C)

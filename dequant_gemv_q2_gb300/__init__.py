@@ -49,7 +49,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "q2_pack_fp16": [vp, i32, i32, vp, psz],
         "q2_pack_bpdq": [vp, vp, vp, i32, i32, vp, psz],
         "q2_pack_trellis": [vp, vp, vp, i32, i32, vp, psz],
-        "q2_pack_leech": [vp, vp, vp, i32, i32, ctypes.c_float, vp, psz],
+        "q2_pack_leech": [vp, vp, vp, i32, i32, ctypes.c_float, i32, vp, psz],
         "q2_pack_noweights": [i32, i32, vp, psz],
         "q2_bind": [vp, vp, ctypes.POINTER(vp)],
         "q2_workspace_bytes": [vp, i32, psz],
@@ -131,14 +131,17 @@ def q2_pack_trellis(stream: np.ndarray, table: np.ndarray, scale: np.ndarray) ->
                  "q2_pack_trellis")
 
 
-def q2_pack_leech(v: np.ndarray, tail: np.ndarray, scale: np.ndarray, C: int) -> np.ndarray:
+LEECH_PLANES3, LEECH_OFFSET4 = 0, 1
+
+
+def q2_pack_leech(v: np.ndarray, tail: np.ndarray, scale: np.ndarray, C: int, layout: int = LEECH_PLANES3) -> np.ndarray:
     vv = np.ascontiguousarray(v, dtype=np.int8)
     tl = np.ascontiguousarray(tail, dtype=np.float16)
     sc = np.ascontiguousarray(scale, dtype=np.float16)
     R = vv.shape[0]
     tptr = _ptr(tl.view(np.uint16)) if tl.size else None
     return _pack("q2_pack_leech", [_ptr(vv), tptr, _ptr(sc.view(np.uint16)), R, C,
-                                   ctypes.c_float(INV_SQRT8_F32)], "q2_pack_leech")
+                                   ctypes.c_float(INV_SQRT8_F32), int(layout)], "q2_pack_leech")
 
 
 def q2_pack_noweights(R: int, C: int) -> np.ndarray:

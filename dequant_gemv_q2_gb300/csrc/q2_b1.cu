@@ -425,26 +425,33 @@ __device__ __forceinline__ void leech_blocks(int g, int nblock, int& bfirst, int
   nbk = max(0, blast - bfirst + 1);
 }
 
-// The three planes hold the two's-complement bits of u = (v - p)/2 per
-// weight (p = the block's parity bit), so v = p + 2*b0 + 4*b1 - 8*b2: three
-// subset sums plus, per 24-column block starting in the slice, the block sum
-// of x when the row's parity bit for the block is set.  The epilogue adds
-// 16 x[col] for each v = +8 exception, multiplies by scale_r / sqrt(8) and
-// adds the fp16 tail ("Tetra", section 5.1: the row scale after the block
-// dot product, then the unquantised tail).
-template <int NT>
+// Two layouts (q2_pack_leech).  NP = 3: the planes hold the two's-complement
+// bits of u = (v - p)/2 per weight (p = the block's parity bit), so
+// v = p + 2*b0 + 4*b1 - 8*b2: three subset sums plus, per 24-column block
+// starting in the slice, the block sum of x when the row's parity bit for
+// the block is set; the epilogue adds 16 x[col] for each v = +8 exception.
+// NP = 4: the planes hold the offset-binary code c = (v - p)/2 + 4, so
+// v = p - 8 + 2*b0 + 4*b1 + 8*b2 + 16*b3 (and every column outside the
+// blocks holds c = 4): four subset sums, the parity term and -8 times the
+// slice's sum of x (no exceptions); plane 3 is set only
+// where v = +8, so its lookups are skipped when no lane of the warp has a
+// bit in it.  Then x scale_r / sqrt(8) and the fp16 tail ("Tetra", section
+// 5.1: the row scale after the block dot product, then the unquantised
+// tail).
+template <int NT, int NP>
 struct LeechF {
   struct Item {
-    uint4 w[6];
+    uint4 w[2 * NP];
     uint32_t pw;         // parity bits of the slice's blocks for this row
   };
   static constexpr bool kStaged = true;
   static constexpr int kGroup = 1;
   static constexpr int kTok = 1;
+  static constexpr int kItemBytes = NP == 4 ? Q2_ITEM_BYTES_LEECH4 : Q2_ITEM_BYTES_LEECH;
   const LeechArgs& a;
   int sg0 = 0;           // first staged slice (block sums in the tail are per staged slice)
   __device__ void load(int it, int g, int lane, Item& b) const {
-    ld_item(a.planes, Q2_ITEM_BYTES_LEECH, it, lane, b.w, 6);
+    ld_item(a.planes, kItemBytes, it, lane, b.w, 2 * NP);
     b.pw = __ldg(a.parity + (size_t)g * a.c.Rpad + (size_t)(it - g * a.c.nrb) * 32 + lane);
   }
   // block sums of x for the blocks that start in each staged slice (<= 11
@@ -482,7 +489,16 @@ struct LeechF {
     // IEEE arithmetic 0 x inf is NaN, so an inf or NaN anywhere in the slice
     // must still make the partial non-finite
     const float gs = *reinterpret_cast<const float*>(q2_smem + kTailGsum);
-    p[0] = fmaf(0.f, gs, fmaf(2.f, P0, fmaf(4.f, P1, fmaf(-8.f, P2, pacc))));
+    if constexpr (NP == 3) {
+      p[0] = fmaf(0.f, gs, fmaf(2.f, P0, fmaf(4.f, P1, fmaf(-8.f, P2, pacc))));
+    } else {
+      const uint4 h0 = b.w[6], h1 = b.w[7];
+      const bool any3 = __any_sync(0xffffffffu, (h0.x | h0.y | h0.z | h0.w | h1.x | h1.y | h1.z | h1.w) != 0u);
+      const float P3 = any3 ? plane_sum(lane4, h0, h1) : 0.f;
+      // every column of the slice carries the -8 offset (columns outside the
+      // blocks hold code 4, so theirs cancels): -8 x (the slice's sum of x)
+      p[0] = fmaf(2.f, P0, fmaf(4.f, P1, fmaf(8.f, P2, fmaf(16.f, P3, fmaf(-8.f, gs, pacc)))));
+    }
   }
   __device__ void finish(int tok, int row, float v) const {
     const __half* xt = a.c.x + (size_t)tok * a.c.C;
@@ -495,10 +511,10 @@ struct LeechF {
   }
 };
 
-template <int W, int AHEAD>
+template <int W, int AHEAD, int NP>
 __global__ void __launch_bounds__(W * 32, 1) k_leech_b1(LeechArgs a) {
   if ((uint32_t)__cvta_generic_to_shared(q2_smem) + kTailFixed > kTabAddr) return;   // layout needs a low window base
-  LeechF<W * 32> f{a};
+  LeechF<W * 32, NP> f{a};
   run_b1<W, AHEAD>(f, a.c, tail1());
 }
 
@@ -1199,7 +1215,9 @@ extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* str
   a.tail_n = d.tail;
   a.tailpad = d.tailpad;
   a.inv_sqrt8 = d.inv_sqrt8;
-  return launch1(k_leech_b1<kWarps, kLeechAhead>, a, geometry(d), kWarps * 32, kTabSmem, stream);
+  if (d.layout == Q2_LEECH_OFFSET4)
+    return launch1(k_leech_b1<kWarps, kLeechAhead, 4>, a, geometry(d), kWarps * 32, kTabSmem, stream);
+  return launch1(k_leech_b1<kWarps, kLeechAhead, 3>, a, geometry(d), kWarps * 32, kTabSmem, stream);
 }
 
 extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* stream, const q2_pf* pf) {

@@ -64,7 +64,7 @@ __global__ void k_dec_trellis(const unsigned char* stream, const uint32_t* table
 // Leech: one thread per (row, block); rebuilds v from parity, planes and the
 // exception list.
 __global__ void k_dec_leech(const unsigned char* planes, const uint16_t* parity, const uint32_t* excptr,
-                            const uint32_t* exccol, int8_t* out, int R, int Rpad, int nblock) {
+                            const uint32_t* exccol, int8_t* out, int R, int Rpad, int nblock, int off4) {
   const size_t n = (size_t)R * nblock;
   for (size_t e = blockIdx.x * (size_t)kThreads + threadIdx.x; e < n; e += (size_t)gridDim.x * kThreads) {
     const int r = (int)(e / nblock), b = (int)(e % nblock);
@@ -77,11 +77,14 @@ __global__ void k_dec_leech(const unsigned char* planes, const uint16_t* parity,
       const int c = c0 + i;
       const int s = c / 256, cc = c % 256, beta = cc / 8, bit = cc % 8;
       const int P = (beta - l + 32) & 31;
-      const unsigned char* it = planes + ((size_t)s * (Rpad / 32) + rb) * Q2_ITEM_BYTES_LEECH + l * 16 + (P & 15);
+      const size_t item = off4 ? Q2_ITEM_BYTES_LEECH4 : Q2_ITEM_BYTES_LEECH;
+      const unsigned char* it = planes + ((size_t)s * (Rpad / 32) + rb) * item + l * 16 + (P & 15);
       const int k = P >> 4;
       const int b0 = (it[k * 512] >> bit) & 1, b1 = (it[(2 + k) * 512] >> bit) & 1,
                 b2 = (it[(4 + k) * 512] >> bit) & 1;
-      int v = p + 2 * b0 + 4 * b1 - 8 * b2;
+      // two's-complement u = (v - p)/2, or the offset-binary code (v - p)/2 + 4
+      int v = off4 ? p - 8 + 2 * b0 + 4 * b1 + 8 * b2 + 16 * ((it[(6 + k) * 512] >> bit) & 1)
+                   : p + 2 * b0 + 4 * b1 - 8 * b2;
       for (uint32_t x = excptr[r]; x < excptr[r + 1]; ++x)
         if (exccol[x] == (uint32_t)c) v = 8;
       out[(size_t)r * nblock * 24 + c] = (int8_t)v;
@@ -133,7 +136,7 @@ extern "C" int q2_launch_decode(const q2_handle* h, void* out, void* stream) {
           h->dev + d.off[SEC_LEECH_PLANES], reinterpret_cast<const uint16_t*>(h->dev + d.off[SEC_LEECH_PARITY]),
           reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_LEECH_EXCPTR]),
           reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_LEECH_EXCCOL]), static_cast<int8_t*>(out), d.R,
-          d.Rpad, d.nblock);
+          d.Rpad, d.nblock, d.layout == Q2_LEECH_OFFSET4 ? 1 : 0);
       if (d.tail) {
         size_t body = (size_t)d.R * d.nblock * 24;
         body = (body + 15) / 16 * 16;

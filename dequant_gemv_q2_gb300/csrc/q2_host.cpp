@@ -228,10 +228,15 @@ int q2_pack_trellis(const uint8_t* stream, const uint16_t* table, const uint16_t
 }
 
 int q2_pack_leech(const int8_t* v, const uint16_t* tail, const uint16_t* scale,
-                  int R, int C, float inv_sqrt8, void* out, size_t* out_bytes) {
+                  int R, int C, float inv_sqrt8, int layout, void* out, size_t* out_bytes) {
   if (!out_bytes || (out && (!v || !scale || (C % 24 && !tail)))) return Q2_EINVAL;
+  if (layout != Q2_LEECH_PLANES3 && layout != Q2_LEECH_OFFSET4) return Q2_EINVAL;
   if (R < 1 || C < 24) return Q2_ESHAPE;
+  const bool off4 = layout == Q2_LEECH_OFFSET4;
+  const int NP = off4 ? 4 : 3;
+  const int item_bytes = off4 ? Q2_ITEM_BYTES_LEECH4 : Q2_ITEM_BYTES_LEECH;
   Builder b(Q2_LEECH, R, C);
+  b.hdr.layout = layout;
   const int nb = C / 24, TL = C % 24, TLp = (TL + 7) / 8 * 8;
   const int S = (C + Q2_SLICE - 1) / Q2_SLICE, Rp = b.hdr.Rpad, nrb = Rp / Q2_ROWS;
   b.hdr.nslice = S;
@@ -247,11 +252,11 @@ int q2_pack_leech(const int8_t* v, const uint16_t* tail, const uint16_t* scale,
       const int p = blk[0] & 1;
       for (int j = 0; j < 24; ++j) {
         if ((blk[j] & 1) != p || blk[j] < -8 || blk[j] > 8) return Q2_EINVAL;
-        if (blk[j] == 8) ++nexc;
+        if (blk[j] == 8 && !off4) ++nexc;
       }
     }
   }
-  b.section(SEC_LEECH_PLANES, (size_t)S * nrb * Q2_ITEM_BYTES_LEECH);
+  b.section(SEC_LEECH_PLANES, (size_t)S * nrb * item_bytes);
   b.section(SEC_LEECH_PARITY, (size_t)S * Rp * 2);
   b.section(SEC_LEECH_SCALE, (size_t)Rp * 2);
   b.section(SEC_LEECH_TAIL, (size_t)Rp * TLp * 2);
@@ -260,7 +265,7 @@ int q2_pack_leech(const int8_t* v, const uint16_t* tail, const uint16_t* scale,
     // size query: reserve the worst case for the exception list is not
     // possible without the data; callers pass v on the query as well.
     uint32_t q = 0;
-    if (v) {
+    if (v && !off4) {
       for (size_t i = 0; i < (size_t)R * nb * 24; ++i) q += (v[i] == 8);
     }
     nexc = q;
@@ -272,8 +277,8 @@ int q2_pack_leech(const int8_t* v, const uint16_t* tail, const uint16_t* scale,
   if (st || !fill) return st;
   // canonical per-row planes (bit c of a [C/8 padded to S*32] byte row)
   const size_t rowbytes = (size_t)S * 32;
-  std::vector<uint8_t> pl[3];
-  for (int p = 0; p < 3; ++p) pl[p].assign(rowbytes, 0);
+  std::vector<uint8_t> pl[4];
+  for (int p = 0; p < NP; ++p) pl[p].assign(rowbytes, 0);
   unsigned char* planes = sec(out, b.hdr, SEC_LEECH_PLANES);
   uint16_t* parity = reinterpret_cast<uint16_t*>(sec(out, b.hdr, SEC_LEECH_PARITY));
   uint32_t* excptr = reinterpret_cast<uint32_t*>(sec(out, b.hdr, SEC_LEECH_EXCPTR));
@@ -281,10 +286,14 @@ int q2_pack_leech(const int8_t* v, const uint16_t* tail, const uint16_t* scale,
   uint32_t ne = 0;
   for (int r = 0; r < Rp; ++r) {
     excptr[r] = ne;
-    if (r >= R) continue;
-    for (int p = 0; p < 3; ++p) std::fill(pl[p].begin(), pl[p].end(), 0);
+    if (r >= R && !off4) continue;
+    for (int p = 0; p < NP; ++p) std::fill(pl[p].begin(), pl[p].end(), 0);
+    // offset binary: every column outside the blocks (tail, padding columns,
+    // padding rows) holds code 4, the code of 0, so the -8 offset cancels there
+    if (off4) std::fill(pl[2].begin(), pl[2].end(), (uint8_t)0xFF);
+    const int nbr = r < R ? nb : 0;             // padding rows: no blocks
     std::vector<uint16_t> par(S, 0);
-    for (int bk = 0; bk < nb; ++bk) {
+    for (int bk = 0; bk < nbr; ++bk) {
       const int8_t* blk = v + ((size_t)r * nb + bk) * 24;
       const int p = blk[0] & 1;
       const int c0 = bk * 24;
@@ -293,22 +302,28 @@ int q2_pack_leech(const int8_t* v, const uint16_t* tail, const uint16_t* scale,
       if (p) par[sl] |= (uint16_t)(1u << (bk - first));
       for (int j = 0; j < 24; ++j) {
         int val = blk[j];
-        if (val == 8) {
-          exccol[ne++] = (uint32_t)(c0 + j);
-          val = -8;
+        int code;
+        if (off4) {
+          code = (val - p) / 2 + 4;         // offset binary, 0..8
+        } else {
+          if (val == 8) {
+            exccol[ne++] = (uint32_t)(c0 + j);
+            val = -8;
+          }
+          code = ((val - p) / 2) & 7;       // u in [-4, 3], three-bit two's complement
         }
-        const int u = (val - p) / 2;        // in [-4, 3]
-        const int code = u & 7;             // three-bit two's complement
         const int c = c0 + j;
-        for (int q = 0; q < 3; ++q)
-          if ((code >> q) & 1) pl[q][c >> 3] |= (uint8_t)(1u << (c & 7));
+        for (int q = 0; q < NP; ++q) {
+          const uint8_t bit = (uint8_t)(1u << (c & 7));
+          pl[q][c >> 3] = ((code >> q) & 1) ? (uint8_t)(pl[q][c >> 3] | bit) : (uint8_t)(pl[q][c >> 3] & ~bit);
+        }
       }
     }
-    for (int s = 0; s < S; ++s) parity[(size_t)s * Rp + r] = par[s];
+    for (int s = 0; s < S; ++s) parity[(size_t)s * Rp + r] = r < R ? par[s] : (uint16_t)0;
     const int rb = r / 32, l = r % 32;
     for (int s = 0; s < S; ++s) {
-      unsigned char* item = planes + ((size_t)s * nrb + rb) * Q2_ITEM_BYTES_LEECH;
-      for (int k = 0; k < 6; ++k)
+      unsigned char* item = planes + ((size_t)s * nrb + rb) * item_bytes;
+      for (int k = 0; k < 2 * NP; ++k)
         for (int q = 0; q < 16; ++q) {
           const int P = (k & 1) * 16 + q;
           const int beta = (P + l) & 31;
@@ -375,6 +390,7 @@ int q2_bind(const void* blob_host, const void* blob_dev, q2_handle** h) {
     return Q2_EBLOB;
   for (int i = 0; i < Q2_MAX_SECTIONS; ++i)
     if (hdr.len[i] && (hdr.off[i] % kAlign || hdr.off[i] + hdr.len[i] > hdr.total_bytes)) return Q2_EBLOB;
+  if (hdr.layout != 0 && !(hdr.fmt == Q2_LEECH && hdr.layout == Q2_LEECH_OFFSET4)) return Q2_EBLOB;
   q2_handle* p = new (std::nothrow) q2_handle;
   if (!p) return Q2_ENOMEM;
   p->hdr = hdr;

@@ -4,12 +4,13 @@
 #include <stddef.h>
 
 #define Q2_MAGIC 0x31423251u   // "Q2B1"
-#define Q2_VERSION 1u
+#define Q2_VERSION 2u
 #define Q2_ROWS 32             // rows per lane-group (one warp, one row per lane)
 #define Q2_SLICE 256           // columns per group / segment / slice
 #define Q2_ITEM_BYTES_BPDQ 2048   // 32 lanes x (2 planes x 32 bytes)
 #define Q2_ITEM_BYTES_TRL 2048    // 32 lanes x 64 bytes of symbols
 #define Q2_ITEM_BYTES_LEECH 3072  // 32 lanes x (3 planes x 32 bytes)
+#define Q2_ITEM_BYTES_LEECH4 4096 // 32 lanes x (4 planes x 32 bytes): offset-binary layout
 #define Q2_MAX_SECTIONS 8
 
 // Workspace layout.  The CUDA-core paths (1..6 tokens) keep one 64-bit
@@ -46,12 +47,14 @@ struct q2_blob_header {
   uint64_t total_bytes;
   uint64_t off[Q2_MAX_SECTIONS];
   uint64_t len[Q2_MAX_SECTIONS];
+  int32_t layout;     // Leech: Q2_LEECH_PLANES3 or Q2_LEECH_OFFSET4; 0 otherwise
+  int32_t reserved;
 };
 
 // Byte layout of one item (slice s, row block rb), item index it = s*nrb + rb:
 //   chunk k of 512 bytes at it*ITEM + k*512; lane l's 16 bytes at +l*16.
 // BPDQ:   chunks 0,1 = plane 0, chunks 2,3 = plane 1.  Leech: chunks 2p, 2p+1
-//         = plane p (p = 0,1,2).  Byte q of chunk k is rotated position
+//         = plane p (p = 0,1,2, and 3 in the offset-binary layout).  Byte q of chunk k is rotated position
 //         P = (k&1)*16 + q, which holds the canonical column-byte
 //         (P + lane) mod 32 of the slice for row rb*32 + lane.
 // Trellis: 16 little-endian words per lane; nibble n (0..127) of the lane's

@@ -229,7 +229,8 @@ constexpr uint32_t kHashHi = 0x9E37u << 16;     // trellis: (s*0x9E37 mod 2^16) 
 // Per-format shape of a slice's K range: 32 chunks of 8 columns, plus, for
 // Leech, 4 chunks carrying the parity term (A = parity bit of the blocks
 // starting in the slice, B = their block sums of x split into fp16 hi + lo).
-template <int FMT>
+// OFF4: the Leech offset-binary layout (four planes).
+template <int FMT, bool OFF4 = false>
 struct TcShape {
   static constexpr int kch = FMT == Q2_LEECH ? 36 : 32;
   static constexpr int kmma = kch / 2;                  // K = 16 steps per slice
@@ -237,7 +238,8 @@ struct TcShape {
   static constexpr uint32_t acols = kch * 4;            // TMEM columns of one A stage
   static constexpr int table = FMT == Q2_TRELLIS ? 4096 * 4 : 0;
   static constexpr int item = FMT == Q2_BPDQ ? Q2_ITEM_BYTES_BPDQ : FMT == Q2_TRELLIS ? Q2_ITEM_BYTES_TRL
-                                                                                     : Q2_ITEM_BYTES_LEECH;
+                              : OFF4 ? Q2_ITEM_BYTES_LEECH4 : Q2_ITEM_BYTES_LEECH;
+  static constexpr int planes = FMT == Q2_BPDQ ? 2 : FMT == Q2_LEECH ? (OFF4 ? 4 : 3) : 0;
 };
 static_assert(kAcol0 + kStagesA * TcShape<Q2_LEECH>::acols <= kTmemCols, "A stages exceed TMEM");
 
@@ -278,6 +280,33 @@ __device__ __forceinline__ uint4 decode_leech_q(const Codes4& c) {
   r.y = __byte_perm(h1, 0u, 0x2404u);       // cols 2,3
   r.z = __byte_perm(h0, 0u, 0x3414u);       // cols 4,5
   r.w = __byte_perm(h1, 0u, 0x3414u);       // cols 6,7
+  return r;
+}
+
+// Offset-binary Leech (four planes): v - p = 2c - 8 for the code
+// c = b0 + 2 b1 + 4 b2 + 8 b3 in 0..8.  The low three bits index the fp16
+// high bytes of -8, -6, ..., 6; c = 8 (v = +8, rare) has low bits 0, so its
+// -8 is turned into +8 by flipping the sign bit of each column whose plane-3
+// bit is set (byte q3 of plane 3 for these 8 columns).
+template <int Q>
+__device__ __forceinline__ uint4 decode_leech4_q(const Codes4& c, uint32_t q3) {
+  // fp16 high bytes of -8, -6, -4, -2, 0, 2, 4, 6 (code 0..7)
+  constexpr uint32_t HA = 0xC0C4C6C8u, HB = 0x46444000u;
+  constexpr uint32_t sel = (uint32_t)Q | ((4u + Q) << 4);
+  const uint32_t s0 = __byte_perm(c.ea, c.oa, sel);   // codes of cols 0,4,1,5
+  const uint32_t s1 = __byte_perm(c.eb, c.ob, sel);   // cols 2,6,3,7
+  const uint32_t h0 = __byte_perm(HA, HB, s0), h1 = __byte_perm(HA, HB, s1);
+  uint4 r;
+  r.x = __byte_perm(h0, 0u, 0x2404u);       // cols 0,1: [0, h(c0), 0, h(c1)]
+  r.y = __byte_perm(h1, 0u, 0x2404u);       // cols 2,3
+  r.z = __byte_perm(h0, 0u, 0x3414u);       // cols 4,5
+  r.w = __byte_perm(h1, 0u, 0x3414u);       // cols 6,7
+  if (q3) {                                 // column i's sign bit: bit 15 (even i) or 31 (odd i) of word i / 2
+    r.x ^= ((q3 & 0x01u) << 15) | ((q3 & 0x02u) << 30);
+    r.y ^= ((q3 & 0x04u) << 13) | ((q3 & 0x08u) << 28);
+    r.z ^= ((q3 & 0x10u) << 11) | ((q3 & 0x20u) << 26);
+    r.w ^= ((q3 & 0x40u) << 9) | ((q3 & 0x80u) << 24);
+  }
   return r;
 }
 
@@ -324,6 +353,19 @@ __device__ __forceinline__ void leech_part(const uint32_t (&L0)[kPartWords + 1],
   }
 }
 
+// Offset-binary Leech: the part from its four planes (values 2c - 8).
+__device__ __forceinline__ void leech4_part(const uint32_t (&L0)[kPartWords + 1], const uint32_t (&L1)[kPartWords + 1],
+                                            const uint32_t (&L2)[kPartWords + 1], const uint32_t (&L3)[kPartWords + 1],
+                                            uint32_t sh, uint32_t ta) {
+#pragma unroll
+  for (int j = 0; j < kPartWords; ++j) {
+    const Codes4 c = codes4x3(unrot(L0[j], L0[j + 1], sh), unrot(L1[j], L1[j + 1], sh), unrot(L2[j], L2[j + 1], sh));
+    const uint32_t w3 = unrot(L3[j], L3[j + 1], sh);
+    tmem_st16(ta + (uint32_t)(16 * j), decode_leech4_q<0>(c, w3 & 0xFFu), decode_leech4_q<1>(c, (w3 >> 8) & 0xFFu),
+              decode_leech4_q<2>(c, (w3 >> 16) & 0xFFu), decode_leech4_q<3>(c, w3 >> 24));
+  }
+}
+
 // Named barrier 1 between the MMA warp and the helper warp, with an AND of a
 // flag: no memory access, so the MMA lane's queue of tensor-core
 // instructions is not drained by the handoff.
@@ -340,9 +382,9 @@ __device__ __forceinline__ bool handoff(bool in) {
   return r != 0;
 }
 
-template <int FMT>
+template <int FMT, bool OFF4>
 __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcArgs a) {
-  using Sh = TcShape<FMT>;
+  using Sh = TcShape<FMT, OFF4>;
   uint32_t* tab = reinterpret_cast<uint32_t*>(q2_smem);            // trellis table
   // kStagesB B buffers from the first 1024-byte boundary after the table
   const uint32_t sbase = saddr(q2_smem);
@@ -398,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
   // (BPDQ / Leech: kPartWords + 1 per plane; trellis: a 5-word window of the
   // 64-byte symbol packet), at per-lane offsets fixed for the whole kernel;
   // plus BPDQ's value table / Leech's parity word.
-  constexpr int NPL = FMT == Q2_BPDQ ? 2 : FMT == Q2_LEECH ? 3 : 0;
+  constexpr int NPL = Sh::planes;
   constexpr int NW = FMT == Q2_TRELLIS ? 5 : NPL * (kPartWords + 1);
   int off[NW];
   {
@@ -573,7 +615,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
           L1[t] = pl[kPartWords + 1 + t];
           L2[t] = pl[2 * (kPartWords + 1) + t];
         }
-        leech_part(L0, L1, L2, sh, ta);
+        if constexpr (OFF4) {
+          uint32_t L3[kPartWords + 1];
+#pragma unroll
+          for (int t = 0; t <= kPartWords; ++t) L3[t] = pl[(NPL - 1) * (kPartWords + 1) + t];
+          leech4_part(L0, L1, L2, L3, sh, ta);
+        } else {
+          leech_part(L0, L1, L2, sh, ta);
+        }
         if (part == 0) {
           // parity columns (K 256..287, TMEM columns 128..143 of the stage):
           // A = 1.0 where the block starting in this slice is odd, once for
@@ -774,9 +823,9 @@ void tc_plan(const q2_blob_header& d, int ntok, int* nsplit, int* fused) {
 // multiple of 16).  Split-K partials (and every trellis / Leech result, whose
 // epilogue needs the row scale, exceptions and tail) go through the reduce
 // kernel.
-template <int FMT>
+template <int FMT, bool OFF4 = false>
 int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
-  using Sh = TcShape<FMT>;
+  using Sh = TcShape<FMT, OFF4>;
   const q2_blob_header& d = h->hdr;
   TcArgs a = {};
   if (FMT == Q2_BPDQ) {
@@ -813,7 +862,7 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
   }
   // table, 1024-byte alignment slack, B buffers, the stage mbarriers, TMEM slot
   const int smem = max(kOneCtaSmem, Sh::table + 1024 + kStagesB * Sh::atoms * a.N * 128 + (2 * kStagesA + kStagesB + 2) * 8 + 16);
-  int st = launch_pdl(k_tc<FMT>, a, a.ntile * a.nsplit, kThreads, smem, stream);
+  int st = launch_pdl(k_tc<FMT, OFF4>, a, a.ntile * a.nsplit, kThreads, smem, stream);
   if (st) return st;
   if (FMT == Q2_BPDQ && (a.nsplit == 1 || a.fused)) return Q2_OK;
   return q2_launch_reduce_n(h, x, y, ntok, a.nsplit, stream);
@@ -841,7 +890,8 @@ extern "C" int q2_tc_trellis(const q2_handle* h, const void* x, void* y, int nto
   return q2::launch_tc<Q2_TRELLIS>(h, x, y, ntok, stream);
 }
 extern "C" int q2_tc_leech(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
-  return q2::launch_tc<Q2_LEECH>(h, x, y, ntok, stream);
+  if (h->hdr.layout == Q2_LEECH_OFFSET4) return q2::launch_tc<Q2_LEECH, true>(h, x, y, ntok, stream);
+  return q2::launch_tc<Q2_LEECH, false>(h, x, y, ntok, stream);
 }
 
 // Device-side error word of the tensor-core kernels since the last call

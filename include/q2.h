@@ -99,15 +99,24 @@ int q2_pack_trellis(const uint8_t* stream, const uint16_t* table, const uint16_t
                     int R, int C, void* out, size_t* out_bytes);
 
 /* Leech lattice ("Unfolding the Leech Lattice": blocks of 24 weights, each a
- * lattice point; unfolded offline into a bit-plane layout).  v: int8
- * [R][C/24][24] lattice points, |v_i| <= 8 with all coordinates of a block
- * of one parity; tail: fp16 bits [R][C%24]; scale: fp16 bits [R].  Any C
- * with C >= 24 is accepted; inv_sqrt8 is the fp32 factor applied with the
- * row scale (the caller passes 1/sqrt(8) rounded to fp32).  Layout: per
- * block a parity bit and three two's-complement planes of u = (v - p)/2;
- * v = +8 goes to an exception side channel. */
+ * lattice point; unfolded offline into a bit-plane layout whose bits per
+ * weight read from memory are a design axis, section 3 and contribution
+ * C2).  v: int8 [R][C/24][24] lattice points, |v_i| <= 8 with all
+ * coordinates of a block of one parity; tail: fp16 bits [R][C%24]; scale:
+ * fp16 bits [R].  Any C with C >= 24 is accepted; inv_sqrt8 is the fp32
+ * factor applied with the row scale (the caller passes 1/sqrt(8) rounded to
+ * fp32).  Layouts, both with a parity bit p per block:
+ *   Q2_LEECH_PLANES3: three two's-complement planes of u = (v - p)/2, so
+ *     v = p + 2 b0 + 4 b1 - 8 b2; v = +8 (rare at shells 2..6) is stored as
+ *     -8 and listed in an exception side channel.  About 3.07 bpw read.
+ *   Q2_LEECH_OFFSET4: four planes of the offset-binary code c = (v - p)/2 + 4
+ *     (0..8), v = p - 8 + 2 b0 + 4 b1 + 8 b2 + 16 b3; no exceptions.  About
+ *     4.07 bpw read.
+ * Anything else returns Q2_EINVAL. */
+#define Q2_LEECH_PLANES3 0
+#define Q2_LEECH_OFFSET4 1
 int q2_pack_leech(const int8_t* v, const uint16_t* tail, const uint16_t* scale,
-                  int R, int C, float inv_sqrt8, void* out, size_t* out_bytes);
+                  int R, int C, float inv_sqrt8, int layout, void* out, size_t* out_bytes);
 
 /* No-weights control: a header only. */
 int q2_pack_noweights(int R, int C, void* out, size_t* out_bytes);

@@ -5,6 +5,7 @@ HEADER = np.dtype([
     ("magic", "<u4"), ("version", "<u4"), ("fmt", "<i4"), ("R", "<i4"), ("C", "<i4"), ("Rpad", "<i4"),
     ("nslice", "<i4"), ("nblock", "<i4"), ("tail", "<i4"), ("tailpad", "<i4"), ("nexc", "<u4"),
     ("inv_sqrt8", "<f4"), ("total", "<u8"), ("off", "<u8", (8,)), ("len", "<u8", (8,)),
+    ("layout", "<i4"), ("reserved", "<i4"),
 ])
 
 

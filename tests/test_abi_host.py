@@ -111,6 +111,40 @@ def test_leech_layout_roundtrip(q2):
     assert np.array_equal(tail, d["tail"])
 
 
+def test_leech_offset_binary_layout_roundtrip(q2):
+    """The second Leech layout: four planes of c = (v - p)/2 + 4, no exceptions."""
+    R, C = 40, 24 * 30 + 8
+    d = synth.leech(R, C, seed=78)
+    v = d["v"].copy()
+    v[3, 5] = 0
+    v[3, 5, 7] = 8                       # +8 is code 8 (plane 3), not an exception
+    v[10, 29] = 0
+    v[10, 29, [0, 1]] = [-8, 0]          # -8 is code 0
+    blob = q2.q2_pack_leech(v, d["tail"], d["scale"], C, q2.LEECH_OFFSET4)
+    h = _blob.header(blob)
+    assert h["layout"] == 1 and h["nexc"] == 0 and h["version"] == 2
+    S = h["nslice"]
+    planes = _blob.unrotate_planes(_blob.section(blob, 0), 4, R, S, int(h["Rpad"]))
+    bits = [np.unpackbits(planes[q], axis=1, bitorder="little").astype(np.int64) for q in range(4)]
+    code = bits[0] + 2 * bits[1] + 4 * bits[2] + 8 * bits[3]
+    par = _blob.section(blob, 1).view(np.uint16).reshape(S, -1)
+    nb = C // 24
+    rec = np.zeros((R, nb, 24), dtype=np.int64)
+    for b in range(nb):
+        sb = 24 * b // 256
+        first = (256 * sb + 23) // 24
+        p = (par[sb, :R] >> (b - first)) & 1
+        rec[:, b] = p[:, None] + 2 * (code[:, 24 * b: 24 * b + 24] - 4)
+    assert np.array_equal(rec, v.astype(np.int64))
+    assert (code[:, nb * 24:] == 4).all()                        # outside the blocks: code 4, the code of 0
+    # 4 planes + parity + scale + tail: one bit per weight more than the three-plane layout
+    b3 = q2.q2_pack_leech(v, d["tail"], d["scale"], C)
+    assert _blob.header(b3)["len"][0] * 4 == h["len"][0] * 3
+    L = q2.load()
+    n = ctypes.c_size_t(0)
+    assert L.q2_pack_leech(None, None, None, R, C, ctypes.c_float(0.35), 2, None, ctypes.byref(n)) == -1
+
+
 def test_status_codes(q2):
     L = q2.load()
     n = ctypes.c_size_t(0)

@@ -159,31 +159,62 @@ def _leech_with_exceptions(R, C, seed):
     return d
 
 
+LAYOUTS = [0, 1]        # three two's-complement planes + exceptions; four offset-binary planes
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("R,C,seed", [(70, 24 * 40 + 8, 3000), (32, 256, 3001), (100, 5120, 3002), (33, 24, 3003)])
 @pytest.mark.parametrize("ntok", [1, 2, 4, 16, 64])
-def test_leech_parity(q2, R, C, seed, ntok):
+def test_leech_parity(q2, R, C, seed, ntok, layout):
     d = _leech_with_exceptions(R, C, seed)
     x = synth.activations(ntok, C, seed)
-    _, y = _run(q2, q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C), x)
+    _, y = _run(q2, q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C, layout), x)
     _check(y, oleech.decode_f64(d["v"], d["scale"], d["tail"]), x)
 
 
+@pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("ntok", [1, 2, 16, 64])
-def test_leech_width_not_multiple_of_8(q2, ntok):
+def test_leech_width_not_multiple_of_8(q2, ntok, layout):
     # C % 8 != 0: the tensor-core path cannot describe x rows to TMA (row
     # stride not a multiple of 16 bytes) and stages the x tiles and the parity
     # block sums with element loads instead
     R, C = 70, 24 * 20 + 12
     d = _leech_with_exceptions(R, C, 3100 + ntok)
     x = synth.activations(ntok, C, 3101)
-    _, y = _run(q2, q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C), x)
+    _, y = _run(q2, q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C, layout), x)
     _check(y, oleech.decode_f64(d["v"], d["scale"], d["tail"]), x)
 
 
-def test_leech_decode_bit_exact(q2):
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("ntok", [1, 16])
+def test_leech_one_hot_columns_bit_exact(q2, layout, ntok):
+    """A unit vector x = e_c selects one weight per row: y[r] = fp16(v[r][c] x
+    (scale_r x 1/sqrt(8))) in fp32, exactly what both kernels compute for it
+    (the subset sums at one token, the tensor-core decode at 16), for columns
+    that include every planted v = +8 and some of its -8 neighbours."""
+    R, C = 70, 24 * 40 + 8
+    d = _leech_with_exceptions(R, C, 3020)
+    pk = q2.Packed(q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C, layout), ntok_max=ntok)
+    cols = [3, 7 * 24 + 1, 7 * 24 + 2, 0, 5, 100, 250, 256, 511, 700, 24 * 40 - 1] + list(range(300, 305))
+    vf = d["v"].reshape(R, -1).astype(np.float32)
+    post = np.float32(q2.INV_SQRT8_F32)
+    sc = d["scale"].astype(np.float32)
+    for k in range(0, len(cols), ntok):
+        batch = cols[k:k + ntok]
+        x = np.zeros((ntok, C), dtype=np.float16)
+        for t, c in enumerate(batch):
+            x[t, c] = 1.0
+        y = pk.gemv(torch.from_numpy(x).cuda()).cpu().numpy()
+        for t, c in enumerate(batch):
+            want = (vf[:, c] * (sc * post)).astype(np.float16)
+            assert np.array_equal(y[t].view(np.uint16), want.view(np.uint16)), f"column {c}"
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_leech_decode_bit_exact(q2, layout):
     R, C = 70, 24 * 40 + 8
     d = _leech_with_exceptions(R, C, 3010)
-    pk = q2.Packed(q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C))
+    pk = q2.Packed(q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C, layout))
     out = pk.decode().cpu().numpy()
     body = R * 40 * 24
     v = out[:body].view(np.int8).reshape(R, 40, 24)
@@ -239,10 +270,11 @@ def test_trellis_full_size(q2, R, C):
     _check(y, otrellis.decode_f64(d["stream"][rows], d["table"], d["scale"][rows]), x, rows)
 
 
+@pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("R,C", [(17408, 5120), (5120, 17408)])
-def test_leech_full_size(q2, R, C):
+def test_leech_full_size(q2, R, C, layout):
     d = synth.leech(R, C, 3000 + (R > C))
     x = synth.activations(1, C, 3000 + (R > C))
-    _, y = _run(q2, q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C), x)
+    _, y = _run(q2, q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C, layout), x)
     rows = _sampled_rows(R)
     _check(y, oleech.decode_f64(d["v"][rows], d["scale"][rows], d["tail"][rows]), x, rows)
