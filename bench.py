@@ -53,7 +53,7 @@ L2_BYTES = 126 * 1024 * 1024
 # the stack's traffic per launch is that ratio times the stack's algorithmic
 # bytes per launch (traffic scales with the items processed).  A kernel with
 # no entry has no capture of its current code, and reports null.
-NCU_TRAFFIC_RATIO = {}
+NCU_TRAFFIC_RATIO = {"k_bpdq1": 27780608 / 27525120}
 
 
 def _peaks():
