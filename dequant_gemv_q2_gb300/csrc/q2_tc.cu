@@ -716,9 +716,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
         }
       }
   }
-  if (warp < 4 && ok && used > 0) {
-    const int orow = (tile * 4 + warp) * 32 + lane;
-    for (int c0 = 0; c0 < a.N; c0 += 16) {
+  // Epilogue over all decoder warps: warp w reads TMEM lane quarter w % 4 (the
+  // lanes a warp may access) and token columns 16 (w / 4) + 64 j, so at 64
+  // tokens 16 warps each take one 16-token group instead of 4 warps taking
+  // four groups one after another (the fused reduction's atomics of one group
+  // are in flight while the others are issued).
+  if (decoder && ok && used > 0) {
+    const int orow = (tile * 4 + rbl) * 32 + lane;
+    for (int c0 = 16 * (warp >> 2); c0 < a.N; c0 += 16 * (kDecWarps / 4)) {
       float v[16];
       tmem_ld16(tlane + (uint32_t)c0, v);
       if (FMT == Q2_BPDQ && a.fused) {
@@ -797,11 +802,16 @@ bool encode_x_map(CUtensorMap* map, const void* x, int C, int ntok, int N) {
 
 // The K split of the tensor-core launch and whether BPDQ reduces it inside
 // the launch.  One CTA per SM at a time, so the makespan is (waves of CTAs)
-// x (slices per CTA + about one slice of prologue and epilogue).  BPDQ with
+// x (slices per CTA + the CTA's fixed cost in slice times): about 1 us of
+// prologue, 2 us until the first group of two slices is decoded and handed
+// to the MMA warp, and 1.5 us of drain and epilogue, against about 1 us per
+// slice (globaltimer traces on GB300), so kSplitOverhead = 4.  BPDQ with
 // a K split reduces inside the launch when its accumulator words fit the
 // workspace's reserve (the scale 2^F keeps a split's partial, at most its
 // slices times the per-slice bound, below 2^45); everything else keeps fp32
 // partials for the reduce kernel.
+constexpr int kSplitOverhead = 4;
+
 void tc_plan(const q2_blob_header& d, int ntok, int* nsplit, int* fused) {
   const int sms = dev_info().sms;
   const int ntile = (d.Rpad + kRows - 1) / kRows, S = d.nslice;
@@ -809,7 +819,7 @@ void tc_plan(const q2_blob_header& d, int ntok, int* nsplit, int* fused) {
   for (int ns = 1; ns <= S; ++ns) {
     const long ctas = (long)ntile * ns;
     const long waves = (ctas + sms - 1) / sms;
-    const long cost = waves * ((S + ns - 1) / ns + 1);
+    const long cost = waves * ((S + ns - 1) / ns + kSplitOverhead);
     if (best < 0 || cost < best) {
       best = cost;
       *nsplit = ns;
