@@ -761,7 +761,7 @@ def main():
         extras["rot"] = rot
 
     achieved = step_bytes / (ms_step * 1e-3) / 1e9
-    kname = "k_bpdq1" if args.ntok == 1 else ("k_bpdq_mt" if args.ntok <= 6 else "k_tc")
+    kname = "k_bpdq1" if args.ntok == 1 else ("k_bpdqm" if args.ntok <= 6 else "k_tc")
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,

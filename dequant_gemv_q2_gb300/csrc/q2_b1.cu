@@ -339,71 +339,12 @@ __device__ __forceinline__ void ld_item(const unsigned char* base, int item_byte
   for (int k = 0; k < n; ++k) w[k] = ldg_stream(p + k * 512);
 }
 
-// Launch shapes: 8 warps and <= 128 registers per thread, two CTAs per SM.
-// BPDQ and Leech keep 1 item ahead per warp (measured: 2 ahead is slower).
+// Launch shape of the generic (run_b1) kernels, Leech and trellis: one
+// 16-warp CTA per SM, one item ahead per warp in registers (measured: 2
+// ahead is slower).
 constexpr int kWarps = 16;
-// CTAs per SM the BPDQ, no-weights and trellis kernels are built for.  With
-// 2, 16 warps fit in 64 registers and an SM holds one CTA of the running
-// GEMV and one of the GEMV launched after it, whose CTAs are then resident
-// early (no launch ramp): faster for GEMVs of ~20 items per CTA (Qwen3-8B
-// o-proj 2.9 vs 3.6 us), slower for large ones whose weight loads then
-// overlap less (gate_up 9.6 vs 8.3 us) and over the whole 8B stack (measured
-// on GB300).  Leech and the 2-token kernel run one per SM in any case.
 constexpr int kMinBlocks = 1;
-constexpr int kBpdqAhead = 1;
 constexpr int kLeechAhead = 1;
-
-// ------------------------------------------------------------------- BPDQ
-struct BpdqArgs {
-  B1 c;
-  const unsigned char* bits;
-  const __half2* c01;
-  const __half* off;
-};
-
-template <int NT>
-struct BpdqF {
-  struct Item {
-    uint4 w[4];          // 64 bytes of planes: two uint4 per plane
-    uint32_t c01;        // c0 | c1 << 16 (fp16)
-    unsigned short off;  // fp16
-  };
-  static constexpr bool kStaged = true;
-  static constexpr int kGroup = 1;
-  static constexpr int kTok = 1;
-  const BpdqArgs& a;
-  __device__ void load(int it, int g, int lane, Item& b) const {
-    ld_item(a.bits, Q2_ITEM_BYTES_BPDQ, it, lane, b.w, 4);
-    const size_t r = (size_t)g * a.c.Rpad + (size_t)(it - g * a.c.nrb) * 32 + lane;
-    b.c01 = __ldg(reinterpret_cast<const unsigned int*>(a.c01) + r);
-    b.off = __ldg(reinterpret_cast<const unsigned short*>(a.off) + r);
-  }
-  __device__ void stage_extra(int, int, unsigned char*) {}
-  __device__ void tables(int, const __half* xs, unsigned char* tail) const {
-    build_table<NT>(xs, tab1(), reinterpret_cast<float*>(tail + kTailGsum));
-  }
-  __device__ void compute(int, int, int lane, const Item& b, float (&p)[1]) const {
-    const uint32_t lane4 = (uint32_t)lane * 4u | kLane4Hi;
-    const float S0 = plane_sum(lane4, b.w[0], b.w[1]);
-    const float S1 = plane_sum(lane4, b.w[2], b.w[3]);
-    const float2 cf = __half22float2(*reinterpret_cast<const __half2*>(&b.c01));
-    const float of = __half2float(__ushort_as_half(b.off));
-    const float xs = *reinterpret_cast<const float*>(q2_smem + kTailGsum);
-    p[0] = fmaf(cf.x, S0, fmaf(cf.y, S1, of * xs));
-  }
-  __device__ void finish(int tok, int row, float v) const { a.c.y[(size_t)tok * a.c.R + row] = __float2half_rn(v); }
-};
-
-// The tail sits at the start of dynamic shared memory for every
-// single-token table kernel.
-__device__ __forceinline__ unsigned char* tail1() { return q2_smem; }
-
-template <int W, int AHEAD>
-__global__ void __launch_bounds__(W * 32, kMinBlocks) k_bpdq_b1(BpdqArgs a) {
-  if ((uint32_t)__cvta_generic_to_shared(q2_smem) + kTailFixed > kTabAddr) return;   // layout needs a low window base
-  BpdqF<W * 32> f{a};
-  run_b1<W, AHEAD>(f, a.c, tail1());
-}
 
 // ------------------------------------------------------------------ Leech
 struct LeechArgs {
@@ -511,49 +452,15 @@ struct LeechF {
   }
 };
 
+// The tail sits at the start of dynamic shared memory for every
+// single-token table kernel.
+__device__ __forceinline__ unsigned char* tail1() { return q2_smem; }
+
 template <int W, int AHEAD, int NP>
 __global__ void __launch_bounds__(W * 32, 1) k_leech_b1(LeechArgs a) {
   if ((uint32_t)__cvta_generic_to_shared(q2_smem) + kTailFixed > kTabAddr) return;   // layout needs a low window base
   LeechF<W * 32, NP> f{a};
   run_b1<W, AHEAD>(f, a.c, tail1());
-}
-
-// ------------------------------------------------------- no-weights control
-// Same grid, PDL, table build, per-lane lookups and in-launch reduction as
-// k_bpdq_b1; the "weight" words are derived from the lane and item index
-// instead of being loaded, so the kernel reads x and writes the workspace
-// and y only.
-template <int NT>
-struct NoWeightsF {
-  struct Item {
-    uint32_t h;
-  };
-  static constexpr bool kStaged = true;
-  static constexpr int kGroup = 1;
-  static constexpr int kTok = 1;
-  const BpdqArgs& a;
-  __device__ void load(int it, int, int lane, Item& b) const { b.h = (uint32_t)it * 0x9E3779B9u ^ (lane * 0x85EBCA6Bu); }
-  __device__ void stage_extra(int, int, unsigned char*) {}
-  __device__ void tables(int, const __half* xs, unsigned char* tail) const {
-    build_table<NT>(xs, tab1(), reinterpret_cast<float*>(tail + kTailGsum));
-  }
-  __device__ void compute(int, int, int lane, const Item& b, float (&p)[1]) const {
-    const uint32_t h = b.h, lane4 = (uint32_t)lane * 4u | kLane4Hi;
-    const uint4 w0 = make_uint4(h, h ^ 0x5bd1e995u, h * 3u, h * 5u);
-    const uint4 w1 = make_uint4(h * 7u, h ^ 0x27d4eb2fu, h * 11u, h * 13u);
-    const float S0 = plane_sum(lane4, w0, w1);
-    const float S1 = plane_sum(lane4, w1, w0);
-    const float xs = *reinterpret_cast<const float*>(q2_smem + kTailGsum);
-    p[0] = fmaf(0.02f, S0, fmaf(0.01f, S1, 0.01f * xs));
-  }
-  __device__ void finish(int tok, int row, float v) const { a.c.y[(size_t)tok * a.c.R + row] = __float2half_rn(v); }
-};
-
-template <int W>
-__global__ void __launch_bounds__(W * 32, kMinBlocks) k_noweights_b1(BpdqArgs a) {
-  if ((uint32_t)__cvta_generic_to_shared(q2_smem) + kTailFixed > kTabAddr) return;   // layout needs a low window base
-  NoWeightsF<W * 32> f{a};
-  run_b1<W, 1>(f, a.c, tail1());
 }
 
 // ------------------------------------------------ BPDQ, one token (lean)
@@ -631,13 +538,13 @@ __device__ __forceinline__ float2 planes_sum(uint32_t lane4, const uint4& a0, co
 }
 
 template <bool kWeights>
-__device__ __forceinline__ void lean_load(const LeanArgs& a, const uint4* wp, size_t ci, int it, int lane,
-                                          LeanItem& b) {
+__device__ __forceinline__ void lean_load(const uint32_t* c01, const unsigned short* off, const uint4* wp, size_t ci,
+                                          int it, int lane, LeanItem& b) {
   if constexpr (kWeights) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) b.w[k] = ldg_stream(wp + k * 32);
-    b.c01 = __ldg(a.c01 + ci);
-    b.off = __ldg(a.off + ci);
+    b.c01 = __ldg(c01 + ci);
+    b.off = __ldg(off + ci);
   } else {
     // the no-weights control: "weights" derived from the item and lane
     const uint32_t h = (uint32_t)it * 0x9E3779B9u ^ ((uint32_t)lane * 0x85EBCA6Bu);
@@ -730,7 +637,7 @@ __global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_c
     unsigned long long* ap = a.acc + (size_t)rb * 32 + lane;
     int row = rb * 32 + lane;
     LeanItem b0, b1;
-    if (it < j1) lean_load<kWeights>(a, wp, ci, it, lane, b0);
+    if (it < j1) lean_load<kWeights>(a.c01, a.off, wp, ci, it, lane, b0);
     if (!waited) {
       if (threadIdx.x == 0) {                           // slots past the first: at once
         q2_pf rest = a.pf;
@@ -751,7 +658,7 @@ __global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_c
     // two items per trip so the two buffers are named statically
     for (; it < j1; it += 2 * W) {
       const bool m1 = it + W < j1;
-      if (m1) lean_load<kWeights>(a, wp + kStrideW, ci + W * 32, it + W, lane, b1);
+      if (m1) lean_load<kWeights>(a.c01, a.off, wp + kStrideW, ci + W * 32, it + W, lane, b1);
       if constexpr (kPaced) pp.step(lane);
       float p = lean_partial(lane4, b0, gs);
       lean_settle(pd, a);
@@ -761,7 +668,7 @@ __global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_c
       pd.row = row;
       if (!m1) break;
       const bool m2 = it + 2 * W < j1;
-      if (m2) lean_load<kWeights>(a, wp + 2 * kStrideW, ci + 2 * W * 32, it + 2 * W, lane, b0);
+      if (m2) lean_load<kWeights>(a.c01, a.off, wp + 2 * kStrideW, ci + 2 * W * 32, it + 2 * W, lane, b0);
       if constexpr (kPaced) pp.step(lane);
       p = lean_partial(lane4, b1, gs);
       lean_settle(pd, a);
@@ -800,13 +707,45 @@ __global__ void __launch_bounds__(W * 32, kLeanMinBlocks) k_bpdq1(const __grid_c
 constexpr int kMtMaxTok = 6;
 constexpr int kPairBytes = 256 * 32 * 8;                   // 64 KiB per token pair
 
+// ------------------------------------------------ BPDQ, token pairs (lean)
+// NP token-pair tables per slice (64 KiB each): for the pair (2p, 2p+1)
+//   E_p[v][b] = (sum of x_2p over the set bits of byte v at column-byte b,
+//                the same for x_2p+1)
+// at byte offset p*64 KiB + v*256 + b*8, with no duplicated columns: a lane
+// at rotated position P reads column-byte b = (P + lane) mod 32, whose
+// address byte b*8 it keeps in one of 11 lane-constant registers (three
+// positions each), so one byte permute still forms v*256 + b*8; each lookup
+// is one 8-byte load and one packed fp32 add per pair, and a half-warp's 16
+// lanes read 16 different column-bytes (conflict-free).  The item loop is
+// k_bpdq1's (host-computed CTA ranges, pointer-walked items, atomics settled
+// one item later).  Per token the lookups, sums and epilogue are those of
+// k_bpdq1 in the same order (lookup P into accumulator P mod 4, then
+// (s0 + s1) + (s2 + s3)), so every token's output is bit-identical to the
+// same token run alone (batch invariance).
+struct LeanMArgs {
+  const __half* x;              // [ntok][C]
+  __half* y;                    // [ntok][R]
+  unsigned long long* acc;      // [ntok][Rpad] accumulator words (zero between calls)
+  const uint4* bits;
+  const uint32_t* c01;
+  const unsigned short* off;
+  float fscale, finv;
+  int R, C, Rpad, nrb, nslice, ntok;
+  q2_pf pf;
+  uint32_t start[kLeanMaxGrid + 1];
+};
+
+// The pair tables of slice g straight from global x (16 tasks share each
+// 16-byte load); per token the same sums in the same order as build_table.
 template <int NT, int NP>
-__device__ __forceinline__ void build_pairs(const __half* xs, int ntok, float* T, float* gsum) {
+__device__ __forceinline__ void build_pairs_g(const __half* __restrict__ x, int C, int ntok, int g, float* T,
+                                              float* gsum) {
   for (int e = threadIdx.x; e < 512 * NP; e += NT) {
     const int p = e >> 9, h = (e >> 5) & 15, b = e & 31;
+    const size_t col = (size_t)g * Q2_SLICE + 8 * b;
     float xa[8], xb[8];
     {
-      const uint4 raw = *reinterpret_cast<const uint4*>(xs + (2 * p) * Q2_SLICE + 8 * b);
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(2 * p) * C + col));
       const __half2* hv = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -816,7 +755,7 @@ __device__ __forceinline__ void build_pairs(const __half* xs, int ntok, float* T
       }
     }
     if (2 * p + 1 < ntok) {                            // an odd count leaves the last pair half empty
-      const uint4 raw = *reinterpret_cast<const uint4*>(xs + (2 * p + 1) * Q2_SLICE + 8 * b);
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(2 * p + 1) * C + col));
       const __half2* hv = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -828,7 +767,7 @@ __device__ __forceinline__ void build_pairs(const __half* xs, int ntok, float* T
 #pragma unroll
       for (int i = 0; i < 8; ++i) xb[i] = 0.f;
     }
-    float2 hs = make_float2(0.f, 0.f);                  // sums selected by the high nibble h
+    float2 hs = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
       if ((h >> i) & 1) {
@@ -843,10 +782,10 @@ __device__ __forceinline__ void build_pairs(const __half* xs, int ntok, float* T
       const int i = (low == 1) ? 0 : (low == 2) ? 1 : (low == 4) ? 2 : 3;
       sv[n] = make_float2(sv[n ^ low].x + xa[i], sv[n ^ low].y + xb[i]);
     }
-    float2* col = reinterpret_cast<float2*>(reinterpret_cast<char*>(T) + p * kPairBytes) + (h * 16) * 32 + b;
+    float2* colp = reinterpret_cast<float2*>(reinterpret_cast<char*>(T) + p * kPairBytes) + (h * 16) * 32 + b;
 #pragma unroll
-    for (int n = 0; n < 16; ++n) col[n * 32] = sv[n];
-    if (h == 15) {                                      // this warp holds the 32 bytes' full sums
+    for (int n = 0; n < 16; ++n) colp[n * 32] = sv[n];
+    if (h == 15) {
       float va = sv[15].x, vb = sv[15].y;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -861,84 +800,147 @@ __device__ __forceinline__ void build_pairs(const __half* xs, int ntok, float* T
   }
 }
 
-template <int NT, int NP>
-struct BpdqMtF {
-  struct Item {
-    uint4 w[4];
-    uint32_t c01;
-    unsigned short off;
-  };
-  static constexpr bool kStaged = true;
-  static constexpr int kGroup = 1;
-  static constexpr int kTok = 2 * NP;
-  const BpdqArgs& a;
-  unsigned char* tail;
-  uint32_t rot[11];      // byte j of rot[k]: ((3k + j + lane) mod 32) * 8; byte 3 = 0
-  __device__ void init(int lane) {
+template <int NP>
+__device__ __forceinline__ void pair_plane(const uint32_t (&rot)[11], const uint4& c0, const uint4& c1,
+                                           float2 (&S)[NP]) {
+  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const char* base = reinterpret_cast<const char*>(q2_smem);
+  float2 acc[NP][4];
 #pragma unroll
-    for (int k = 0; k < 11; ++k) {
-      uint32_t r = 0;
+  for (int p = 0; p < NP; ++p)
 #pragma unroll
-      for (int j = 0; j < 3; ++j) r |= (uint32_t)(((3 * k + j + lane) & 31) * 8) << (8 * j);
-      rot[k] = r;
-    }
-  }
-  __device__ void load(int it, int g, int lane, Item& b) const {
-    ld_item(a.bits, Q2_ITEM_BYTES_BPDQ, it, lane, b.w, 4);
-    const size_t r = (size_t)g * a.c.Rpad + (size_t)(it - g * a.c.nrb) * 32 + lane;
-    b.c01 = __ldg(reinterpret_cast<const unsigned int*>(a.c01) + r);
-    b.off = __ldg(reinterpret_cast<const unsigned short*>(a.off) + r);
-  }
-  __device__ void stage_extra(int, int, unsigned char*) {}
-  __device__ void tables(int, const __half* xs, unsigned char* tl) const {
-    build_pairs<NT, NP>(xs, a.c.ntok, reinterpret_cast<float*>(q2_smem), reinterpret_cast<float*>(tl + kTailGsum));
-  }
-  // Lookup P into accumulator P mod 4, then (s0 + s1) + (s2 + s3): the
-  // order plane_sum uses at one token, so each token's partial (and output)
-  // is bit-identical to the single-token kernel's.
-  __device__ void plane(const uint4& c0, const uint4& c1, float2 (&S)[NP]) const {
-    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    const char* base = reinterpret_cast<const char*>(q2_smem);
-    float2 acc[NP][4];
+    for (int k = 0; k < 4; ++k) acc[p][k] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int P = 0; P < 32; ++P) {
+    const uint32_t sel = (4u + (uint32_t)(P % 3)) | ((uint32_t)(P & 3) << 4) | 0x7700u;
+    const uint32_t ad = __byte_perm(w[P >> 2], rot[P / 3], sel);
 #pragma unroll
     for (int p = 0; p < NP; ++p)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[p][k] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int P = 0; P < 32; ++P) {
-      const uint32_t sel = (4u + (uint32_t)(P % 3)) | ((uint32_t)(P & 3) << 4) | 0x7700u;
-      const uint32_t ad = __byte_perm(w[P >> 2], rot[P / 3], sel);
-#pragma unroll
-      for (int p = 0; p < NP; ++p)
-        acc[p][P & 3] = __fadd2_rn(acc[p][P & 3], *reinterpret_cast<const float2*>(base + p * kPairBytes + ad));
-    }
-#pragma unroll
-    for (int p = 0; p < NP; ++p) S[p] = __fadd2_rn(__fadd2_rn(acc[p][0], acc[p][1]), __fadd2_rn(acc[p][2], acc[p][3]));
+      acc[p][P & 3] = __fadd2_rn(acc[p][P & 3], *reinterpret_cast<const float2*>(base + p * kPairBytes + ad));
   }
-  __device__ void compute(int, int, int, const Item& b, float (&p)[2 * NP]) const {
-    float2 S0[NP], S1[NP];
 #pragma unroll
-    for (int q = 0; q < NP; ++q) S0[q] = S1[q] = make_float2(0.f, 0.f);
-    plane(b.w[0], b.w[1], S0);
-    plane(b.w[2], b.w[3], S1);
-    const float2 cf = __half22float2(*reinterpret_cast<const __half2*>(&b.c01));
-    const float of = __half2float(__ushort_as_half(b.off));
-    const float* xs = reinterpret_cast<const float*>(tail + kTailGsum);
-#pragma unroll
-    for (int q = 0; q < NP; ++q) {
-      p[2 * q] = fmaf(cf.x, S0[q].x, fmaf(cf.y, S1[q].x, of * xs[2 * q]));
-      p[2 * q + 1] = fmaf(cf.x, S0[q].y, fmaf(cf.y, S1[q].y, of * xs[2 * q + 1]));
-    }
-  }
-  __device__ void finish(int tok, int row, float v) const { a.c.y[(size_t)tok * a.c.R + row] = __float2half_rn(v); }
+  for (int p = 0; p < NP; ++p) S[p] = __fadd2_rn(__fadd2_rn(acc[p][0], acc[p][1]), __fadd2_rn(acc[p][2], acc[p][3]));
+}
+
+template <int NP>
+struct LeanMPending {
+  unsigned long long old[2 * NP], add[2 * NP];
+  unsigned long long* p;    // token 0's word of the row
+  int row;                  // -1: nothing pending
 };
 
-template <int W, int AHEAD, int NP>
-__global__ void __launch_bounds__(W * 32, 1) k_bpdq_mt(BpdqArgs a) {
-  unsigned char* tail = q2_smem + (size_t)NP * kPairBytes;
-  BpdqMtF<W * 32, NP> f{a, tail};
-  f.init(threadIdx.x & 31);
-  run_b1<W, AHEAD>(f, a.c, tail);
+template <int NP>
+__device__ __forceinline__ void leanm_settle(LeanMPending<NP>& pd, const LeanMArgs& a) {
+  if (pd.row < 0) return;
+#pragma unroll
+  for (int t = 0; t < 2 * NP; ++t)
+    if (t < a.ntok) {
+      const unsigned long long w = pd.old[t] + pd.add[t];
+      if ((int)(w >> 56) == a.nslice) {
+        if (pd.row < a.R) a.y[(size_t)t * a.R + pd.row] = __float2half_rn(fx_value(w, a.nslice, a.finv));
+        pd.p[(size_t)t * a.Rpad] = 0ull;
+      }
+    }
+  pd.row = -1;
+}
+
+template <int NP>
+__device__ __forceinline__ void leanm_issue(LeanMPending<NP>& pd, const LeanMArgs& a, unsigned long long* ap, int row,
+                                            const float (&p)[2 * NP]) {
+#pragma unroll
+  for (int t = 0; t < 2 * NP; ++t)
+    if (t < a.ntok) {
+      unsigned long long* word = ap + (size_t)t * a.Rpad;
+      pd.add[t] = fx_prepare(word, p[t], a.fscale);
+      pd.old[t] = atomicAdd(word, pd.add[t]);
+    }
+  pd.p = ap;
+  pd.row = row;
+}
+
+template <int NP>
+__device__ __forceinline__ void leanm_partials(const uint32_t (&rot)[11], const LeanItem& b, const float* gsum,
+                                               float (&p)[2 * NP]) {
+  float2 S0[NP], S1[NP];
+  pair_plane<NP>(rot, b.w[0], b.w[1], S0);
+  pair_plane<NP>(rot, b.w[2], b.w[3], S1);
+  const float2 cf = __half22float2(*reinterpret_cast<const __half2*>(&b.c01));
+  const float of = __half2float(__ushort_as_half(b.off));
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    p[2 * q] = fmaf(cf.x, S0[q].x, fmaf(cf.y, S1[q].x, of * gsum[2 * q]));
+    p[2 * q + 1] = fmaf(cf.x, S0[q].y, fmaf(cf.y, S1[q].y, of * gsum[2 * q + 1]));
+  }
+}
+
+template <int W, int NP>
+__global__ void __launch_bounds__(W * 32, 1) k_bpdqm(const __grid_constant__ LeanMArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t rot[11];      // byte j of rot[k]: ((3k + j + lane) mod 32) * 8; byte 3 = 0
+#pragma unroll
+  for (int k = 0; k < 11; ++k) {
+    uint32_t r = 0;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) r |= (uint32_t)(((3 * k + j + lane) & 31) * 8) << (8 * j);
+    rot[k] = r;
+  }
+  const int i0 = (int)a.start[blockIdx.x], i1 = (int)a.start[blockIdx.x + 1];
+  float* gsum = reinterpret_cast<float*>(q2_smem + (size_t)NP * kPairBytes + kTailGsum);
+  LeanMPending<NP> pd;
+  pd.row = -1;
+  bool waited = false;
+  int g = i0 / a.nrb;
+  for (int j0 = i0; j0 < i1; ++g) {
+    const int j1 = min(i1, (g + 1) * a.nrb);
+    int it = j0 + warp;
+    const int rb = it - g * a.nrb;
+    const uint4* wp = a.bits + (size_t)it * (Q2_ITEM_BYTES_BPDQ / 16) + lane;
+    size_t ci = (size_t)g * a.Rpad + (size_t)rb * 32 + lane;
+    unsigned long long* ap = a.acc + (size_t)rb * 32 + lane;
+    int row = rb * 32 + lane;
+    LeanItem b0, b1;
+    if (it < j1) lean_load<true>(a.c01, a.off, wp, ci, it, lane, b0);
+    if (!waited) {
+      if (threadIdx.x == 0) prefetch_next(a.pf);
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    } else {
+      __syncthreads();                                  // the previous slice's tables are no longer read
+    }
+    build_pairs_g<W * 32, NP>(a.x, a.C, a.ntok, g, reinterpret_cast<float*>(q2_smem), gsum);
+    __syncthreads();
+    float gs[2 * NP];
+#pragma unroll
+    for (int t = 0; t < 2 * NP; ++t) gs[t] = gsum[t];
+    constexpr int kStrideW = W * (Q2_ITEM_BYTES_BPDQ / 16);
+    for (; it < j1; it += 2 * W) {
+      const bool m1 = it + W < j1;
+      if (m1) lean_load<true>(a.c01, a.off, wp + kStrideW, ci + W * 32, it + W, lane, b1);
+      float p[2 * NP];
+      leanm_partials<NP>(rot, b0, gs, p);
+      leanm_settle<NP>(pd, a);
+      leanm_issue<NP>(pd, a, ap, row, p);
+      if (!m1) break;
+      const bool m2 = it + 2 * W < j1;
+      if (m2) lean_load<true>(a.c01, a.off, wp + 2 * kStrideW, ci + 2 * W * 32, it + 2 * W,
+                              lane, b0);
+      leanm_partials<NP>(rot, b1, gs, p);
+      leanm_settle<NP>(pd, a);
+      leanm_issue<NP>(pd, a, ap + W * 32, row + W * 32, p);
+      wp += 2 * kStrideW;
+      ci += 2 * W * 32;
+      ap += 2 * W * 32;
+      row += 2 * W * 32;
+    }
+    j0 = j1;
+  }
+  if (!waited) {
+    if (threadIdx.x == 0) prefetch_next(a.pf);
+    pdl_wait();
+    pdl_trigger();
+  }
+  leanm_settle<NP>(pd, a);
 }
 
 // ---------------------------------------------------------------- trellis
@@ -1048,13 +1050,8 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks) k_trellis_b1(TrellisArgs a
 }
 
 // ------------------------------------------------------------ host side
-// With kMinBlocks == 2 the kernels ask for more than a third of an SM's
-// shared memory, so an SM holds at most two of their CTAs: while a GEMV
-// runs, every SM holds one of its CTAs and has room for exactly one CTA of
-// the next GEMV, which therefore spreads one per SM.  With kMinBlocks == 1
-// they ask for more than half.  The kernels for 3..6 tokens (two or three
-// token-pair tables) need more than half and run one per SM with the whole
-// register file.
+// The generic kernels ask for more than half of an SM's shared memory, so an
+// SM holds one of their CTAs.
 constexpr int kOneCtaSmem = 116 * 1024;
 constexpr int kMaxDynSmem = 227 * 1024;   // opt-in dynamic shared memory per CTA
 constexpr int kTwoCtaSmem = kMinBlocks == 2 ? 80 * 1024 : kOneCtaSmem;
@@ -1146,6 +1143,32 @@ LeanArgs make_lean(const q2_handle* h, const void* x, void* y, const q2_pf* pf, 
 
 int lean_grid(const q2_blob_header& d) { return std::min(geometry(d).grid, kLeanMaxGrid); }
 
+// The lean multi-token kernel's arguments: those of make_lean plus ntok.
+LeanMArgs make_leanm(const q2_handle* h, const void* x, void* y, int ntok, const q2_pf* pf, int grid) {
+  const LeanArgs l = make_lean(h, x, y, pf, grid);
+  LeanMArgs a;
+  a.x = l.x;
+  a.y = l.y;
+  a.acc = l.acc;
+  a.bits = l.bits;
+  a.c01 = l.c01;
+  a.off = l.off;
+  a.fscale = l.fscale;
+  a.finv = l.finv;
+  a.R = l.R;
+  a.C = l.C;
+  a.Rpad = l.Rpad;
+  a.nrb = l.nrb;
+  a.nslice = l.nslice;
+  a.ntok = ntok;
+  a.pf = l.pf;
+  for (int b = 0; b <= grid; ++b) a.start[b] = l.start[b];
+  return a;
+}
+
+// Warps per CTA of the one-pair kernel (127 registers).
+constexpr int kMWarps = 16;
+
 }  // namespace
 }  // namespace q2
 
@@ -1160,32 +1183,31 @@ extern "C" int q2_b1_bpdq(const q2_handle* h, const void* x, void* y, void* stre
   return launch_pdl(k_bpdq1<kLeanW, true, false>, a, G, kLeanW * 32, kTabSmem, stream);
 }
 
-// BPDQ at 2..6 tokens on CUDA cores (x is [ntok][C]; partials [ntok][nslice][Rpad]).
+// BPDQ at 2..6 tokens on CUDA cores.  Each token pair runs through the lean
+// one-pair kernel and an odd last token through the single-token kernel,
+// stream-ordered (x is [ntok][C], y [ntok][R]); each launch uses the first
+// 2 x Rpad accumulator words and leaves them zero for the next.  Measured on
+// the Qwen3-8B stack (ms per step at 2/3/4/5/6 tokens): one launch with
+// ceil(ntok/2) pair tables (12 warps for two pairs, 8 for three, by
+// registers) ran 0.92/1.81/2.01/3.17/3.42, the pair launches 0.92 at two
+// tokens and less at more, since the lookups are bound by shared-memory
+// bandwidth and more warps hide it better.  Every token's result is
+// bit-identical to the same token run alone through q2_b1_bpdq.
 extern "C" int q2_mt_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream, const q2_pf* pf) {
   const q2_blob_header& d = h->hdr;
   if (ntok < 2 || ntok > kMtMaxTok) return Q2_ENTOK;
   if (!b1_shape_ok(d)) return Q2_ESHAPE;
-  BpdqArgs a;
-  a.c = make_b1(h, x, y, ntok);
-  a.bits = h->dev + d.off[SEC_BPDQ_BITS];
-  a.c01 = reinterpret_cast<const __half2*>(h->dev + d.off[SEC_BPDQ_C01]);
-  a.off = reinterpret_cast<const __half*>(h->dev + d.off[SEC_BPDQ_OFF]);
-  // Tokens go in pairs through the one-pair kernel, an odd last token
-  // through the single-token kernel: measured faster than two- and
-  // three-pair kernels (their registers allow only 8 warps per SM), and
-  // every token's result is the same bit for bit whichever kernel runs it.
-  // The launches are stream-ordered; each leaves its accumulator words zero
-  // for the next.
-  const Geo g = geometry(d);
+  const int G = lean_grid(d);
   const __half* xh = static_cast<const __half*>(x);
   __half* yh = static_cast<__half*>(y);
   for (int t = 0; t < ntok; t += 2) {
+    const q2_pf* p = t == 0 ? pf : nullptr;
     int st;
     if (t + 1 < ntok) {
-      a.c = make_b1(h, xh + (size_t)t * d.C, yh + (size_t)t * d.R, 2, t == 0 ? pf : nullptr);
-      st = launch1(k_bpdq_mt<kWarps, 2, 1>, a, g, kWarps * 32, 1 * kPairBytes, stream);
+      const LeanMArgs a = make_leanm(h, xh + (size_t)t * d.C, yh + (size_t)t * d.R, 2, p, G);
+      st = launch_pdl(k_bpdqm<kMWarps, 1>, a, G, kMWarps * 32, kPairBytes + 256, stream);
     } else {
-      st = q2_b1_bpdq(h, xh + (size_t)t * d.C, yh + (size_t)t * d.R, stream, t == 0 ? pf : nullptr);
+      st = q2_b1_bpdq(h, xh + (size_t)t * d.C, yh + (size_t)t * d.R, stream, p);
     }
     if (st) return st;
   }
