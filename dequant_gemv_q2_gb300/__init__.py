@@ -62,6 +62,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "q2_gemv_chain": [i32, vp, vp, vp, vp, i32, i32, vp],
         "q2_gemv_bpdq_noalloc": [vp, vp, vp, vp],
         "q2_device_errors": [ctypes.POINTER(ctypes.c_uint)],
+        "q2_debug_wait_limit": [ctypes.c_longlong],
         "q2_rotate": [vp, vp, i32, i32, i32, vp, vp, vp],
         "q2_rotate_split": [i32, ctypes.POINTER(i32), ctypes.POINTER(i32)],
     }
@@ -80,7 +81,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
 EXPORTS = ["q2_pack_fp16", "q2_pack_bpdq", "q2_pack_trellis", "q2_pack_leech", "q2_pack_noweights",
            "q2_bind", "q2_unbind", "q2_workspace_bytes", "q2_set_workspace", "q2_info", "q2_bytes",
            "q2_gemv", "q2_gemv_chain", "q2_decode_bytes", "q2_decode", "q2_strerror", "q2_gemv_bpdq_noalloc",
-           "q2_device_errors", "q2_rotate", "q2_rotate_split"]
+           "q2_device_errors", "q2_debug_wait_limit", "q2_rotate", "q2_rotate_split"]
 
 
 def q2_strerror(status: int) -> str:
@@ -159,6 +160,11 @@ def device_errors() -> int:
     v = ctypes.c_uint(0)
     _check(load().q2_device_errors(ctypes.byref(v)), "q2_device_errors")
     return v.value
+
+
+def debug_wait_limit(polls: int) -> None:
+    """Test hook: limit the tensor-core kernel's stage waits to `polls` polls (0 = normal)."""
+    _check(load().q2_debug_wait_limit(int(polls)), "q2_debug_wait_limit")
 
 
 class Packed:

@@ -59,6 +59,10 @@ extern __shared__ __align__(1024) unsigned char q2_smem[];
 extern "C" int q2_launch_reduce_n(const q2_handle* h, const void* x, void* y, int ntok, int nsplit, void* stream);
 
 __device__ unsigned int q2_tc_error = 0;
+// Poll limit of the helper warp's stage waits (decoded A and x tile of a
+// slice ready), 0 = the normal bound.  Set only by q2_debug_wait_limit, so
+// that a test can make these waits run out and check the error path.
+__device__ long long q2_tc_stage_wait_limit = 0;
 
 namespace q2 {
 namespace {
@@ -396,6 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
   uint64_t* fullB = emptyA + kStagesA;                                      // TMA bytes
   uint64_t* emptyG = fullB + kStagesB;        // MMA commits per group: the group's B stages are free
   uint32_t* tslot = reinterpret_cast<uint32_t*>(emptyG + 2);
+  // set by the first role whose wait runs out: the others stop waiting on
+  // each other (the drains of copies and MMAs in flight keep their full bound)
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool decoder = warp < kDecWarps;
   const int rbl = warp & 3, part = (warp >> 2) & (kParts - 1);   // row block in tile (= TMEM lane quarter), part of the slice
@@ -416,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
     }
     for (int st = 0; st < kStagesB; ++st) mbar_init(saddr(&fullB[st]), 1);
     for (int st = 0; st < 2; ++st) mbar_init(saddr(&emptyG[st]), 1);
+    *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -536,20 +544,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
         if (lane == 0) mbar_arrive(fb);
       }
     };
-    for (int i = 0; i < min(kStagesB, used); ++i) produce(i);
+    const long long stage_limit = q2_tc_stage_wait_limit > 0 ? q2_tc_stage_wait_limit : kSpinLimit;
+    int produced = min(kStagesB, used), waitedB = 0;   // slices whose x copy was issued / seen complete
+    for (int i = 0; i < produced; ++i) produce(i);
     int handed = 0;
     for (int g = 0; g * kGroup < used; ++g) {
       bool ready = true;
 #pragma unroll
       for (int u = 0; u < kGroup; ++u) {
         const int i = g * kGroup + u;
-        if (ready && i < used)
-          ready = mbar_wait(saddr(&fullA[i % kStagesA]), (uint32_t)(i / kStagesA) & 1u) &&
-                  mbar_wait(saddr(&fullB[i % kStagesB]), (uint32_t)(i / kStagesB) & 1u);
+        if (ready && i < used) {
+          ready = mbar_wait(saddr(&fullA[i % kStagesA]), (uint32_t)(i / kStagesA) & 1u, stage_limit);
+          ready = ready && mbar_wait(saddr(&fullB[i % kStagesB]), (uint32_t)(i / kStagesB) & 1u, stage_limit);
+          if (__all_sync(~0u, ready)) waitedB = i + 1;
+        }
       }
       if (!__all_sync(~0u, ready)) {
         ok = false;
-        if (lane == 0) atomicExch(&q2_tc_error, 3u);
+        if (lane == 0) {
+          atomicExch(&q2_tc_error, 3u);
+          *abort_flag = 1;
+        }
       }
       tc_fence_before();
       ok = handoff(ok);
@@ -558,14 +573,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
       // refill the B stages of group g - 1 (its MMAs precede group g's) with the slices kStagesB later
       const int j0 = (g - 1) * kGroup + kStagesB;
       if (g >= 1 && j0 < used) {
-        if (!__all_sync(~0u, mbar_wait(saddr(&emptyG[(g - 1) & 1]), (uint32_t)((g - 1) >> 1) & 1u))) {
+        if (!__all_sync(~0u, mbar_wait(saddr(&emptyG[(g - 1) & 1]), (uint32_t)((g - 1) >> 1) & 1u, kSpinLimit,
+                                       abort_flag))) {
           ok = false;
-          if (lane == 0) atomicExch(&q2_tc_error, 4u);
+          if (lane == 0) {
+            atomicExch(&q2_tc_error, 4u);
+            *abort_flag = 1;
+          }
         }
         if (ok)
-          for (int u = 0; u < kGroup && j0 + u < used; ++u) produce(j0 + u);
+          for (int u = 0; u < kGroup && j0 + u < used; ++u) {
+            produce(j0 + u);
+            produced = j0 + u + 1;
+          }
       }
     }
+    // on an error, wait (with the full bound) for every x copy still in
+    // flight, so that none lands in shared memory after the CTA has exited
+    if (!ok)
+      for (int i = waitedB; i < produced; ++i)
+        (void)mbar_wait(saddr(&fullB[i % kStagesB]), (uint32_t)(i / kStagesB) & 1u);
     // the last commit covers every MMA issued; on an error, also give the
     // copies in flight time to land before the CTA exits
     if (handed > 0 &&
@@ -587,9 +614,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
       if (valid && i + 2 < used) load(s + 2, n2, v2, p2);
       // the stage is free once the MMAs of slice i - kStagesA have completed
       if (i >= kStagesA &&
-          !__all_sync(~0u, mbar_wait(saddr(&emptyA[sa]), (uint32_t)(i / kStagesA - 1) & 1u))) {
+          !__all_sync(~0u, mbar_wait(saddr(&emptyA[sa]), (uint32_t)(i / kStagesA - 1) & 1u, kSpinLimit, abort_flag))) {
         ok = false;
-        if (lane == 0) atomicExch(&q2_tc_error, 6u);
+        if (lane == 0) {
+          atomicExch(&q2_tc_error, 6u);
+          *abort_flag = 1;
+        }
         break;
       }
       tc_fence_after();
@@ -691,9 +721,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
     }
     // the accumulator is final once the last slice's commit has arrived
     if (ok && warp < 4 && used > 0 &&
-        !__all_sync(~0u, mbar_wait(saddr(&emptyA[(used - 1) % kStagesA]), (uint32_t)((used - 1) / kStagesA) & 1u))) {
+        !__all_sync(~0u, mbar_wait(saddr(&emptyA[(used - 1) % kStagesA]), (uint32_t)((used - 1) / kStagesA) & 1u,
+                                   kSpinLimit, abort_flag))) {
       ok = false;
-      if (lane == 0) atomicExch(&q2_tc_error, 2u);
+      if (lane == 0) {
+        atomicExch(&q2_tc_error, 2u);
+        *abort_flag = 1;
+      }
     }
   }
   ok = __syncthreads_and(ok);
@@ -902,6 +936,13 @@ extern "C" int q2_tc_trellis(const q2_handle* h, const void* x, void* y, int nto
 extern "C" int q2_tc_leech(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
   if (h->hdr.layout == Q2_LEECH_OFFSET4) return q2::launch_tc<Q2_LEECH, true>(h, x, y, ntok, stream);
   return q2::launch_tc<Q2_LEECH, false>(h, x, y, ntok, stream);
+}
+
+// Test hook: the poll limit of the tensor-core kernel's stage waits (0 = the
+// normal bound), on the current device.
+extern "C" int q2_debug_wait_limit(long long polls) {
+  if (polls < 0) return Q2_EINVAL;
+  return cudaMemcpyToSymbol(q2_tc_stage_wait_limit, &polls, sizeof(polls)) == cudaSuccess ? Q2_OK : Q2_ECUDA;
 }
 
 // Device-side error word of the tensor-core kernels since the last call

@@ -276,8 +276,18 @@ int q2_rotate_split(int C, int* nh, int* nq);
 /* Device-side error word of the tensor-core (multi-token) kernels, then
  * cleared: 0 in normal operation; nonzero means a bounded wait on the
  * tensor core ran out and the kernel skipped its work (its outputs are not
- * valid).  Synchronous: reads device memory of the current device. */
+ * valid: NaN where BPDQ's K split is reduced inside the launch, whose
+ * accumulator words are still left at zero).  Before such a kernel's CTA
+ * exits it waits, with the full bound, for its copies and MMAs in flight.
+ * Synchronous: reads device memory of the current device. */
 int q2_device_errors(unsigned int* out);
+
+/* Test hook, not for production use: limits the tensor-core kernel's stage
+ * waits (the helper warp's wait for a slice's decoded weights and x tile) to
+ * `polls` polls on the current device (0 restores the normal bound), so a
+ * test can make them run out and check the error path above without
+ * faulting or hanging the GPU.  Synchronous.  Q2_EINVAL for polls < 0. */
+int q2_debug_wait_limit(long long polls);
 
 const char* q2_strerror(int status);
 
