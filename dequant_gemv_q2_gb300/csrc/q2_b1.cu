@@ -339,12 +339,15 @@ __device__ __forceinline__ void ld_item(const unsigned char* base, int item_byte
   for (int k = 0; k < n; ++k) w[k] = ldg_stream(p + k * 512);
 }
 
-// Launch shape of the generic (run_b1) kernels, Leech and trellis: one
-// 16-warp CTA per SM, one item ahead per warp in registers (measured: 2
-// ahead is slower).
-constexpr int kWarps = 16;
+// Launch shape of the generic (run_b1) kernels, Leech and trellis: one CTA
+// per SM (16 warps for Leech, 24 for the trellis), one item ahead per warp
+// in registers (measured: 2 ahead is slower).
 constexpr int kMinBlocks = 1;
 constexpr int kLeechAhead = 1;
+#ifndef Q2_LEECH_W
+#define Q2_LEECH_W 16
+#endif
+constexpr int kLeechWarps = Q2_LEECH_W;   // warps per CTA of the Leech kernel
 
 // ------------------------------------------------------------------ Leech
 struct LeechArgs {
@@ -1028,7 +1031,14 @@ struct TrellisF {
   }
 };
 
-constexpr int kTrellisAhead = 1;
+#ifndef Q2_TRL_W
+#define Q2_TRL_W 24                   // 16: 13.8 us, 24: 13.2, 32: 13.8 per 12288x4096 GEMV (GB300)
+#endif
+#ifndef Q2_TRL_AHEAD
+#define Q2_TRL_AHEAD 1
+#endif
+constexpr int kTrellisAhead = Q2_TRL_AHEAD;
+constexpr int kTrlWarps = Q2_TRL_W;   // warps per CTA of the trellis kernel
 
 template <int W, int AHEAD, int K>
 __global__ void __launch_bounds__(W * 32, kMinBlocks) k_trellis_b1(TrellisArgs a) {
@@ -1238,8 +1248,8 @@ extern "C" int q2_b1_leech(const q2_handle* h, const void* x, void* y, void* str
   a.tailpad = d.tailpad;
   a.inv_sqrt8 = d.inv_sqrt8;
   if (d.layout == Q2_LEECH_OFFSET4)
-    return launch1(k_leech_b1<kWarps, kLeechAhead, 4>, a, geometry(d), kWarps * 32, kTabSmem, stream);
-  return launch1(k_leech_b1<kWarps, kLeechAhead, 3>, a, geometry(d), kWarps * 32, kTabSmem, stream);
+    return launch1(k_leech_b1<kLeechWarps, kLeechAhead, 4>, a, geometry(d), kLeechWarps * 32, kTabSmem, stream);
+  return launch1(k_leech_b1<kLeechWarps, kLeechAhead, 3>, a, geometry(d), kLeechWarps * 32, kTabSmem, stream);
 }
 
 extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* stream, const q2_pf* pf) {
@@ -1254,12 +1264,12 @@ extern "C" int q2_b1_trellis(const q2_handle* h, const void* x, void* y, void* s
   const int xbytes = (d.C * 2 + 15) / 16 * 16;
   auto fits = [&](int tb) { return tb + xbytes + kTailFixed <= kMaxDynSmem; };
   if (fits(trl_table_bytes<8>()))
-    return launch1(k_trellis_b1<kWarps, kTrellisAhead, 8>, a, geometry(d), kWarps * 32, trl_table_bytes<8>() + xbytes,
+    return launch1(k_trellis_b1<kTrlWarps, kTrellisAhead, 8>, a, geometry(d), kTrlWarps * 32, trl_table_bytes<8>() + xbytes,
                    stream);
   if (fits(trl_table_bytes<4>()))
-    return launch1(k_trellis_b1<kWarps, kTrellisAhead, 4>, a, geometry(d), kWarps * 32, trl_table_bytes<4>() + xbytes,
+    return launch1(k_trellis_b1<kTrlWarps, kTrellisAhead, 4>, a, geometry(d), kTrlWarps * 32, trl_table_bytes<4>() + xbytes,
                    stream);
-  return launch1(k_trellis_b1<kWarps, kTrellisAhead, 1>, a, geometry(d), kWarps * 32, trl_table_bytes<1>() + xbytes,
+  return launch1(k_trellis_b1<kTrlWarps, kTrellisAhead, 1>, a, geometry(d), kTrlWarps * 32, trl_table_bytes<1>() + xbytes,
                  stream);
 }
 
