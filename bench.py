@@ -354,8 +354,8 @@ def sweep14b(q2, stream, formats, ntoks, distinct: int, steps: int, hbm: float) 
                                    workspace=torch.zeros(16, dtype=torch.uint8, device="cuda"))
                 row.append(pk)
             mats.append(row)
-        if fmt not in ("cublas", "fp16"):
-            need = max(p.workspace_bytes(max(ntoks)) for row in mats for p in row)
+        if fmt != "cublas":
+            need = max(1, max(p.workspace_bytes(max(ntoks)) for row in mats for p in row))
             wsbuf = torch.zeros(need, dtype=torch.uint8, device="cuda")
             for row in mats:
                 for p in row:
@@ -756,7 +756,7 @@ def main():
         del lin, g, xbuf, ybuf, wsbuf, xv, yv
         torch.cuda.empty_cache()
         extras["sweep14b"] = sweep14b(q2, stream, ["bpdq", "trellis", "leech", "cublas"], [1, 16, 64], 4, 10, hbm)
-        extras["sweep14b"]["fp16"] = sweep14b(q2, stream, ["fp16"], [1], 4, 10, hbm)["fp16"]
+        extras["sweep14b"]["fp16"] = sweep14b(q2, stream, ["fp16"], [1, 16, 64], 4, 10, hbm)["fp16"]
         extras["fmt"] = per_format(q2, stream, hbm)
         extras["rot"] = rot
 

@@ -1,7 +1,8 @@
 // Dense fp16 control GEMV ("Unfolding the Leech Lattice", section 7: the
-// byte bound is the fp16 control's measured bandwidth).  A warp owns one
-// row at a time; each lane streams 16-byte chunks of the row and accumulates
-// in fp32 with mixed-precision FMAs; a shuffle reduction finishes the row.
+// byte bound is the fp16 control's measured bandwidth), one token.  A warp
+// owns one row at a time; each lane streams 16-byte chunks of the row and
+// accumulates in fp32 with mixed-precision FMAs; a shuffle reduction
+// finishes the row.  More tokens run on the tensor cores (q2_tc.cu).
 #include <cuda_fp16.h>
 
 #include "q2_common.cuh"
@@ -18,7 +19,7 @@ struct DenseArgs {
   const __half* w;
   const __half* x;
   __half* y;
-  int R, C, ntok;
+  int R, C;
 };
 
 __device__ __forceinline__ float dot8(const uint4& w, const uint4& x, float acc) {
@@ -61,39 +62,17 @@ __global__ void __launch_bounds__(kThreads) k_fp16_b1(DenseArgs a) {
   }
 }
 
-template <int NT>
-__global__ void __launch_bounds__(kThreads) k_fp16_mt(DenseArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int nch = a.C / 8;
-  const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5), nw = gridDim.x * kWarps;
-  for (int r = gw; r < a.R; r += nw) {
-    const uint4* wr = reinterpret_cast<const uint4*>(a.w + (size_t)r * a.C);
-    float acc[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-    for (int c = lane; c < nch; c += 32) {
-      const uint4 w = ldg_stream(wr + c);
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-        if (t < a.ntok) acc[t] = dot8(w, __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * a.C) + c), acc[t]);
-    }
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      if (t >= a.ntok) break;
-      float v = acc[t];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) a.y[(size_t)t * a.R + r] = __float2half_rn(v);
-    }
-  }
-}
-
 }  // namespace
 }  // namespace q2
 
 using namespace q2;
 
+extern "C" int q2_tc_fp16(const q2_handle* h, const void* x, void* y, int ntok, void* stream);
+
+// One token on CUDA cores; 2..64 through the tensor-core kernel (q2_tc.cu),
+// whose weight stage is a plain row load for this format.
 extern "C" int q2_launch_fp16(const q2_handle* h, const void* x, void* y, int ntok, void* stream, const q2_pf*) {
+  if (ntok > 1) return q2_tc_fp16(h, x, y, ntok, stream);
   const q2_blob_header& d = h->hdr;
   DenseArgs a;
   a.w = reinterpret_cast<const __half*>(h->dev + d.off[SEC_FP16_W]);
@@ -101,20 +80,11 @@ extern "C" int q2_launch_fp16(const q2_handle* h, const void* x, void* y, int nt
   a.y = static_cast<__half*>(y);
   a.R = d.R;
   a.C = d.C;
-  a.ntok = ntok;
   const DevInfo di = dev_info();
   const int grid = max(1, min((d.R + kWarps - 1) / kWarps, 8 * di.sms));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (ntok == 1) {
-    const int smem = d.C * 2;
-    if (set_smem(reinterpret_cast<const void*>(k_fp16_b1), smem)) return Q2_ECUDA;
-    k_fp16_b1<<<grid, kThreads, smem, st>>>(a);
-  } else if (ntok <= 4) {
-    k_fp16_mt<4><<<grid, kThreads, 0, st>>>(a);
-  } else if (ntok <= 16) {
-    k_fp16_mt<16><<<grid, kThreads, 0, st>>>(a);
-  } else {
-    k_fp16_mt<64><<<grid, kThreads, 0, st>>>(a);
-  }
+  const int smem = d.C * 2;
+  if (set_smem(reinterpret_cast<const void*>(k_fp16_b1), smem)) return Q2_ECUDA;
+  k_fp16_b1<<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? Q2_OK : Q2_ECUDA;
 }

@@ -409,11 +409,11 @@ extern "C" size_t q2_tc_workspace_bytes(const q2_handle* h, int ntok);   // q2_t
 int q2_workspace_bytes(const q2_handle* h, int ntok, size_t* bytes) {
   if (!h || !bytes) return Q2_EINVAL;
   if (ntok < 1 || ntok > Q2_MAX_NTOK) return Q2_ENTOK;
-  if (h->hdr.fmt == Q2_FP16) {
-    *bytes = 0;
+  const int fmt = h->hdr.fmt;
+  if (fmt == Q2_FP16) {                                        // one token: none; more: the tensor-core plan
+    *bytes = ntok == 1 ? 0 : q2_tc_workspace_bytes(h, ntok);
     return Q2_OK;
   }
-  const int fmt = h->hdr.fmt;
   const bool cuda_core = ntok == 1 || (fmt == Q2_BPDQ && ntok <= Q2_MAX_ACC_TOK) ||
                          (fmt == Q2_LEECH && ntok == 2 && h->hdr.C % 8 == 0 && h->hdr.R % 8 == 0);
   if (cuda_core)

@@ -1,6 +1,7 @@
 // Skinny-GEMM path on the 5th-generation tensor cores (tcgen05) for
 // 2..64 tokens (padded to N = 16, 32, 48 or 64): decode once per tile,
-// multiply for every token.
+// multiply for every token.  The dense fp16 control runs through the same
+// kernel with plain row loads in place of a decode.
 //
 // A CTA owns 128 output rows (four 32-row blocks) and a range of 256-column
 // slices, and runs them through rings of stages with three roles:
@@ -79,6 +80,7 @@ constexpr int kParts = kDecWarps / 4;         // warps per 32-row block, each de
 constexpr int kPartBytes = 32 / kParts;       // column-bytes of one plane per lane and part
 constexpr int kPartWords = kPartBytes / 4;    // canonical 32-bit words of one plane per lane and part
 constexpr int kRows = 128;                    // M of the MMA
+constexpr int kPf16Ahead = 3;                 // fp16 control: slices of rows fetched into L2 ahead
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAcol0 = 64;               // D takes TMEM columns 0..63
 constexpr int kOneCtaSmem = 116 * 1024;       // two CTAs never share an SM (each holds all of TMEM)
@@ -214,6 +216,7 @@ struct TcArgs {
   const unsigned char* bits;   // item stream (BPDQ bits, trellis symbols, Leech planes)
   const uint2* vtab;           // BPDQ: [G][Rpad] 4 halves
   const uint32_t* table;       // trellis: 4096 half2
+  const __half* w16;           // fp16 control: [R][C]
   const uint16_t* parity;      // Leech: [S][Rpad]
   const __half* x;             // [ntok][C]
   __half* y;                   // [ntok][R]  (nsplit == 1, BPDQ only)
@@ -236,13 +239,14 @@ constexpr uint32_t kHashHi = 0x9E37u << 16;     // trellis: (s*0x9E37 mod 2^16) 
 // OFF4: the Leech offset-binary layout (four planes).
 template <int FMT, bool OFF4 = false>
 struct TcShape {
-  static constexpr int kch = FMT == Q2_LEECH ? 36 : 32;
+  static constexpr int kch = FMT == Q2_LEECH ? 36 : 32;   // fp16 control: 32, like BPDQ and trellis
   static constexpr int kmma = kch / 2;                  // K = 16 steps per slice
   static constexpr int atoms = (kch + 7) / 8;           // 64-column swizzle atoms of B
   static constexpr uint32_t acols = kch * 4;            // TMEM columns of one A stage
-  static constexpr int table = FMT == Q2_TRELLIS ? 4096 * 4 : 0;
+  // trellis: the codebook; fp16 control: each decoder warp's 4 KB transpose tile
+  static constexpr int table = FMT == Q2_TRELLIS ? 4096 * 4 : FMT == Q2_FP16 ? kDecWarps * 4096 : 0;
   static constexpr int item = FMT == Q2_BPDQ ? Q2_ITEM_BYTES_BPDQ : FMT == Q2_TRELLIS ? Q2_ITEM_BYTES_TRL
-                              : OFF4 ? Q2_ITEM_BYTES_LEECH4 : Q2_ITEM_BYTES_LEECH;
+                              : FMT == Q2_FP16 ? 0 : OFF4 ? Q2_ITEM_BYTES_LEECH4 : Q2_ITEM_BYTES_LEECH;
   static constexpr int planes = FMT == Q2_BPDQ ? 2 : FMT == Q2_LEECH ? (OFF4 ? 4 : 3) : 0;
 };
 static_assert(kAcol0 + kStagesA * TcShape<Q2_LEECH>::acols <= kTmemCols, "A stages exceed TMEM");
@@ -415,8 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
   const int tile_rbs = min(4, a.nrb - tile * 4);
 
   if (threadIdx.x == 0) {
-    for (int s = sA; s < sB; ++s)
-      prefetch_l2(a.bits + ((size_t)s * a.nrb + tile * 4) * Sh::item, (size_t)tile_rbs * Sh::item);
+    if (Sh::item)        // the packed formats: the CTA's whole range (a few KB per slice)
+      for (int s = sA; s < sB; ++s)
+        prefetch_l2(a.bits + ((size_t)s * a.nrb + tile * 4) * Sh::item, (size_t)tile_rbs * Sh::item);
     for (int st = 0; st < kStagesA; ++st) {
       mbar_init(saddr(&fullA[st]), kDecWarps);
       mbar_init(saddr(&emptyA[st]), 1);
@@ -449,7 +454,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
   // 64-byte symbol packet), at per-lane offsets fixed for the whole kernel;
   // plus BPDQ's value table / Leech's parity word.
   constexpr int NPL = Sh::planes;
-  constexpr int NW = FMT == Q2_TRELLIS ? 5 : NPL * (kPartWords + 1);
+  // (fp16 control: nothing is held ahead; the rows are read when the slice is stored)
+  constexpr int NW = FMT == Q2_TRELLIS ? 5 : FMT == Q2_FP16 ? 1 : NPL * (kPartWords + 1);
   int off[NW];
   {
     const int aa = lane >> 2;
@@ -470,7 +476,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
   uint32_t pl[NW], n1[NW];
   uint2 vt = make_uint2(0, 0), v1 = make_uint2(0, 0);
   uint32_t par = 0, p1 = 0;
+  // fp16 control: the warp's 32 rows x the part's 64 columns of slice s,
+  // read as whole 128-byte row segments (load k: rows 4k .. 4k + 3 of the
+  // block, lane l the 16-byte chunk l % 8 of row 4k + l / 8; zeros past R
+  // and C, C being a multiple of 8), one slice held ahead of the one being
+  // stored.  A load touching 32 rows (one per lane) keeps 32 lines in flight
+  // per instruction and was measured at 0.4 of HBM; these keep 4.
+  uint4 fcur[FMT == Q2_FP16 ? 8 : 1], fnext[FMT == Q2_FP16 ? 8 : 1];
+  auto load16 = [&](int s, uint4* w) {
+    const int c = s * 256 + part * 64 + (lane & 7) * 8;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int r = rb * 32 + 4 * k + (lane >> 3);
+      w[k] = (valid && r < a.R && c < a.C) ? ldg_stream(a.w16 + (size_t)r * a.C + c) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  // ... and the rows' 512-byte segments of slice s fetched into L2 ahead of
+  // the register loads (by the part-0 warps, one lane per row), kPf16Ahead
+  // slices ahead of the slice being stored, so the register loads hit L2
+  auto prefetch16 = [&](int s) {
+    if (part == 0 && valid && row < a.R && s * 256 < a.C)
+      prefetch_l2(a.w16 + (size_t)row * a.C + (size_t)s * 256, (size_t)min(256, a.C - s * 256) * 2);
+  };
+  if constexpr (FMT == Q2_FP16) {
+    for (int j = 1; j <= kPf16Ahead && j < used; ++j) prefetch16(sA + j);
+    if (used > 0) load16(sA, fcur);
+  }
   auto load = [&](int s, uint32_t (&d)[NW], uint2& v, uint32_t& pw) {
+    if (FMT == Q2_FP16) return;
     const unsigned char* ip = a.bits + ((size_t)s * a.nrb + rb) * Sh::item + lane * 16;
 #pragma unroll
     for (int t = 0; t < NW; ++t) d[t] = __ldg(reinterpret_cast<const uint32_t*>(ip + off[t]));
@@ -612,6 +645,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
 #pragma unroll
       for (int t = 0; t < NW; ++t) n2[t] = 0;
       if (valid && i + 2 < used) load(s + 2, n2, v2, p2);
+      if constexpr (FMT == Q2_FP16) {
+        if (i + 1 + kPf16Ahead < used) prefetch16(s + 1 + kPf16Ahead);
+        if (i + 1 < used) load16(s + 1, fnext);
+      }
       // the stage is free once the MMAs of slice i - kStagesA have completed
       if (i >= kStagesA &&
           !__all_sync(~0u, mbar_wait(saddr(&emptyA[sa]), (uint32_t)(i / kStagesA - 1) & 1u, kSpinLimit, abort_flag))) {
@@ -624,7 +661,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
       }
       tc_fence_after();
       const uint32_t ta = tlane + kAcol0 + (uint32_t)sa * Sh::acols + (uint32_t)(32 * part);
-      if (FMT == Q2_TRELLIS) {
+      if (FMT == Q2_FP16) {
+        // transpose through the warp's shared-memory tile (row r at 128 r,
+        // chunk c at 16 (c ^ r % 8): conflict-free both ways) so that lane r
+        // holds row r's 64 columns, then store them as they are
+        unsigned char* tt = q2_smem + warp * 4096;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int r = 4 * k + (lane >> 3), c = lane & 7;
+          *reinterpret_cast<uint4*>(tt + r * 128 + ((c ^ (r & 7)) << 4)) = fcur[k];
+        }
+        __syncwarp();
+        uint4 w[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) w[c] = *reinterpret_cast<const uint4*>(tt + lane * 128 + ((c ^ (lane & 7)) << 4));
+        __syncwarp();
+        tmem_st16(ta, w[0], w[1], w[2], w[3]);
+        tmem_st16(ta + 16u, w[4], w[5], w[6], w[7]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) fcur[k] = fnext[k];
+      } else if (FMT == Q2_TRELLIS) {
         const uint32_t Lw[5] = {pl[0], pl[1], pl[2], pl[3], pl[4]};
         trellis_part(Lw, tab, ta);
       } else if (FMT == Q2_BPDQ) {
@@ -787,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
       for (int i = 0; i < 16; ++i) {
         const int t = c0 + i;
         if (t < a.ntok) {
-          if (a.nsplit == 1 && FMT == Q2_BPDQ) {
+          if (a.nsplit == 1 && (FMT == Q2_BPDQ || FMT == Q2_FP16)) {
             if (orow < a.R) a.y[(size_t)t * a.R + orow] = __float2half_rn(v[i]);
           } else if (orow < a.Rpad) {
             a.partial[((size_t)t * a.nsplit + split) * a.Rpad + orow] = v[i];
@@ -846,9 +902,13 @@ bool encode_x_map(CUtensorMap* map, const void* x, int C, int ntok, int N) {
 // partials for the reduce kernel.
 constexpr int kSplitOverhead = 4;
 
+// 256-column slices of the tensor-core launch (the fp16 control's last one
+// may be partial)
+int tc_slices(const q2_blob_header& d) { return d.fmt == Q2_FP16 ? (d.C + Q2_SLICE - 1) / Q2_SLICE : d.nslice; }
+
 void tc_plan(const q2_blob_header& d, int ntok, int* nsplit, int* fused) {
   const int sms = dev_info().sms;
-  const int ntile = (d.Rpad + kRows - 1) / kRows, S = d.nslice;
+  const int ntile = (d.Rpad + kRows - 1) / kRows, S = tc_slices(d);
   long best = -1;
   for (int ns = 1; ns <= S; ++ns) {
     const long ctas = (long)ntile * ns;
@@ -872,7 +932,9 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
   using Sh = TcShape<FMT, OFF4>;
   const q2_blob_header& d = h->hdr;
   TcArgs a = {};
-  if (FMT == Q2_BPDQ) {
+  if (FMT == Q2_FP16) {
+    a.w16 = reinterpret_cast<const __half*>(h->dev + d.off[SEC_FP16_W]);
+  } else if (FMT == Q2_BPDQ) {
     a.bits = h->dev + d.off[SEC_BPDQ_BITS];
     a.vtab = reinterpret_cast<const uint2*>(h->dev + d.off[SEC_BPDQ_VTAB]);
   } else if (FMT == Q2_TRELLIS) {
@@ -890,7 +952,7 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
   a.C = d.C;
   a.Rpad = d.Rpad;
   a.nrb = q2_nrb(d);
-  a.S = d.nslice;
+  a.S = tc_slices(d);
   a.ntok = ntok;
   a.N = (ntok + 15) / 16 * 16;
   a.ntile = (d.Rpad + kRows - 1) / kRows;
@@ -908,7 +970,8 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
   const int smem = max(kOneCtaSmem, Sh::table + 1024 + kStagesB * Sh::atoms * a.N * 128 + (2 * kStagesA + kStagesB + 2) * 8 + 16);
   int st = launch_pdl(k_tc<FMT, OFF4>, a, a.ntile * a.nsplit, kThreads, smem, stream);
   if (st) return st;
-  if (FMT == Q2_BPDQ && (a.nsplit == 1 || a.fused)) return Q2_OK;
+  if ((FMT == Q2_BPDQ || FMT == Q2_FP16) && a.nsplit == 1) return Q2_OK;
+  if (FMT == Q2_BPDQ && a.fused) return Q2_OK;
   return q2_launch_reduce_n(h, x, y, ntok, a.nsplit, stream);
 }
 
@@ -922,11 +985,14 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
 extern "C" size_t q2_tc_workspace_bytes(const q2_handle* h, int ntok) {
   int nsplit = 1, fused = 0;
   q2::tc_plan(h->hdr, ntok, &nsplit, &fused);
-  if (h->hdr.fmt == Q2_BPDQ && nsplit == 1) return 0;
+  if ((h->hdr.fmt == Q2_BPDQ || h->hdr.fmt == Q2_FP16) && nsplit == 1) return 0;
   if (fused) return (size_t)ntok * h->hdr.Rpad * 8;
   return Q2_WS_PARTIAL_OFFSET + (size_t)nsplit * ntok * h->hdr.Rpad * 4;
 }
 
+extern "C" int q2_tc_fp16(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
+  return q2::launch_tc<Q2_FP16>(h, x, y, ntok, stream);
+}
 extern "C" int q2_tc_bpdq(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
   return q2::launch_tc<Q2_BPDQ>(h, x, y, ntok, stream);
 }

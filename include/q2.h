@@ -162,7 +162,10 @@ int q2_bytes(const q2_handle* h, int ntok, size_t* weight_bytes_read_per_call);
  * y = W x ("Unfolding the Leech Lattice", introduction).  x: device fp16
  * [ntok][C]; y: device fp16 [ntok][R]; both 16-byte aligned; 1 <= ntok <= 64.
  * Asynchronous and ordered on `stream`; never synchronises.  Needs the
- * workspace of q2_workspace_bytes(h, ntok) bound first (0 bytes for fp16).
+ * workspace of q2_workspace_bytes(h, ntok) bound first (0 bytes for fp16 at
+ * one token).  The dense fp16 control runs one token on CUDA cores and
+ * 2..64 tokens through the tensor-core kernel, loading its rows as they are
+ * (fp32 partials and the reduction launch when it splits K).
  * The packed formats at 1 token, and BPDQ at 2..6 tokens, run on CUDA cores
  * in launches that reduce their split-K partial sums themselves, through the
  * workspace's fixed-point accumulator words (integer sums: the result does

@@ -225,12 +225,41 @@ def test_leech_decode_bit_exact(q2, layout):
 
 
 # ---------------------------------------------------------------- fp16
-@pytest.mark.parametrize("ntok", [1, 3, 16, 64])
-def test_fp16_parity(q2, ntok):
-    d = synth.fp16_dense(300, 1032, 4000)
-    x = synth.activations(ntok, 1032, 4000)
+# One token on CUDA cores, 2..64 through the tensor-core kernel with plain
+# row loads: ragged rows (R % 128 != 0), a partial last 256-column slice
+# (C % 256 != 0), a single short row, and a K split reduced by the second
+# launch (17408 columns).
+@pytest.mark.parametrize("R,C", [(300, 1032), (1, 8), (129, 4104)])
+@pytest.mark.parametrize("ntok", [1, 2, 3, 7, 16, 33, 64])
+def test_fp16_parity(q2, R, C, ntok):
+    d = synth.fp16_dense(R, C, 4000 + R)
+    x = synth.activations(ntok, C, 4000)
     _, y = _run(q2, q2.q2_pack_fp16(d["w"]), x)
     _check(y, ofp16.decode_f64(d["w"]), x)
+
+
+@pytest.mark.parametrize("ntok", [2, 16, 64])
+def test_fp16_tensor_path_full_size(q2, ntok):
+    R, C = 5120, 17408
+    d = synth.fp16_dense(R, C, 4100)
+    x = synth.activations(ntok, C, 4101)
+    _, y = _run(q2, q2.q2_pack_fp16(d["w"]), x)
+    rows = _sampled_rows(R, seed=4102)
+    _check(y, ofp16.decode_f64(d["w"][rows]), x, rows)
+    assert q2.device_errors() == 0
+
+
+def test_fp16_tensor_path_one_hot_bit_exact(q2):
+    # x = e_c per token selects one weight per row: y[t][r] = w[r][c_t]
+    # exactly (one fp32 product by 1.0, rounded back to fp16), which pins the
+    # order in which the rows reach tensor memory column by column
+    R, C = 200, 776
+    d = synth.fp16_dense(R, C, 4200)
+    cols = np.array([0, 1, 7, 8, 63, 64, 255, 256, 511, 512, 700, 767, 768, 775] + list(range(100, 150)))   # 64 tokens
+    x = np.zeros((len(cols), C), dtype=np.float16)
+    x[np.arange(len(cols)), cols] = 1.0
+    _, y = _run(q2, q2.q2_pack_fp16(d["w"]), x)
+    assert np.array_equal(y.view(np.uint16), d["w"][:, cols].T.view(np.uint16))
 
 
 def test_noweights_control_runs(q2):
