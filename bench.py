@@ -355,7 +355,8 @@ def sweep14b(q2, stream, formats, ntoks, distinct: int, steps: int, hbm: float) 
                 row.append(pk)
             mats.append(row)
         if fmt != "cublas":
-            need = max(1, max(p.workspace_bytes(max(ntoks)) for row in mats for p in row))
+            # the workspace a handle needs is not monotone in ntok: the largest over the counts timed
+            need = max(1, max(p.workspace_bytes(nt) for row in mats for p in row for nt in ntoks))
             wsbuf = torch.zeros(need, dtype=torch.uint8, device="cuda")
             for row in mats:
                 for p in row:
