@@ -152,17 +152,7 @@ __device__ __forceinline__ void build_table(const __half* __restrict__ xg, int n
   }
 }
 
-// ---------------------------------------------------- split-K reduction
-// Each (slice, 32-row block) item writes fp32 partials for its rows with
-// plain stores.  A second kernel (q2_reduce.cu), chained by programmatic
-// dependent launch, sums the partials of every output in slice order, so the
-// result does not depend on scheduling.
-struct Reduce {
-  float* partial;      // [ntok][nslice][Rpad]
-  int nslice;
-  int Rpad;
-};
-
+// ------------------------------------------- programmatic dependent launch
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

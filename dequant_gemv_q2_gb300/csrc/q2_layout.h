@@ -15,13 +15,10 @@
 
 // Workspace layout.  The CUDA-core paths (1..6 tokens) keep one 64-bit
 // accumulator per (token, row) at offset 0: [ntok][Rpad] words, zero between
-// calls (see q2_b1.cu).  The tensor-core path keeps fp32 partial sums
-// [ntok][nsplit][Rpad] at offset Q2_WS_PARTIAL_OFFSET, which lies past the
-// largest accumulator region any handle can have, so one workspace can
-// serve every handle without a partial sum ever landing on an accumulator.
+// calls (see q2_b1.cu).  The tensor-core path (2..64 tokens) needs none: it
+// sums its K splits in distributed shared memory.
 #define Q2_MAX_ROWS 524288
 #define Q2_MAX_ACC_TOK 6
-#define Q2_WS_PARTIAL_OFFSET ((size_t)Q2_MAX_ACC_TOK * Q2_MAX_ROWS * 8)
 #define Q2_MAX_SPLIT 255          // count field of the accumulator word
 
 // Section indices per format.

@@ -21,12 +21,14 @@
 // access: any memory access by the issuing thread waits for its queue of
 // MMAs to drain and leaves the tensor core idle (about 350 cycles per
 // access on GB300), so the MMA lane touches no memory at all.
-// At the end decoder warps 0..3 (one per TMEM lane quarter) read the
-// accumulator, each its 32 lanes = 32 rows, and write y directly (one K
-// split), add it as fixed-point terms to the rows' accumulator words (BPDQ
-// with a K split; the completing add writes y), or write fp32 partial sums
-// for the split-K reduction kernel (trellis and Leech, whose epilogue needs
-// the row scale, tail and exceptions).
+// At the end the decoder warps copy the accumulator (fp32, 128 rows x N)
+// into shared memory.  A tile split over K runs as one thread-block cluster
+// of its nsplit CTAs: each sums a share of the tile's rows over the
+// cluster's partials through distributed shared memory, in split order, so
+// the result does not depend on which CTA finished first; no global
+// atomics, no workspace and no second launch.  The same pass applies the
+// format's row epilogue (trellis: x scale; Leech: exceptions, scale, tail)
+// and writes y.
 //
 // TMEM columns (all 512 are allocated; one CTA per SM): D at 0 .. N - 1,
 // A of stage st at kAcol0 + st * (4 x K chunks); A column j of a lane holds
@@ -51,13 +53,14 @@
 #include <cuda.h>
 #include <cmath>
 #include <algorithm>
+#include <mutex>
+#include <vector>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include "q2_common.cuh"
 
 extern __shared__ __align__(1024) unsigned char q2_smem[];
-extern "C" int q2_launch_reduce_n(const q2_handle* h, const void* x, void* y, int ntok, int nsplit, void* stream);
 
 __device__ unsigned int q2_tc_error = 0;
 // Poll limit of the helper warp's stage waits (decoded A and x tile of a
@@ -80,6 +83,7 @@ constexpr int kParts = kDecWarps / 4;         // warps per 32-row block, each de
 constexpr int kPartBytes = 32 / kParts;       // column-bytes of one plane per lane and part
 constexpr int kPartWords = kPartBytes / 4;    // canonical 32-bit words of one plane per lane and part
 constexpr int kRows = 128;                    // M of the MMA
+constexpr int kMaxSplit = 8;                  // K splits of a tile at most: the portable cluster size
 constexpr int kPf16Ahead = 3;                 // fp16 control: slices of rows fetched into L2 ahead
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAcol0 = 64;               // D takes TMEM columns 0..63
@@ -219,17 +223,45 @@ struct TcArgs {
   const __half* w16;           // fp16 control: [R][C]
   const uint16_t* parity;      // Leech: [S][Rpad]
   const __half* x;             // [ntok][C]
-  __half* y;                   // [ntok][R]  (nsplit == 1, BPDQ only)
-  float* partial;              // [ntok][nsplit][Rpad]
+  __half* y;                   // [ntok][R]
   int R, C, Rpad, nrb, S, ntok, N, nsplit, ntile, nblock;
   int use_tma;                 // 0: x rows not 16-byte aligned, staged with element loads
-  // BPDQ with a K split: the splits' partials are added inside the launch as
-  // fixed-point terms to accumulator words [ntok][Rpad] (the batch-1 scheme:
-  // the add that completes the count writes y and zeroes the word)
-  int fused;
-  unsigned long long* acc;
-  float fscale, finv;
+  // Per-row finish after the K sum (the reduction kernel's epilogue before):
+  // trellis x scale_r; Leech + 16 x[col] for each v = +8 exception, x scale_r
+  // * post (1/sqrt(8)), + the fp16 tail dot product ("Tetra", section 5.1:
+  // the row scale after the block dot product, then the unquantised tail)
+  const __half* scale;         // [R] or null
+  float post;
+  const __half* tail;          // Leech [Rpad][tailpad]
+  int tail_n, tailpad, tail_col0;
+  const uint32_t* excptr;      // Leech [Rpad + 1] (empty lists for the offset-binary layout)
+  const uint32_t* exccol;
 };
+
+// Distributed shared memory: this CTA's shared address in CTA `rank` of the
+// cluster, and a 16-byte load from it (ordered against writes by the
+// cluster barriers around the reads).
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t saddr_local, uint32_t rank) {
+  uint32_t remote;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr_local), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote));
+  return v;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t saddr_local, uint32_t rank) {
+  uint32_t remote;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr_local), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
+  return v;
+}
+// Every thread of every CTA of the cluster: writes before it are visible to
+// reads after it, cluster-wide.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 constexpr uint32_t kHashHi = 0x9E37u << 16;     // trellis: (s*0x9E37 mod 2^16) in bits 16..31
 
@@ -410,7 +442,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool decoder = warp < kDecWarps;
   const int rbl = warp & 3, part = (warp >> 2) & (kParts - 1);   // row block in tile (= TMEM lane quarter), part of the slice
-  const int tile = blockIdx.x % a.ntile, split = blockIdx.x / a.ntile;
+  // the K splits of a tile are consecutive CTAs, one thread-block cluster
+  // (split = the CTA's rank in it)
+  const int tile = blockIdx.x / a.nsplit, split = blockIdx.x % a.nsplit;
   const int sA = split * a.S / a.nsplit, sB = (split + 1) * a.S / a.nsplit;
   const int used = sB - sA;
   const int rb = tile * 4 + rbl;
@@ -788,70 +822,113 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
   }
   ok = __syncthreads_and(ok);
   tc_fence_after();
-  if (FMT == Q2_BPDQ && a.fused && !ok && warp < 4 && used > 0) {
-    // A bounded wait ran out: the accumulator is not valid, but the other
-    // splits have added (or will add) their terms to these rows' words.
-    // Add a poison term for every token so the counts still complete: the
-    // completing lane writes NaN and resets the word, so the workspace is
-    // left at zero for the next call, as after a normal one.
-    const int orow = (tile * 4 + warp) * 32 + lane;
-    if (orow < a.Rpad)
-      for (int t = 0; t < a.ntok; ++t) {
-        unsigned long long* word = a.acc + (size_t)t * a.Rpad + orow;
-        atomicOr(word, kNonFinite);
-        const unsigned long long w = atomicAdd(word, kCountOne) + kCountOne;
-        if ((int)(w >> 56) == a.nsplit) {
-          if (orow < a.R) a.y[(size_t)t * a.R + orow] = __ushort_as_half((unsigned short)0x7E00u);
-          a.acc[(size_t)t * a.Rpad + orow] = 0ull;
-        }
-      }
-  }
-  // Epilogue over all decoder warps: warp w reads TMEM lane quarter w % 4 (the
-  // lanes a warp may access) and token columns 16 (w / 4) + 64 j, so at 64
-  // tokens 16 warps each take one 16-token group instead of 4 warps taking
-  // four groups one after another (the fused reduction's atomics of one group
-  // are in flight while the others are issued).
-  if (decoder && ok && used > 0) {
-    const int orow = (tile * 4 + rbl) * 32 + lane;
+  // ---- epilogue.  (1) The accumulator, or NaN where a bounded wait ran out,
+  // into this CTA's partial P [token][128 rows] fp32, over the B stages (all
+  // MMAs have completed): warp w reads TMEM lane quarter w % 4 (the lanes a
+  // warp may access) and token columns 16 (w / 4) + 64 j.
+  float* P = reinterpret_cast<float*>(B0);
+  if (decoder)
     for (int c0 = 16 * (warp >> 2); c0 < a.N; c0 += 16 * (kDecWarps / 4)) {
       float v[16];
-      tmem_ld16(tlane + (uint32_t)c0, v);
-      if (FMT == Q2_BPDQ && a.fused) {
-        // 16 tokens' atomics in flight, then the completion checks
-        if (orow < a.Rpad) {
-          unsigned long long add[16], old[16];
+      if (ok && used > 0) {
+        tmem_ld16(tlane + (uint32_t)c0, v);
+      } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (c0 + i < a.ntok) {
-              unsigned long long* word = a.acc + (size_t)(c0 + i) * a.Rpad + orow;
-              add[i] = fx_prepare(word, v[i], a.fscale);
-              old[i] = atomicAdd(word, add[i]);
-            }
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (c0 + i < a.ntok) {
-              const unsigned long long w = old[i] + add[i];
-              if ((int)(w >> 56) == a.nsplit) {
-                if (orow < a.R) a.y[(size_t)(c0 + i) * a.R + orow] = __float2half_rn(fx_value(w, a.nsplit, a.finv));
-                a.acc[(size_t)(c0 + i) * a.Rpad + orow] = 0ull;
-              }
-            }
-        }
-        continue;
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(0x7FC00000u);
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int t = c0 + i;
-        if (t < a.ntok) {
-          if (a.nsplit == 1 && (FMT == Q2_BPDQ || FMT == Q2_FP16)) {
-            if (orow < a.R) a.y[(size_t)t * a.R + orow] = __float2half_rn(v[i]);
-          } else if (orow < a.Rpad) {
-            a.partial[((size_t)t * a.nsplit + split) * a.Rpad + orow] = v[i];
+      for (int i = 0; i < 16; ++i) P[(c0 + i) * kRows + rbl * 32 + lane] = v[i];
+    }
+  __syncthreads();
+  // (2) With a K split, the tile's CTAs form a cluster: after a cluster
+  // barrier CTA `split` sums its share of the rows over the cluster's
+  // partials through distributed shared memory, in split order (the result
+  // does not depend on which CTA finished first), finishes and writes y; a
+  // second barrier keeps every partial readable until all shares are done.
+  // Without a split the CTA finishes all 128 rows from its own partial.
+  const int CS = a.nsplit;
+  if (CS > 1) cluster_sync();
+  if constexpr (FMT == Q2_LEECH) {
+    // Leech: one row per element (its finish, exceptions and the tail dot
+    // product, is a chain of loads per row); CTA `split` takes rows
+    // [split * 128 / CS, (split + 1) * 128 / CS)
+    const int r0 = split * kRows / CS, nr = (split + 1) * kRows / CS - r0;
+    const uint32_t pbase = saddr(P);
+    for (int e = threadIdx.x; e < nr * a.ntok; e += kThreads) {
+      const int t = e / nr, rl = r0 + (e - t * nr);
+      const int row = tile * kRows + rl;
+      if (row >= a.R) continue;
+      float v;
+      if (CS == 1) {
+        v = P[t * kRows + rl];
+      } else {
+        // every partial's load in flight, then the sum in split order
+        float pv[kMaxSplit];
+        const uint32_t off = pbase + (uint32_t)(t * kRows + rl) * 4u;
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q)
+          if (q < CS) pv[q] = ld_cluster_f32(off, (uint32_t)q);
+        v = pv[0];
+#pragma unroll
+        for (int q = 1; q < kMaxSplit; ++q)
+          if (q < CS) v += pv[q];
+      }
+      const __half* xt = a.x + (size_t)t * a.C;
+      for (uint32_t k = a.excptr[row]; k < a.excptr[row + 1]; ++k) v = fmaf(16.f, __half2float(xt[a.exccol[k]]), v);
+      v *= __half2float(a.scale[row]) * a.post;
+      for (int c = 0; c < a.tail_n; ++c)
+        v = fmaf(__half2float(a.tail[(size_t)row * a.tailpad + c]), __half2float(xt[a.tail_col0 + c]), v);
+      a.y[(size_t)t * a.R + row] = __float2half_rn(v);
+    }
+  } else {
+    // rows in groups of 4 (one float4 of every partial per token); CTA
+    // `split` takes groups [split * 32 / CS, (split + 1) * 32 / CS)
+    const int g0 = split * (kRows / 4) / CS, ng = (split + 1) * (kRows / 4) / CS - g0;
+    const uint32_t pbase = saddr(P);
+    for (int e = threadIdx.x; e < ng * a.ntok; e += kThreads) {
+      const int t = e / ng, rl = 4 * (g0 + (e - t * ng));
+      const int row0 = tile * kRows + rl;
+      if (row0 >= a.R) continue;
+      float4 v;
+      if (CS == 1) {
+        v = *reinterpret_cast<const float4*>(P + t * kRows + rl);
+      } else {
+        float4 pv[kMaxSplit];
+        const uint32_t off = pbase + (uint32_t)(t * kRows + rl) * 4u;
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q)
+          if (q < CS) pv[q] = ld_cluster_f32x4(off, (uint32_t)q);
+        v = pv[0];
+#pragma unroll
+        for (int q = 1; q < kMaxSplit; ++q)
+          if (q < CS) {
+            v.x += pv[q].x;
+            v.y += pv[q].y;
+            v.z += pv[q].z;
+            v.w += pv[q].w;
           }
-        }
+      }
+      float f[4] = {v.x, v.y, v.z, v.w};
+      if (FMT == Q2_TRELLIS) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (row0 + j < a.R) f[j] *= __half2float(a.scale[row0 + j]);
+      }
+      __half* yp = a.y + (size_t)t * a.R + row0;
+      if ((a.R & 3) == 0) {                      // 8-byte aligned, all four rows inside R
+        const __half2 lo = __floats2half2_rn(f[0], f[1]), hi = __floats2half2_rn(f[2], f[3]);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&lo);
+        u.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(yp) = u;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (row0 + j < a.R) yp[j] = __float2half_rn(f[j]);
       }
     }
   }
+  if (CS > 1) cluster_sync();
   tc_fence_before();
   __syncthreads();
   if (warp == 0)
@@ -890,48 +967,88 @@ bool encode_x_map(CUtensorMap* map, const void* x, int C, int ntok, int N) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The K split of the tensor-core launch and whether BPDQ reduces it inside
-// the launch.  One CTA per SM at a time, so the makespan is (waves of CTAs)
-// x (slices per CTA + the CTA's fixed cost in slice times): about 1 us of
-// prologue, 2 us until the first group of two slices is decoded and handed
-// to the MMA warp, and 1.5 us of drain and epilogue, against about 1 us per
-// slice (globaltimer traces on GB300), so kSplitOverhead = 4.  BPDQ with
-// a K split reduces inside the launch when its accumulator words fit the
-// workspace's reserve (the scale 2^F keeps a split's partial, at most its
-// slices times the per-slice bound, below 2^45); everything else keeps fp32
-// partials for the reduce kernel.
+// The K split of the tensor-core launch.  One CTA per SM at a time, so the
+// makespan is (waves of tiles) x (slices per CTA + the CTA's fixed cost in
+// slice times): about 1 us from the previous kernel's end to the wait
+// release, 2 us until the first pair of slices is decoded and handed to the
+// MMA warp, and about 1 us of drain and epilogue, against about 1 us per
+// slice (globaltimer traces on GB300), so kSplitOverhead = 4.  A split tile's
+// CTAs run as one cluster, so a wave holds as many tiles as clusters of that
+// size fit on the device at once (cudaOccupancyMaxActiveClusters: clusters
+// live inside one GPC).  At most kMaxSplit = 8 splits, the portable cluster
+// size.
 constexpr int kSplitOverhead = 4;
 
 // 256-column slices of the tensor-core launch (the fp16 control's last one
 // may be partial)
 int tc_slices(const q2_blob_header& d) { return d.fmt == Q2_FP16 ? (d.C + Q2_SLICE - 1) / Q2_SLICE : d.nslice; }
 
-void tc_plan(const q2_blob_header& d, int ntok, int* nsplit, int* fused) {
-  const int sms = dev_info().sms;
+std::mutex g_cl_mu;
+struct ClusterFit {
+  int dev;
+  const void* fn;
+  int smem, cs, n;
+};
+std::vector<ClusterFit> g_cl;
+
+// Clusters of `cs` CTAs of `fn` (kThreads threads, `smem` bytes each) that
+// fit on the current device at once (cached).
+int max_clusters(const void* fn, int smem, int cs) {
+  if (cs == 1) return dev_info().sms;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lk(g_cl_mu);
+    for (const ClusterFit& c : g_cl)
+      if (c.dev == dev && c.fn == fn && c.smem == smem && c.cs == cs) return c.n;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lk(g_cl_mu);
+  g_cl.push_back({dev, fn, smem, cs, n});
+  return n;
+}
+
+int tc_nsplit(const q2_blob_header& d, const void* fn, int smem) {
   const int ntile = (d.Rpad + kRows - 1) / kRows, S = tc_slices(d);
   long best = -1;
-  for (int ns = 1; ns <= S; ++ns) {
-    const long ctas = (long)ntile * ns;
-    const long waves = (ctas + sms - 1) / sms;
+  int nsplit = 1;
+  for (int ns = 1; ns <= std::min(S, kMaxSplit); ++ns) {
+    const int per_wave = max_clusters(fn, smem, ns);
+    if (per_wave < 1) continue;
+    const long waves = (ntile + per_wave - 1) / per_wave;
     const long cost = waves * ((S + ns - 1) / ns + kSplitOverhead);
     if (best < 0 || cost < best) {
       best = cost;
-      *nsplit = ns;
+      nsplit = ns;
     }
   }
-  *fused = (d.fmt == Q2_BPDQ && *nsplit > 1 &&
-            (size_t)ntok * d.Rpad <= (size_t)Q2_MAX_ACC_TOK * Q2_MAX_ROWS) ? 1 : 0;
+  return nsplit;
 }
 
-// Packed formats at 2..64 tokens on the tensor cores (tokens padded to a
-// multiple of 16).  Split-K partials (and every trellis / Leech result, whose
-// epilogue needs the row scale, exceptions and tail) go through the reduce
-// kernel.
+// Packed formats and the fp16 control at 2..64 tokens on the tensor cores
+// (tokens padded to a multiple of 16), one launch: the K split is summed
+// inside it and every format's epilogue applied there.
 template <int FMT, bool OFF4 = false>
 int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
   using Sh = TcShape<FMT, OFF4>;
   const q2_blob_header& d = h->hdr;
   TcArgs a = {};
+  a.post = 1.f;
   if (FMT == Q2_FP16) {
     a.w16 = reinterpret_cast<const __half*>(h->dev + d.off[SEC_FP16_W]);
   } else if (FMT == Q2_BPDQ) {
@@ -940,14 +1057,22 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
   } else if (FMT == Q2_TRELLIS) {
     a.bits = h->dev + d.off[SEC_TRL_STREAM];
     a.table = reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_TRL_TABLE]);
+    a.scale = reinterpret_cast<const __half*>(h->dev + d.off[SEC_TRL_SCALE]);
   } else {
     a.bits = h->dev + d.off[SEC_LEECH_PLANES];
     a.parity = reinterpret_cast<const uint16_t*>(h->dev + d.off[SEC_LEECH_PARITY]);
     a.nblock = d.nblock;
+    a.scale = reinterpret_cast<const __half*>(h->dev + d.off[SEC_LEECH_SCALE]);
+    a.post = d.inv_sqrt8;
+    a.tail = reinterpret_cast<const __half*>(h->dev + d.off[SEC_LEECH_TAIL]);
+    a.tail_n = d.tail;
+    a.tailpad = d.tailpad;
+    a.tail_col0 = d.nblock * 24;
+    a.excptr = reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_LEECH_EXCPTR]);
+    a.exccol = reinterpret_cast<const uint32_t*>(h->dev + d.off[SEC_LEECH_EXCCOL]);
   }
   a.x = static_cast<const __half*>(x);
   a.y = static_cast<__half*>(y);
-  a.partial = reinterpret_cast<float*>(static_cast<unsigned char*>(h->ws) + Q2_WS_PARTIAL_OFFSET);
   a.R = d.R;
   a.C = d.C;
   a.Rpad = d.Rpad;
@@ -956,39 +1081,41 @@ int launch_tc(const q2_handle* h, const void* x, void* y, int ntok, void* stream
   a.ntok = ntok;
   a.N = (ntok + 15) / 16 * 16;
   a.ntile = (d.Rpad + kRows - 1) / kRows;
-  tc_plan(d, ntok, &a.nsplit, &a.fused);
   a.use_tma = encode_x_map(&a.xmap, x, d.C, ntok, a.N) ? 1 : 0;
-  if (a.fused) {
-    int e = 0;
-    if (h->pbound > 0.0) std::frexp(h->pbound * (double)((a.S + a.nsplit - 1) / a.nsplit), &e);
-    const int F = std::max(-100, std::min(100, 45 - e));
-    a.acc = static_cast<unsigned long long*>(h->ws);
-    a.fscale = std::ldexp(1.0f, F);
-    a.finv = std::ldexp(1.0f, -F);
+  // table (or transpose tiles), 1024-byte alignment slack, B buffers (the
+  // partial sums reuse them), the mbarriers, TMEM slot and abort flag
+  const int smem =
+      max(kOneCtaSmem, Sh::table + 1024 + kStagesB * Sh::atoms * a.N * 128 + (2 * kStagesA + kStagesB + 2) * 8 + 16);
+  const void* fn = reinterpret_cast<const void*>(k_tc<FMT, OFF4>);
+  if (set_smem(fn, smem)) return Q2_ECUDA;
+  a.nsplit = tc_nsplit(d, fn, smem);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.ntile * a.nsplit);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = a.nsplit;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.nsplit > 1 ? 2 : 1;
+  if (cudaLaunchKernelEx(&cfg, k_tc<FMT, OFF4>, a) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return Q2_ECUDA;
   }
-  // table, 1024-byte alignment slack, B buffers, the stage mbarriers, TMEM slot
-  const int smem = max(kOneCtaSmem, Sh::table + 1024 + kStagesB * Sh::atoms * a.N * 128 + (2 * kStagesA + kStagesB + 2) * 8 + 16);
-  int st = launch_pdl(k_tc<FMT, OFF4>, a, a.ntile * a.nsplit, kThreads, smem, stream);
-  if (st) return st;
-  if ((FMT == Q2_BPDQ || FMT == Q2_FP16) && a.nsplit == 1) return Q2_OK;
-  if (FMT == Q2_BPDQ && a.fused) return Q2_OK;
-  return q2_launch_reduce_n(h, x, y, ntok, a.nsplit, stream);
+  return cudaGetLastError() == cudaSuccess ? Q2_OK : Q2_ECUDA;
 }
 
 }  // namespace
 }  // namespace q2
 
-// Workspace bytes of a tensor-core launch on the current device: none for
-// BPDQ without a K split (it writes y), the accumulator words when BPDQ's
-// split is reduced inside the launch, else the fp32 partials past the
-// accumulator reserve.
-extern "C" size_t q2_tc_workspace_bytes(const q2_handle* h, int ntok) {
-  int nsplit = 1, fused = 0;
-  q2::tc_plan(h->hdr, ntok, &nsplit, &fused);
-  if ((h->hdr.fmt == Q2_BPDQ || h->hdr.fmt == Q2_FP16) && nsplit == 1) return 0;
-  if (fused) return (size_t)ntok * h->hdr.Rpad * 8;
-  return Q2_WS_PARTIAL_OFFSET + (size_t)nsplit * ntok * h->hdr.Rpad * 4;
-}
+// Workspace bytes of a tensor-core launch: none (the K split is summed in
+// distributed shared memory).
+extern "C" size_t q2_tc_workspace_bytes(const q2_handle*, int) { return 0; }
 
 extern "C" int q2_tc_fp16(const q2_handle* h, const void* x, void* y, int ntok, void* stream) {
   return q2::launch_tc<Q2_FP16>(h, x, y, ntok, stream);

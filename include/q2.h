@@ -136,20 +136,14 @@ void q2_unbind(q2_handle* h);
  * completes the count writes y and resets the word.  These words must be
  * zero when the workspace is first used (allocate it zero-filled); every
  * completed call leaves them at zero again (a call whose x holds an inf or
- * NaN, or whose tensor-core launch hit a bounded-wait timeout, too: its
- * outputs are NaN).  The tensor-core path writes y directly when it does
- * not split K (BPDQ; no workspace), adds BPDQ's K-split partials to the same
- * words (one term per split) when the split is at most 15 and ntok x Rpad
- * <= 6 x 524288; otherwise, and for trellis and Leech, it keeps fp32
- * partial sums (nsplit x ntok x Rpad floats) at byte offset
- * 6 x 524288 x 8 (24 MiB), past any handle's accumulators, so one
- * workspace may serve many handles whose calls are ordered on one stream;
- * calls that overlap on the GPU must use different workspaces.  Limits:
- * R <= 524288 rows; on the CUDA-core paths C <= 255 x 256 columns.
- * The size depends on the path a token count takes (and, for the
- * tensor-core path, on the K split chosen for the current device's SM
- * count), so it is not monotone in ntok: a workspace for every call up to
- * N tokens is the largest q2_workspace_bytes over ntok = 1..N. */
+ * NaN too: its outputs are NaN).  The tensor-core path (2..64 tokens) uses
+ * no workspace: a K split's CTAs run as one thread-block cluster and sum
+ * their fp32 partials in distributed shared memory.  One workspace may serve
+ * many handles whose calls are ordered on one stream; calls that overlap on
+ * the GPU must use different workspaces.  Limits: R <= 524288 rows; on the
+ * CUDA-core paths C <= 255 x 256 columns.  The size depends on the path a
+ * token count takes, so it is not monotone in ntok: a workspace for every
+ * call up to N tokens is the largest q2_workspace_bytes over ntok = 1..N. */
 int q2_workspace_bytes(const q2_handle* h, int ntok, size_t* bytes);
 int q2_set_workspace(q2_handle* h, void* ws_dev, size_t ws_bytes);
 
@@ -164,8 +158,7 @@ int q2_bytes(const q2_handle* h, int ntok, size_t* weight_bytes_read_per_call);
  * Asynchronous and ordered on `stream`; never synchronises.  Needs the
  * workspace of q2_workspace_bytes(h, ntok) bound first (0 bytes for fp16 at
  * one token).  The dense fp16 control runs one token on CUDA cores and
- * 2..64 tokens through the tensor-core kernel, loading its rows as they are
- * (fp32 partials and the reduction launch when it splits K).
+ * 2..64 tokens through the tensor-core kernel, loading its rows as they are.
  * The packed formats at 1 token, and BPDQ at 2..6 tokens, run on CUDA cores
  * in launches that reduce their split-K partial sums themselves, through the
  * workspace's fixed-point accumulator words (integer sums: the result does
@@ -174,11 +167,13 @@ int q2_bytes(const q2_handle* h, int ntok, size_t* weight_bytes_read_per_call);
  * token's BPDQ result at 1..6 tokens is bit-identical whatever the batch.
  * Leech at 2 tokens runs two single-token launches when C and R are
  * multiples of 8.  The tensor-core path (7..64 tokens, or 2..64 for trellis
- * and the other Leech cases) reduces BPDQ's K splits the same way inside its
- * launch; trellis and Leech add a second, in-order reduction launch.  The
- * fixed-point scale 2^F is chosen per matrix (and, on the tensor-core path,
- * per K split) from its largest weight magnitude so that no fp16 x can
- * overflow it; each term then carries an absolute rounding error of at most
+ * and the other Leech cases) is one launch: a tile's K splits (at most 8,
+ * one thread-block cluster) add their fp32 partials in split order, so the
+ * result does not depend on which finished first, and the same pass applies
+ * the format's row epilogue (trellis: scale; Leech: exceptions, scale,
+ * tail).  The fixed-point scale 2^F of the CUDA-core paths is chosen per
+ * matrix from its largest weight magnitude so that no fp16 x can overflow
+ * it; each term then carries an absolute rounding error of at most
  * 2^-(F+1), about 2e-8 per 256-column slice for weights of magnitude
  * 0.05.  An inf or NaN in a token's x makes that token's outputs NaN (the
  * IEEE result is non-finite for every row; the fixed-point sums carry a
@@ -278,11 +273,11 @@ int q2_rotate_split(int C, int* nh, int* nq);
 
 /* Device-side error word of the tensor-core (multi-token) kernels, then
  * cleared: 0 in normal operation; nonzero means a bounded wait on the
- * tensor core ran out and the kernel skipped its work (its outputs are not
- * valid: NaN where BPDQ's K split is reduced inside the launch, whose
- * accumulator words are still left at zero).  Before such a kernel's CTA
- * exits it waits, with the full bound, for its copies and MMAs in flight.
- * Synchronous: reads device memory of the current device. */
+ * tensor core ran out and the kernel skipped its work (the rows of the tiles
+ * concerned are NaN).  Before such a kernel's CTA exits it waits, with the
+ * full bound, for its copies and MMAs in flight, and it still meets the
+ * other CTAs of its cluster at both of their barriers.  Synchronous: reads
+ * device memory of the current device. */
 int q2_device_errors(unsigned int* out);
 
 /* Test hook, not for production use: limits the tensor-core kernel's stage

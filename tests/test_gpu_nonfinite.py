@@ -2,14 +2,14 @@
 
 In IEEE arithmetic one inf or NaN in a token's x makes every output of that
 token non-finite (every row has a weight in that column, and 0 x inf is
-NaN); the oracle (f64 numpy) shows it.  The fixed-point split-K sums cannot
-carry infs or NaNs, so the kernels detect them: the CUDA-core paths scan
-the whole x of their tokens, the tensor-core path's fused reduction adds a
-poison term for a non-finite split partial.  These tests put an inf in one
+NaN); the oracle (f64 numpy) shows it.  The fixed-point split-K sums of
+the CUDA-core paths cannot carry infs or NaNs, so those kernels flag them
+in the accumulator word; the tensor-core path sums fp32 partials (in a
+cluster's shared memory), which carry them.  These tests put an inf in one
 token and a NaN in another, at 1 token (every format), 3 tokens (BPDQ
-token pairs) and 16 tokens (the tensor-core path, with and without the
-fused reduction), and check that exactly the affected tokens' outputs are
-non-finite while the other tokens still match the oracle.
+token pairs) and 16 tokens (the tensor-core path, with and without a K
+split), and check that exactly the affected tokens' outputs are non-finite
+while the other tokens still match the oracle.
 Tolerance for the finite tokens: |y - y_ref| <= 2e-3 * sum_c |w x|.
 """
 import numpy as np
@@ -53,8 +53,8 @@ CASES = [
     ("bpdq", 1024, 4096, 1),     # single-token kernel, 16 slices
     ("bpdq", 2048, 12288, 1),    # 48 slices
     ("bpdq", 512, 2048, 3),      # token pairs + single token
-    ("bpdq", 256, 2048, 16),     # tensor cores, K split reduced inside the launch
-    ("bpdq", 256, 4096, 16),     # tensor cores, K split through fp32 partials
+    ("bpdq", 256, 2048, 16),     # tensor cores, K split over a cluster
+    ("bpdq", 256, 4096, 16),     # tensor cores, a wider K split
     ("trellis", 512, 2048, 1),
     ("trellis", 256, 2048, 16),
     ("leech", 544, 1040, 1),

@@ -11,7 +11,9 @@ These tests check, through the C ABI, that
     weights and the fp16 range, not from x) stay within the tolerance;
   - a chain of GEMVs of different formats and shapes sharing one workspace
     on one stream is correct, leaves every accumulator word at zero, and
-    gives bit-identical outputs run after run.
+    gives bit-identical outputs run after run; at 16 and 64 tokens the same
+    for the tensor-core path, whose K splits are summed over a thread-block
+    cluster in split order (no workspace).
 Tolerance: |y - y_ref| <= 2e-3 * sum_c |w x| per output.
 """
 import numpy as np
@@ -124,11 +126,11 @@ def test_shared_workspace_chain_is_correct_and_repeatable(q2, ntok):
     mats = _chain(q2)
     if ntok > 1:
         # 2..6 tokens share the split-K path in BPDQ only; from 7 the tensor
-        # cores reduce BPDQ's K split inside the launch (these shapes split K)
+        # cores sum BPDQ's K split over a cluster (these shapes split K)
         mats = [m for m in mats if m[0] == "bpdq"]
     pks = [q2.Packed(blob, ntok_max=ntok, workspace=torch.zeros(16, dtype=torch.uint8, device="cuda"))
            for _, _, _, _, blob in mats]
-    ws = torch.zeros(max(p.workspace_bytes(ntok) for p in pks), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(16, max(p.workspace_bytes(ntok) for p in pks)), dtype=torch.uint8, device="cuda")
     for p in pks:
         p.set_workspace(ws)
     xs = [torch.from_numpy(synth.activations(ntok, C, 8300 + i)).cuda() for i, (_, _, C, _, _) in enumerate(mats)]
@@ -140,7 +142,7 @@ def test_shared_workspace_chain_is_correct_and_repeatable(q2, ntok):
         stream.synchronize()
         return [y.cpu().numpy() for y in ys]
 
-    acc = ws[:6 * 524288 * 8]               # the accumulator words (fp32 partials may follow)
+    acc = ws                                # the accumulator words
     plain = run()
     assert not acc.any().item()
     again = [run() for _ in range(3)]

@@ -5,11 +5,12 @@ Every wait in the tensor-core kernel is bounded.  A test hook
 slice's decoded weights and x tile ready) to a single poll, so they give up
 before the decoders can finish; the roles then stop waiting on each other,
 the CTA waits with the full bound for its x copies and MMAs still in flight,
-frees its tensor memory and exits.  Nothing faults and nothing hangs: the
-host reads a nonzero error word, the fused BPDQ reduction has written NaN
-and left the workspace's accumulator words at zero, and the next call with
-the normal bound is correct again.  Tolerance for the normal calls:
-|y - y_ref| <= 2e-3 * sum_c |w x|.
+puts NaN in place of its partial sums, still meets its cluster at both
+barriers (a K split's CTAs sum their partials together), frees its tensor
+memory and exits.  Nothing faults and nothing hangs: the host reads a
+nonzero error word, the rows of the tiles that gave up are NaN, the
+workspace is untouched, and the next call with the normal bound is correct
+again.  Tolerance for the normal calls: |y - y_ref| <= 2e-3 * sum_c |w x|.
 """
 import numpy as np
 import pytest
@@ -38,8 +39,7 @@ def _passes(y, w, x):
 
 
 def test_stage_wait_timeout_reports_error_and_leaves_workspace_clean(q2):
-    # BPDQ 1024 x 4096 at 16 tokens: 8 row tiles, K split 16 ways, reduced
-    # inside the launch through the workspace's accumulator words
+    # BPDQ 1024 x 4096 at 16 tokens: 8 row tiles, K split over clusters
     R, C, ntok = 1024, 4096, 16
     d = synth.bpdq(R, C, 9600)
     w = obpdq.decode_f64(d["plane0"], d["plane1"], d["coef"])
@@ -53,17 +53,17 @@ def test_stage_wait_timeout_reports_error_and_leaves_workspace_clean(q2):
         q2.debug_wait_limit(0)
     err = q2.device_errors()
     assert err != 0
-    assert np.isnan(y.astype(np.float32)).any()          # rows of the splits that gave up
-    acc = pk.ws[:ntok * R * 8]
-    assert not acc.any().item()                          # every word completed and reset
+    assert np.isnan(y.astype(np.float32)).any()          # rows of the tiles that gave up
+    if pk.ws is not None:
+        assert not pk.ws.any().item()                    # the accumulator words are untouched
     # the next call with the normal bound is correct and reports nothing
     y2 = pk.gemv(xd).cpu().numpy()
     assert q2.device_errors() == 0
     assert _passes(y2, w, x)
 
 
-def test_stage_wait_timeout_on_the_partial_sum_path(q2):
-    # trellis at 16 tokens keeps fp32 partials for the reduce launch
+def test_stage_wait_timeout_with_a_row_epilogue(q2):
+    # trellis at 16 tokens: the cluster's sum is scaled per row before y
     R, C, ntok = 512, 2048, 16
     d = synth.trellis(R, C, 9610)
     w = otrellis.decode_f64(d["stream"], d["table"], d["scale"])
