@@ -548,7 +548,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
   for (int t = 0; t < NW; ++t) pl[t] = n1[t] = 0;
   if (valid && used > 0) load(sA, pl, vt, par);
   if (valid && used > 1) load(sA + 1, n1, v1, p1);
-  pdl_wait();
+  // Programmatic dependent launch: only x and y depend on the kernel before
+  // this one on the stream, so a role waits for it (griddepcontrol.wait) just
+  // before it first reads x (the helper's copies; Leech's decoders, whose
+  // parity columns use block sums of x) and every thread before the
+  // epilogue writes y.  The weights are decoded into TMEM meanwhile: a CTA
+  // that lands on an SM freed early has its first slices decoded when the
+  // previous kernel completes.
   pdl_trigger();
   tc_fence_before();
   __syncthreads();
@@ -612,6 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
       }
     };
     const long long stage_limit = q2_tc_stage_wait_limit > 0 ? q2_tc_stage_wait_limit : kSpinLimit;
+    pdl_wait();                                      // x is the previous kernel's output
     int produced = min(kStagesB, used), waitedB = 0;   // slices whose x copy was issued / seen complete
     for (int i = 0; i < produced; ++i) produce(i);
     int handed = 0;
@@ -670,6 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
     if (!ok) sleep_us(50);
   } else {
     // ---- decoders: slice i into A stage i % kStagesA
+    if (FMT == Q2_LEECH) pdl_wait();                 // the parity columns read x
     const uint32_t sh = 32u - 8u * (uint32_t)(lane & 3);
     for (int i = 0; i < used; ++i) {
       const int s = sA + i, sa = i % kStagesA;
@@ -820,6 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
       }
     }
   }
+  pdl_wait();                                        // before anything writes y (returns at once if done)
   ok = __syncthreads_and(ok);
   tc_fence_after();
   // ---- epilogue.  (1) The accumulator, or NaN where a bounded wait ran out,

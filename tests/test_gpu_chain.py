@@ -104,3 +104,45 @@ def test_chain_refuses_bad_arguments_before_launching(q2):
         ch.run()
     torch.cuda.synchronize()
     assert (y == 7.0).all().item()                          # nothing was launched
+
+
+@pytest.mark.parametrize("fmt", ["bpdq", "trellis", "leech", "fp16"])
+@pytest.mark.parametrize("ntok", [16, 64])
+def test_tensor_core_chain_with_true_dependency_matches_oracle(q2, fmt, ntok):
+    """The tensor-core kernel waits for the previous kernel only where it reads
+    x and before it writes y (its weights are decoded before the wait): a chain
+    whose y is the next GEMV's x, launched back to back, must match the oracle
+    run in the same order from the GPU's own fp16 inputs."""
+    from oracle import fp16 as ofp16, leech as oleech, trellis as otrellis
+    C = 2048 if fmt != "leech" else 2064                     # Leech: 86 blocks, no tail
+    pks, ws64 = [], []
+    for i in range(4):
+        if fmt == "bpdq":
+            d = synth.bpdq(C, C, 9500 + i)
+            pks.append(q2.Packed(q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]), ntok_max=ntok))
+            ws64.append(obpdq.decode_f64(d["plane0"], d["plane1"], d["coef"]))
+        elif fmt == "trellis":
+            d = synth.trellis(C, C, 9510 + i)
+            pks.append(q2.Packed(q2.q2_pack_trellis(d["stream"], d["table"], d["scale"]), ntok_max=ntok))
+            ws64.append(otrellis.decode_f64(d["stream"], d["table"], d["scale"]))
+        elif fmt == "leech":
+            d = synth.leech(C, C, 9520 + i)
+            pks.append(q2.Packed(q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C), ntok_max=ntok))
+            ws64.append(oleech.decode_f64(d["v"], d["scale"], d["tail"]))
+        else:
+            d = synth.fp16_dense(C, C, 9530 + i)
+            pks.append(q2.Packed(q2.q2_pack_fp16(d["w"]), ntok_max=ntok))
+            ws64.append(ofp16.decode_f64(d["w"]))
+    x0 = synth.activations(ntok, C, 9540)
+    bufs = [torch.from_numpy(x0).cuda()] + [torch.empty((ntok, C), dtype=torch.float16, device="cuda") for _ in pks]
+    chain = q2.Chain([(p, bufs[i], bufs[i + 1]) for i, p in enumerate(pks)], ntok, 0)
+    chain.run()
+    torch.cuda.synchronize()
+    x = x0
+    for i, w in enumerate(ws64):
+        y = bufs[i + 1].cpu().numpy()
+        assert np.isfinite(y.astype(np.float32)).all(), f"GEMV {i}: non-finite outputs"
+        ok = matvec.passes(y, matvec.gemv(w, x), matvec.abs_bound(w, x), 2e-3)
+        assert ok.all(), f"GEMV {i}: {(~ok).sum()} outputs outside the tolerance"
+        x = y
+    assert q2.device_errors() == 0
