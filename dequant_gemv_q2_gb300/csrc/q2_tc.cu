@@ -265,13 +265,11 @@ __device__ __forceinline__ void cluster_sync() {
 
 constexpr uint32_t kHashHi = 0x9E37u << 16;     // trellis: (s*0x9E37 mod 2^16) in bits 16..31
 
-// Per-format shape of a slice's K range: 32 chunks of 8 columns, plus, for
-// Leech, 4 chunks carrying the parity term (A = parity bit of the blocks
-// starting in the slice, B = their block sums of x split into fp16 hi + lo).
-// OFF4: the Leech offset-binary layout (four planes).
+// Per-format shape of a slice's K range: 32 chunks of 8 columns.  OFF4: the
+// Leech offset-binary layout (four planes).
 template <int FMT, bool OFF4 = false>
 struct TcShape {
-  static constexpr int kch = FMT == Q2_LEECH ? 36 : 32;   // fp16 control: 32, like BPDQ and trellis
+  static constexpr int kch = 32;
   static constexpr int kmma = kch / 2;                  // K = 16 steps per slice
   static constexpr int atoms = (kch + 7) / 8;           // 64-column swizzle atoms of B
   static constexpr uint32_t acols = kch * 4;            // TMEM columns of one A stage
@@ -305,12 +303,15 @@ __device__ __forceinline__ Codes4 codes4x3(uint32_t w0, uint32_t w1, uint32_t w2
   return c;
 }
 
-// 2u = 2*(b0 + 2*b1 - 4*b2) in fp16 for the 8 columns of byte Q; the low
-// byte of every such fp16 value is 0, so only high bytes are looked up.
+// v = p + 2u = p + 2*(b0 + 2*b1 - 4*b2) in fp16 for the 8 columns of byte
+// Q, p being the parity bit of the block the byte lies in (a block is three
+// column-bytes, so a byte never straddles two).  Every value in -8..7 has a
+// zero low byte in fp16, so only high bytes are looked up, from the table
+// of the byte's parity.
 template <int Q>
-__device__ __forceinline__ uint4 decode_leech_q(const Codes4& c) {
-  // fp16 high bytes of 0, 2, 4, 6, -8, -6, -4, -2 (code 0..7)
-  constexpr uint32_t HA = 0x46444000u, HB = 0xC0C4C6C8u;
+__device__ __forceinline__ uint4 decode_leech_q(const Codes4& c, uint32_t p) {
+  // fp16 high bytes of p + (0, 2, 4, 6, -8, -6, -4, -2) (code 0..7)
+  const uint32_t HA = p ? 0x4745423Cu : 0x46444000u, HB = p ? 0xBCC2C5C7u : 0xC0C4C6C8u;
   constexpr uint32_t sel = (uint32_t)Q | ((4u + Q) << 4);
   const uint32_t s0 = __byte_perm(c.ea, c.oa, sel);   // codes of cols 0,4,1,5
   const uint32_t s1 = __byte_perm(c.eb, c.ob, sel);   // cols 2,6,3,7
@@ -323,15 +324,16 @@ __device__ __forceinline__ uint4 decode_leech_q(const Codes4& c) {
   return r;
 }
 
-// Offset-binary Leech (four planes): v - p = 2c - 8 for the code
-// c = b0 + 2 b1 + 4 b2 + 8 b3 in 0..8.  The low three bits index the fp16
-// high bytes of -8, -6, ..., 6; c = 8 (v = +8, rare) has low bits 0, so its
-// -8 is turned into +8 by flipping the sign bit of each column whose plane-3
-// bit is set (byte q3 of plane 3 for these 8 columns).
+// Offset-binary Leech (four planes): v = p + 2c - 8 for the code
+// c = b0 + 2 b1 + 4 b2 + 8 b3 in 0..8 and the byte's block parity p.  The
+// low three bits index the fp16 high bytes of p + (-8, -6, ..., 6); c = 8
+// (v = +8, rare, p = 0) has low bits 0, so its -8 is turned into +8 by
+// flipping the sign bit of each column whose plane-3 bit is set (byte q3 of
+// plane 3 for these 8 columns).
 template <int Q>
-__device__ __forceinline__ uint4 decode_leech4_q(const Codes4& c, uint32_t q3) {
-  // fp16 high bytes of -8, -6, -4, -2, 0, 2, 4, 6 (code 0..7)
-  constexpr uint32_t HA = 0xC0C4C6C8u, HB = 0x46444000u;
+__device__ __forceinline__ uint4 decode_leech4_q(const Codes4& c, uint32_t q3, uint32_t p) {
+  // fp16 high bytes of p + (-8, -6, -4, -2, 0, 2, 4, 6) (code 0..7)
+  const uint32_t HA = p ? 0xBCC2C5C7u : 0xC0C4C6C8u, HB = p ? 0x4745423Cu : 0x46444000u;
   constexpr uint32_t sel = (uint32_t)Q | ((4u + Q) << 4);
   const uint32_t s0 = __byte_perm(c.ea, c.oa, sel);   // codes of cols 0,4,1,5
   const uint32_t s1 = __byte_perm(c.eb, c.ob, sel);   // cols 2,6,3,7
@@ -382,27 +384,32 @@ __device__ __forceinline__ void bpdq_part(const uint32_t (&L0)[kPartWords + 1], 
   }
 }
 
-// Leech: the same for the three sign/magnitude planes (values 2u).
+// Leech: the same for the three sign/magnitude planes (values p + 2u); bit
+// k of pm is the parity of the part's column-byte k.
 __device__ __forceinline__ void leech_part(const uint32_t (&L0)[kPartWords + 1], const uint32_t (&L1)[kPartWords + 1],
-                                           const uint32_t (&L2)[kPartWords + 1], uint32_t sh, uint32_t ta) {
+                                           const uint32_t (&L2)[kPartWords + 1], uint32_t sh, uint32_t ta,
+                                           uint32_t pm) {
 #pragma unroll
   for (int j = 0; j < kPartWords; ++j) {
     const Codes4 c = codes4x3(unrot(L0[j], L0[j + 1], sh), unrot(L1[j], L1[j + 1], sh), unrot(L2[j], L2[j + 1], sh));
-    tmem_st16(ta + (uint32_t)(16 * j), decode_leech_q<0>(c), decode_leech_q<1>(c), decode_leech_q<2>(c),
-              decode_leech_q<3>(c));
+    const uint32_t pb = pm >> (4 * j);
+    tmem_st16(ta + (uint32_t)(16 * j), decode_leech_q<0>(c, pb & 1u), decode_leech_q<1>(c, pb & 2u),
+              decode_leech_q<2>(c, pb & 4u), decode_leech_q<3>(c, pb & 8u));
   }
 }
 
-// Offset-binary Leech: the part from its four planes (values 2c - 8).
+// Offset-binary Leech: the part from its four planes (values p + 2c - 8).
 __device__ __forceinline__ void leech4_part(const uint32_t (&L0)[kPartWords + 1], const uint32_t (&L1)[kPartWords + 1],
                                             const uint32_t (&L2)[kPartWords + 1], const uint32_t (&L3)[kPartWords + 1],
-                                            uint32_t sh, uint32_t ta) {
+                                            uint32_t sh, uint32_t ta, uint32_t pm) {
 #pragma unroll
   for (int j = 0; j < kPartWords; ++j) {
     const Codes4 c = codes4x3(unrot(L0[j], L0[j + 1], sh), unrot(L1[j], L1[j + 1], sh), unrot(L2[j], L2[j + 1], sh));
     const uint32_t w3 = unrot(L3[j], L3[j + 1], sh);
-    tmem_st16(ta + (uint32_t)(16 * j), decode_leech4_q<0>(c, w3 & 0xFFu), decode_leech4_q<1>(c, (w3 >> 8) & 0xFFu),
-              decode_leech4_q<2>(c, (w3 >> 16) & 0xFFu), decode_leech4_q<3>(c, w3 >> 24));
+    const uint32_t pb = pm >> (4 * j);
+    tmem_st16(ta + (uint32_t)(16 * j), decode_leech4_q<0>(c, w3 & 0xFFu, pb & 1u),
+              decode_leech4_q<1>(c, (w3 >> 8) & 0xFFu, pb & 2u), decode_leech4_q<2>(c, (w3 >> 16) & 0xFFu, pb & 4u),
+              decode_leech4_q<3>(c, w3 >> 24, pb & 8u));
   }
 }
 
@@ -473,20 +480,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
   }
   if (FMT == Q2_TRELLIS)
     for (int i = threadIdx.x; i < 4096; i += kThreads) tab[i] = a.table[i];
-  // zero what the TMA does not write: the Leech parity atom (token rows past
-  // ntok stay zero), or every atom when x is staged without TMA
-  {
-    const int z0 = a.use_tma ? 4 * atom_bytes : 0;
+  // zero the B stages when x is staged without TMA (token rows past ntok
+  // stay zero); the TMA fills whole boxes itself
+  if (!a.use_tma)
     for (int st = 0; st < kStagesB; ++st)
-      for (int i = threadIdx.x * 16 + z0; i < bbytes; i += kThreads * 16)
+      for (int i = threadIdx.x * 16; i < bbytes; i += kThreads * 16)
         *reinterpret_cast<uint4*>(B0 + st * bbytes + i) = make_uint4(0, 0, 0, 0);
-  }
   fence_async_smem();
 
   // Decoder payload of one slice: the rotated words this lane's part needs
   // (BPDQ / Leech: kPartWords + 1 per plane; trellis: a 5-word window of the
   // 64-byte symbol packet), at per-lane offsets fixed for the whole kernel;
-  // plus BPDQ's value table / Leech's parity word.
+  // plus BPDQ's value table / Leech's parity words.
   constexpr int NPL = Sh::planes;
   // (fp16 control: nothing is held ahead; the rows are read when the slice is stored)
   constexpr int NW = FMT == Q2_TRELLIS ? 5 : FMT == Q2_FP16 ? 1 : NPL * (kPartWords + 1);
@@ -542,17 +547,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
 #pragma unroll
     for (int t = 0; t < NW; ++t) d[t] = __ldg(reinterpret_cast<const uint32_t*>(ip + off[t]));
     if (FMT == Q2_BPDQ) v = a.vtab[(size_t)s * a.Rpad + row];
-    if (FMT == Q2_LEECH) pw = a.parity[(size_t)s * a.Rpad + row];
+    // Leech: the parity bits of the blocks starting in slice s, and in the
+    // high half those of slice s - 1 (its last block may reach into slice s)
+    if (FMT == Q2_LEECH)
+      pw = (uint32_t)a.parity[(size_t)s * a.Rpad + row] |
+           (s > 0 ? (uint32_t)a.parity[(size_t)(s - 1) * a.Rpad + row] << 16 : 0u);
   };
 #pragma unroll
   for (int t = 0; t < NW; ++t) pl[t] = n1[t] = 0;
   if (valid && used > 0) load(sA, pl, vt, par);
   if (valid && used > 1) load(sA + 1, n1, v1, p1);
   // Programmatic dependent launch: only x and y depend on the kernel before
-  // this one on the stream, so a role waits for it (griddepcontrol.wait) just
-  // before it first reads x (the helper's copies; Leech's decoders, whose
-  // parity columns use block sums of x) and every thread before the
-  // epilogue writes y.  The weights are decoded into TMEM meanwhile: a CTA
+  // this one on the stream, so the helper waits for it (griddepcontrol.wait)
+  // just before it first copies x, and every thread before the epilogue
+  // writes y.  The weights are decoded into TMEM meanwhile: a CTA
   // that lands on an SM freed early has its first slices decoded when the
   // previous kernel completes.
   pdl_trigger();
@@ -677,7 +685,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
     if (!ok) sleep_us(50);
   } else {
     // ---- decoders: slice i into A stage i % kStagesA
-    if (FMT == Q2_LEECH) pdl_wait();                 // the parity columns read x
     const uint32_t sh = 32u - 8u * (uint32_t)(lane & 3);
     for (int i = 0; i < used; ++i) {
       const int s = sA + i, sa = i % kStagesA;
@@ -743,65 +750,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcAr
           L1[t] = pl[kPartWords + 1 + t];
           L2[t] = pl[2 * (kPartWords + 1) + t];
         }
+        // The parity of each of the part's 8 column-bytes.  Byte GB of the
+        // row lies in block GB / 3; blocks from bf on start in slice s (low
+        // half of par), block bf - 1 in slice s - 1 (high half).  With
+        // P = (bit of block bf - 1) | (slice s's bits << 1), the part's
+        // first byte q lies in block q / 3 and its 8 bytes in blocks
+        // q / 3 .. q / 3 + 3: take those 4 bits, widen each to the 3 bytes
+        // of its block and drop the q % 3 bytes before q.
+        const int q = s * 32 + part * kPartBytes, bf = (s * 32 + 2) / 3;
+        const int bfp = s > 0 ? ((s - 1) * 32 + 2) / 3 : 0;
+        const uint32_t P = ((par >> (16 + bf - 1 - bfp)) & 1u) | ((par & 0xFFFFu) << 1);
+        const uint32_t B = (P >> (q / 3 - bf + 1)) & 0xFu;
+        const uint32_t E = (B & 1u) * 7u | (B & 2u) * 28u | (B & 4u) * 112u | (B & 8u) * 448u;
+        const uint32_t pm = (E >> (q % 3)) & 0xFFu;
         if constexpr (OFF4) {
           uint32_t L3[kPartWords + 1];
 #pragma unroll
           for (int t = 0; t <= kPartWords; ++t) L3[t] = pl[(NPL - 1) * (kPartWords + 1) + t];
-          leech4_part(L0, L1, L2, L3, sh, ta);
+          leech4_part(L0, L1, L2, L3, sh, ta, pm);
         } else {
-          leech_part(L0, L1, L2, sh, ta);
+          leech_part(L0, L1, L2, sh, ta, pm);
         }
-        if (part == 0) {
-          // parity columns (K 256..287, TMEM columns 128..143 of the stage):
-          // A = 1.0 where the block starting in this slice is odd, once for
-          // the hi and once for the lo part of the block sums
-          uint32_t pv[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t lo = ((par >> (2 * q)) & 1u) ? 0x3C00u : 0u;
-            const uint32_t hi = ((par >> (2 * q + 1)) & 1u) ? 0x3C000000u : 0u;
-            pv[q] = lo | hi;
-          }
-          const uint4 q0 = make_uint4(pv[0], pv[1], pv[2], pv[3]), q1 = make_uint4(pv[4], pv[5], pv[6], pv[7]);
-          tmem_st16(tlane + kAcol0 + (uint32_t)sa * Sh::acols + 128u, q0, q1, q0, q1);
-        }
-        // B side of the parity columns (atom 4 of B stage i % kStagesB, free:
-        // the MMAs up to slice i - kStagesA, which include those of slice
-        // i - kStagesB, are done):
-        // block sums of x for the blocks starting in this slice, hi part at
-        // K 256 + jb, lo part (sum - hi) at K 272 + jb
-        const int bfirst = (s * 256 + 23) / 24;
-        const int blast = min(a.nblock - 1, (s * 256 + 256 + 23) / 24 - 1);
-        const int nbk = max(0, blast - bfirst + 1);
-        unsigned char* Bp = B0 + (i % kStagesB) * bbytes + 4 * atom_bytes;
-        for (int e = threadIdx.x; e < a.ntok * 16; e += kDecWarps * 32) {
-          const int n = e >> 4, jb = e & 15;
-          float xsum = 0.f;
-          if (jb < nbk) {
-            const __half* xp = a.x + (size_t)n * a.C + (size_t)(bfirst + jb) * 24;
-            if (a.use_tma) {                         // 48-byte blocks of 16-byte aligned rows
-              const uint4* xv = reinterpret_cast<const uint4*>(xp);
-#pragma unroll
-              for (int k = 0; k < 3; ++k) {
-                const uint4 r = __ldg(xv + k);
-                const __half2* h2 = reinterpret_cast<const __half2*>(&r);
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                  const float2 f = __half22float2(h2[m]);
-                  xsum += f.x + f.y;
-                }
-              }
-            } else {
-              for (int k = 0; k < 24; ++k) xsum += __half2float(xp[k]);
-            }
-          }
-          const __half hi = __float2half_rn(xsum);
-          const __half lo = __float2half_rn(xsum - __half2float(hi));
-          unsigned char* rp = Bp + n * 128 + (jb & 7) * 2;
-          *reinterpret_cast<__half*>(rp + ((((jb >> 3) + 0) ^ (n & 7)) << 4)) = hi;
-          *reinterpret_cast<__half*>(rp + ((((jb >> 3) + 2) ^ (n & 7)) << 4)) = lo;
-        }
-        fence_async_smem();
       }
       tmem_wait_st();
       tc_fence_before();
