@@ -153,3 +153,31 @@ def test_shared_workspace_chain_is_correct_and_repeatable(q2, ntok):
     for (kind, R, C, d, _), y, x in zip(mats, plain, xs):
         rows = np.unique(np.linspace(0, R - 1, 48).astype(int))
         _check(y, _w64(kind, d, rows), x.cpu().numpy(), rows)
+
+
+@pytest.mark.parametrize("fmt", ["bpdq", "trellis", "leech", "fp16"])
+@pytest.mark.parametrize("slices", [2, 3, 5, 8, 13, 64])
+def test_tensor_core_k_split_over_clusters(q2, fmt, slices):
+    """K splits of 2..8 CTAs summed over a thread-block cluster, on a ragged
+    row count (the last tile's rows past R, and R % 4 != 0, which takes the
+    epilogue's scalar stores); every format, 16 tokens."""
+    from oracle import fp16 as ofp16
+    R, ntok = 201, 16
+    C = 256 * slices if fmt != "leech" else 256 * slices + 8       # Leech: C % 24 != 0, a tail
+    if fmt == "bpdq":
+        d = synth.bpdq(R, C, 8600 + slices)
+        blob, w = q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]), obpdq.decode_f64(d["plane0"], d["plane1"], d["coef"])
+    elif fmt == "trellis":
+        d = synth.trellis(R, C, 8610 + slices)
+        blob, w = q2.q2_pack_trellis(d["stream"], d["table"], d["scale"]), otrellis.decode_f64(d["stream"], d["table"], d["scale"])
+    elif fmt == "leech":
+        d = synth.leech(R, C, 8620 + slices)
+        blob, w = q2.q2_pack_leech(d["v"], d["tail"], d["scale"], C), oleech.decode_f64(d["v"], d["scale"], d["tail"])
+    else:
+        d = synth.fp16_dense(R, C, 8630 + slices)
+        blob, w = q2.q2_pack_fp16(d["w"]), ofp16.decode_f64(d["w"])
+    pk = q2.Packed(blob, ntok_max=ntok)
+    x = synth.activations(ntok, C, 8640 + slices)
+    y = pk.gemv(torch.from_numpy(x).cuda()).cpu().numpy()
+    _check(y, w, x)
+    assert q2.device_errors() == 0
