@@ -343,7 +343,10 @@ __device__ __forceinline__ void ld_item(const unsigned char* base, int item_byte
 // per SM (16 warps for Leech, 24 for the trellis), one item ahead per warp
 // in registers (measured: 2 ahead is slower).
 constexpr int kMinBlocks = 1;
-constexpr int kLeechAhead = 1;
+#ifndef Q2_LEECH_AHEAD
+#define Q2_LEECH_AHEAD 1
+#endif
+constexpr int kLeechAhead = Q2_LEECH_AHEAD;   // items a warp holds in registers beyond the one it sums
 #ifndef Q2_LEECH_W
 #define Q2_LEECH_W 16
 #endif
