@@ -218,3 +218,41 @@ def test_rotation_split_and_argument_checks(q2):
     assert L.q2_rotate(x, y, 1, 2048 * 32, 2048, s, q, None) == -2                  # C over the maximum
     assert L.q2_rotate(x, y, 1, 4096, 1024, s, None, None) == -1                    # nq = 4 needs Q
     assert L.q2_rotate(x, x, 1, 4096, 4096, s, None, None) == -1                    # in place
+
+
+_PACK_SCRIPT = r"""
+import hashlib, sys
+sys.path.insert(0, {root!r})
+import numpy as np
+import dequant_gemv_q2_gb300 as q2
+import synth
+out = []
+d = synth.bpdq(70, 768, 5)
+out.append(q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"]))
+d = synth.trellis(70, 512, 6)
+out.append(q2.q2_pack_trellis(d["stream"], d["table"], d["scale"]))
+d = synth.leech(70, 1040, 7)
+out.append(q2.q2_pack_leech(d["v"], d["tail"], d["scale"], 1040))
+out.append(q2.q2_pack_leech(d["v"], d["tail"], d["scale"], 1040, layout=q2.LEECH_OFFSET4))
+d = synth.fp16_dense(70, 1032, 8)
+out.append(q2.q2_pack_fp16(d["w"]))
+out.append(q2.q2_pack_noweights(70, 768))
+print(" ".join(hashlib.sha256(np.ascontiguousarray(b).tobytes()).hexdigest() for b in out))
+"""
+
+
+def test_packed_blobs_are_identical_across_processes(q2):
+    """A blob is a pure function of its canonical inputs: every byte,
+    alignment padding included, is the same in two separate processes (so a
+    blob written on one machine matches one packed on another)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = _PACK_SCRIPT.format(root=root)
+    runs = [subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300, cwd=root)
+            for _ in range(2)]
+    for r in runs:
+        assert r.returncode == 0, r.stderr[-2000:]
+    assert runs[0].stdout.split() == runs[1].stdout.split()
+    assert len(runs[0].stdout.split()) == 6
