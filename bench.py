@@ -9,14 +9,14 @@ buffer per projection, shared by the layers as an engine's activation
 buffers are.  Prints one JSON line.
 
 Besides the headline, the line carries per-format GEMV timings at the other
-configurations (trellis 12288x4096 and 4096x12288, Leech 17408x5120 and
+workloads (trellis 12288x4096 and 4096x12288, Leech 17408x5120 and
 5120x17408, the fp16 control and the no-weights control at the 8B shapes),
 each cycling enough distinct copies of its matrix to exceed L2 several times.
 
 --impl reference times the CPU oracle (decode + f64 matvec) on a bounded
 sample of the same workload and reports the same metric.
 
-The JSON line ends with the other configurations, compact (lists are
+The JSON line ends with the other workloads, compact (lists are
 [us or ms, GB/s or tok/s, fraction of the measured HBM bandwidth]):
   "stack8b":  the 8B stack at 1, 4 and 16 tokens  [ms/step, tok/s, frac]
   "sweep14b": the 14B stack (40 layers, 4 distinct layer copies cycled) per
@@ -147,21 +147,22 @@ def _job_value(ws: int, ntok: int, steps: int, ms: float) -> float:
     return ws * ntok * steps / (ms / 1e3)
 
 
-def build_stack(q2, ntok: int, config: int = 1):
+def build_stack(q2, ntok: int, seed0: int = 1000):
     """36 layers x 4 BPDQ linears with distinct seeded weights.  The inputs
     are one seeded activation per projection (qkv, o, gate_up, down), shared
     by the 36 layers as an inference engine's activation buffers are: every
     layer's projection reads the same buffer, which therefore stays in L2
     (as the output of the kernel before it would be) while the weights
-    stream from HBM."""
+    stream from HBM.  Seeds: seed0 + 4*layer + projection for the weights,
+    seed0 + 900 + projection for the activations."""
     import torch
     import synth
-    xs = {name: torch.from_numpy(synth.activations(ntok, C, 1000 * config + 900 + j)).cuda()
+    xs = {name: torch.from_numpy(synth.activations(ntok, C, seed0 + 900 + j)).cuda()
           for j, (name, R, C) in enumerate(SHAPES_8B)}
     lin = []
     for layer in range(LAYERS):
         for j, (name, R, C) in enumerate(SHAPES_8B):
-            seed = 1000 * config + 4 * layer + j
+            seed = seed0 + 4 * layer + j
             d = synth.bpdq(R, C, seed)
             blob = q2.q2_pack_bpdq(d["plane0"], d["plane1"], d["coef"])
             del d
@@ -311,7 +312,7 @@ def _leech_pool_matrix(R: int, C: int, seed: int, pool: np.ndarray) -> dict:
 
 
 def sweep14b(q2, stream, formats, ntoks, distinct: int, steps: int, hbm: float) -> dict:
-    """Config 4: the Qwen3-14B-shaped stack (40 layers x qkv/o/gate_up/down)
+    """The Qwen3-14B-shaped stack (40 layers x qkv/o/gate_up/down)
     per format at each token count; `distinct` layer copies are cycled
     through the 40 layers (their footprint is several times L2).  Returns
     {fmt: {ntok: [ms/step, tok/s, frac of HBM]}}; "cublas" is torch.matmul
@@ -393,7 +394,7 @@ def sweep14b(q2, stream, formats, ntoks, distinct: int, steps: int, hbm: float) 
 
 
 def sweep(args):
-    """--sweep: config 4 over the formats and token counts given on the command line."""
+    """--sweep: the Qwen3-14B-shaped stack over the formats and token counts given on the command line."""
     import torch
     import dequant_gemv_q2_gb300 as q2
     q2.load()
@@ -407,8 +408,9 @@ def sweep(args):
                       "distinct_layer_copies": args.sweep_distinct, "results": res}), flush=True)
 
 
-# Oracle cases timed on the host cores: configs 0, 2 and 3 per GEMV, and the
-# four 8B projections (config 1: one layer, times 36 for the step).
+# Oracle cases timed on the host cores, per GEMV: BPDQ 1024x1024, the trellis
+# and Leech shapes, and the four Qwen3-8B projections (one layer; the stack
+# step is 36 times their sum).
 CPU_CASES = [("bpdq_1024x1024", "bpdq", 1024, 1024),
              ("trellis_12288x4096", "trellis", 12288, 4096), ("trellis_4096x12288", "trellis", 4096, 12288),
              ("leech_17408x5120", "leech", 17408, 5120), ("leech_5120x17408", "leech", 5120, 17408)] + \

@@ -271,7 +271,7 @@ def test_noweights_control_runs(q2):
     assert torch.isfinite(y1.float()).all() and torch.equal(y1, y2)
 
 
-# ------------------------------------------------------ full-size configs
+# ------------------------------------------------------- full-size shapes
 def _sampled_rows(R, n=96, seed=0):
     rng = np.random.default_rng(seed)
     rows = np.sort(rng.choice(R, size=min(n, R), replace=False))

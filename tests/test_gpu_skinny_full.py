@@ -1,6 +1,6 @@
 """Parity of the skinny path at the full sizes of the benchmarks: the
 Qwen3-14B stack's shapes (qkv 7168x5120, gate_up 34816x5120, down
-5120x17408) and the trellis and Leech configurations, at 3, 16 and 64
+5120x17408), trellis 12288x4096 / 4096x12288 and Leech 17408x5120, at 3, 16 and 64
 tokens, in the launch configurations the sweep times (tensor-core path with
 its K split and reduction; BPDQ at 3 tokens as a token pair plus a single
 token).  The oracle computes sampled rows only.  Tolerance as everywhere:
