@@ -561,7 +561,8 @@ def stack_weights() -> int:
 def profile_case(fmt: str, launches: int = 4, ntok: int = 1):
     """A few launches of one layer-shaped matrix per format, for ncu captures
     (no timing): bpdq 24576x4096 and 4096x12288, trellis 12288x4096, leech
-    17408x5120, fp16 4096x4096, noweights 24576x4096; rotate: the activation
+    17408x5120 in the three-plane then the offset-binary layout, fp16
+    4096x4096, noweights 24576x4096; rotate: the activation
     rotation at widths 17408 and 4096."""
     import torch
     import dequant_gemv_q2_gb300 as q2
@@ -577,7 +578,8 @@ def profile_case(fmt: str, launches: int = 4, ntok: int = 1):
         mats.append((q2.q2_pack_trellis(d["stream"], d["table"], d["scale"]), 4096))
     elif fmt == "leech":
         d = synth.leech(17408, 5120, 3001)
-        mats.append((q2.q2_pack_leech(d["v"], d["tail"], d["scale"], 5120), 5120))
+        for lay in (q2.LEECH_PLANES3, q2.LEECH_OFFSET4):
+            mats.append((q2.q2_pack_leech(d["v"], d["tail"], d["scale"], 5120, layout=lay), 5120))
     elif fmt == "fp16":
         mats.append((q2.q2_pack_fp16(np.zeros((4096, 4096), dtype=np.float16)), 4096))
     elif fmt == "noweights":
