@@ -52,7 +52,6 @@ struct B1 {
   unsigned long long* acc;      // [ntok][Rpad] accumulator words (zero between calls)
   float fscale, finv;           // 2^F and 2^-F of the fixed-point partials
   int R, C, Rpad, nrb, nslice, ntok;
-  int aligned;                  // 1: slice-aligned CTA ranges, 0: equal contiguous ranges
   q2_pf pf;                     // weights of later launches to fetch into L2 (zero lengths: none)
 };
 
@@ -214,32 +213,13 @@ __device__ __forceinline__ void acc_settle(Pending<NT>& pd, const B1& c, const F
 }
 
 // ------------------------------------------------------- work split
-// The CTA's contiguous range [i0, i1) of items in slice-major order.
-// Equal shares (c.aligned == 0) balance the item counts, but a CTA whose
-// share crosses a slice boundary builds a second table.  Slice-aligned
-// shares (c.aligned == 1): with at least as many CTAs as slices, slice g
-// gets the CTAs b with floor(b*ns/G) == g (floor(G/ns) or ceil(G/ns) of
-// them), which split its nrb row blocks evenly, so no CTA builds a second
-// table; with fewer CTAs than slices, each CTA takes whole slices
-// [floor(b*ns/G), floor((b+1)*ns/G)).  BPDQ items are cheap enough that the
-// second table costs more than the few extra items of the aligned split;
-// Leech and trellis items are not (measured on GB300).
+// The CTA's contiguous range [i0, i1) of items in slice-major order: equal
+// shares of all items (the Leech and trellis kernels).  A share that crosses
+// a slice boundary builds a second table; their items are heavy enough that
+// balancing the counts pays more (measured on GB300).  The BPDQ kernels
+// split by slice instead (make_lean).
 __device__ __forceinline__ void b1_range(const B1& c, int& i0, int& i1) {
-  // 32-bit arithmetic throughout (b*ns <= 152*255, k*nrb <= 152*16384): the
-  // 64-bit divisions this replaces cost close to a microsecond of prologue
-  const int G = gridDim.x, b = blockIdx.x, ns = c.nslice, nrb = c.nrb;
-  if (!c.aligned) {
-    cta_range(ns * nrb, i0, i1);
-  } else if (ns <= G) {
-    const int g = b * ns / G;
-    const int first = (g * G + ns - 1) / ns, last = ((g + 1) * G + ns - 1) / ns;
-    const int k = b - first, kc = last - first;
-    i0 = g * nrb + k * nrb / kc;
-    i1 = g * nrb + (k + 1) * nrb / kc;
-  } else {
-    i0 = b * ns / G * nrb;
-    i1 = (b + 1) * ns / G * nrb;
-  }
+  cta_range(c.nslice * c.nrb, i0, i1);
 }
 
 // This CTA's 1/grid share of each range in c.pf, fetched into L2 by one
@@ -477,8 +457,8 @@ __global__ void __launch_bounds__(W * 32, 1) k_leech_b1(LeechArgs a) {
 // 24576x4096 GEMV whose weights are all in L2 is no faster than one
 // reading them from HBM):
 //   - the CTA's item range comes from the host in the parameter block
-//     (the slice-aligned split of run_b1's b1_range, computed once per
-//     launch), so no warp spends its prologue on integer divisions;
+//     (a slice-aligned split, make_lean), so no warp spends its prologue on
+//     integer divisions;
 //   - each warp walks its items with pointers advanced by a constant
 //     stride instead of recomputing 64-bit addresses per item;
 //   - the lookups of plane 0 and plane 1 at the same rotated position are
@@ -1089,7 +1069,6 @@ B1 make_b1(const q2_handle* h, const void* x, void* y, int ntok, const q2_pf* pf
   B1 c;
   if (pf) c.pf = *pf;
   else c.pf = q2_pf{};
-  c.aligned = (d.fmt == Q2_BPDQ || d.fmt == Q2_NOWEIGHTS) ? 1 : 0;
   c.x = static_cast<const __half*>(x);
   c.y = static_cast<__half*>(y);
   c.acc = static_cast<unsigned long long*>(h->ws);
@@ -1116,7 +1095,16 @@ int launch1(void (*kernel)(A), const A& args, const Geo& g, int threads, int tab
 }
 
 // The lean single-token kernel's arguments: the pointers and scalars of
-// make_b1, and each CTA's slice-aligned item range (b1_range, aligned mode).
+// make_b1, and each CTA's item range.  The split is slice-aligned, so no CTA
+// builds a second table (BPDQ items are cheap enough that a second table
+// costs more than the few extra items this leaves on some CTAs).  With at
+// least as many CTAs as slices, slice g gets CTAs [floor(g*G/ns),
+// floor((g+1)*G/ns)), floor(G/ns) or ceil(G/ns) of them, which split its nrb
+// row blocks evenly; the last slice gets the larger count, so the CTAs with
+// the highest indices, which start last (the previous launch frees their
+// SMs last), get the fewer items (Qwen3-8B stack on GB300: 651.4 against
+// 655.3 us per step with the larger counts first).  With fewer CTAs than
+// slices, each CTA takes whole slices [floor(b*ns/G), floor((b+1)*ns/G)).
 LeanArgs make_lean(const q2_handle* h, const void* x, void* y, const q2_pf* pf, int grid) {
   const q2_blob_header& d = h->hdr;
   const B1 c = make_b1(h, x, y, 1, pf);
@@ -1139,16 +1127,13 @@ LeanArgs make_lean(const q2_handle* h, const void* x, void* y, const q2_pf* pf, 
   a.pfq = (uint32_t)(units / parts);
   a.pfr = (uint32_t)(units % parts);
   const int ns = c.nslice, nrb = c.nrb, G = grid;
-  for (int b = 0; b < G; ++b) {
-    int i0;
-    if (ns <= G) {
-      const int g = b * ns / G;
-      const int first = (g * G + ns - 1) / ns, last = ((g + 1) * G + ns - 1) / ns;
-      i0 = g * nrb + (b - first) * nrb / (last - first);
-    } else {
-      i0 = b * ns / G * nrb;
+  if (ns <= G) {
+    for (int g = 0; g < ns; ++g) {
+      const int f0 = g * G / ns, f1 = (g + 1) * G / ns, n = f1 - f0;
+      for (int k = 0; k < n; ++k) a.start[f0 + k] = (uint32_t)(g * nrb + k * nrb / n);
     }
-    a.start[b] = (uint32_t)i0;
+  } else {
+    for (int b = 0; b < G; ++b) a.start[b] = (uint32_t)(b * ns / G * nrb);
   }
   a.start[G] = (uint32_t)(ns * nrb);
   return a;
