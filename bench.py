@@ -16,16 +16,16 @@ each cycling enough distinct copies of its matrix to exceed L2 several times.
 --impl reference times the CPU oracle (decode + f64 matvec) on a bounded
 sample of the same workload and reports the same metric.
 
-The JSON line ends with the other workloads, compact (lists are
-[us or ms, GB/s or tok/s, fraction of the measured HBM bandwidth]):
+The JSON line ends with the other workloads, compact, so that they survive
+a tail of the output ("frac" is the fraction of the measured HBM bandwidth):
   "stack8b":  the 8B stack at 1, 4 and 16 tokens  [ms/step, tok/s, frac]
   "sweep14b": the 14B stack (40 layers, 4 distinct layer copies cycled) per
-              format at 1, 16 and 64 tokens        [ms/step, tok/s, frac]
+              format, tok/s at each count of "ntok" (1, 2, 4, 8, 16, 32,
+              64); "frac1": each format's frac at one token
   "fmt":      single GEMVs at batch 1 per format and shape, each cycling
-              copies of its matrix over >= 4x L2   [us, GB/s, frac]
+              copies of its matrix over >= 4x L2   [us, frac]
   "rot":      activation rotation us at 1 and 64 tokens, and the 8B stack
               with every input rotated first
-so that they survive a tail of the output.
 """
 from __future__ import annotations
 
@@ -46,6 +46,7 @@ METRIC = "batch-1 GEMV µs and achieved HBM GB/s (% of byte bound) per format; d
 HIDDEN, QKV, INTER, LAYERS = 4096, 6144, 12288, 36
 SHAPES_8B = [("qkv", QKV, HIDDEN), ("o", HIDDEN, HIDDEN), ("gate_up", 2 * INTER, HIDDEN), ("down", HIDDEN, INTER)]
 L2_BYTES = 126 * 1024 * 1024
+SWEEP_NTOK = [1, 2, 4, 8, 16, 32, 64]     # token counts of the Qwen3-14B-shaped stack sweep
 
 # DRAM traffic of the dominant kernel per launch, as a ratio to its
 # algorithmic bytes, from an ncu capture (dram__bytes_read.sum +
@@ -760,9 +761,13 @@ def main():
         rot["stack_ms"] = round(rms, 4)
         del lin, g, xbuf, ybuf, wsbuf, xv, yv
         torch.cuda.empty_cache()
-        extras["sweep14b"] = sweep14b(q2, stream, ["bpdq", "trellis", "leech", "cublas"], [1, 16, 64], 4, 10, hbm)
-        extras["sweep14b"]["fp16"] = sweep14b(q2, stream, ["fp16"], [1, 16, 64], 4, 10, hbm)["fp16"]
-        extras["fmt"] = per_format(q2, stream, hbm)
+        sw = sweep14b(q2, stream, ["bpdq", "trellis", "leech", "cublas"], SWEEP_NTOK, 4, 10, hbm)
+        sw["fp16"] = sweep14b(q2, stream, ["fp16"], SWEEP_NTOK, 4, 10, hbm)["fp16"]
+        # compact: tok/s per format at each token count, and batch 1's fraction of HBM
+        extras["sweep14b"] = {"ntok": SWEEP_NTOK,
+                              **{f: [sw[f][str(nt)][1] for nt in SWEEP_NTOK] for f in sw},
+                              "frac1": {f: sw[f]["1"][2] for f in sw}}
+        extras["fmt"] = {k: [v[0], v[2]] if len(v) == 3 else v for k, v in per_format(q2, stream, hbm).items()}
         extras["rot"] = rot
 
     achieved = step_bytes / (ms_step * 1e-3) / 1e9
