@@ -177,6 +177,26 @@ __device__ __forceinline__ float plane_sum(uint32_t lane4, const uint4& c0, cons
   return (s[0] + s[1]) + (s[2] + s[3]);
 }
 
+// Lookup P of both planes into pair accumulator P mod 4, then the rest.
+template <int P>
+__device__ __forceinline__ void pair_steps(uint32_t lane4, const uint32_t (&w0)[8], const uint32_t (&w1)[8],
+                                           float2 (&s)[4]) {
+  if constexpr (P < 32) {
+    s[P & 3] = __fadd2_rn(s[P & 3], make_float2(tl<P>(lane4, w0[P >> 2]), tl<P>(lane4, w1[P >> 2])));
+    pair_steps<P + 1>(lane4, w0, w1, s);
+  }
+}
+
+// (sum of plane 0's 32 lookups, sum of plane 1's)
+__device__ __forceinline__ float2 planes_sum(uint32_t lane4, const uint4& a0, const uint4& a1, const uint4& b0,
+                                             const uint4& b1) {
+  const uint32_t w0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+  const uint32_t w1[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+  float2 s[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  pair_steps<0>(lane4, w0, w1, s);
+  return __fadd2_rn(__fadd2_rn(s[0], s[1]), __fadd2_rn(s[2], s[3]));
+}
+
 // Atomics a lane has issued for one item (NT tokens), settled one item later
 // so the atomic's round trip overlaps the next item's work.
 template <int NT>
@@ -404,8 +424,8 @@ struct LeechF {
   }
   __device__ void compute(int, int g, int lane, const Item& b, float (&p)[1]) const {
     const uint32_t lane4 = (uint32_t)lane * 4u | kLane4Hi;
-    const float P0 = plane_sum(lane4, b.w[0], b.w[1]);
-    const float P1 = plane_sum(lane4, b.w[2], b.w[3]);
+    const float2 P01 = planes_sum(lane4, b.w[0], b.w[1], b.w[2], b.w[3]);   // same sums as plane_sum, paired
+    const float P0 = P01.x, P1 = P01.y;
     const float P2 = plane_sum(lane4, b.w[4], b.w[5]);
     int bfirst, nbk;
     leech_blocks(g, a.nblock, bfirst, nbk);
@@ -502,26 +522,6 @@ struct LeanItem {
   uint32_t c01;
   unsigned short off;
 };
-
-// Lookup P of both planes into pair accumulator P mod 4, then the rest.
-template <int P>
-__device__ __forceinline__ void pair_steps(uint32_t lane4, const uint32_t (&w0)[8], const uint32_t (&w1)[8],
-                                           float2 (&s)[4]) {
-  if constexpr (P < 32) {
-    s[P & 3] = __fadd2_rn(s[P & 3], make_float2(tl<P>(lane4, w0[P >> 2]), tl<P>(lane4, w1[P >> 2])));
-    pair_steps<P + 1>(lane4, w0, w1, s);
-  }
-}
-
-// (sum of plane 0's 32 lookups, sum of plane 1's)
-__device__ __forceinline__ float2 planes_sum(uint32_t lane4, const uint4& a0, const uint4& a1, const uint4& b0,
-                                             const uint4& b1) {
-  const uint32_t w0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-  const uint32_t w1[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-  float2 s[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-  pair_steps<0>(lane4, w0, w1, s);
-  return __fadd2_rn(__fadd2_rn(s[0], s[1]), __fadd2_rn(s[2], s[3]));
-}
 
 template <bool kWeights>
 __device__ __forceinline__ void lean_load(const uint32_t* c01, const unsigned short* off, const uint4* wp, size_t ci,
